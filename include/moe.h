@@ -1,0 +1,229 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) fused Mixture-of-Experts layer.
+ *
+ * The layer computes, for every token t of a batch,
+ *
+ *   out[t] = sum_j  w[t,j] * W2[e_j] * ( SiLU(x_t . Wgate[e_j]^T) (.) (x_t . Wup[e_j]^T) ),
+ *   e_j = topk_ids[t,j],  Wgate[e] = W13[e, 0:I, :],  Wup[e] = W13[e, I:2I, :],
+ *
+ * as the pipeline that the "HPC-Ops × SGLang" post (LMSYS blog, section "MoE:
+ * reducing the overhead around small expert GEMMs") describes: a routing/index
+ * build, a Gate-Up GEMM that reads token rows through the index, a fused
+ * SiLU-and-mul (+ FP8 requantisation), a Down GEMM, and a top-k weighted
+ * reduction back to token order, chained with Programmatic Dependent Launch.
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; tensors are
+ *     dense and row-major.  The library never allocates, frees or synchronises
+ *     inside these calls (the one set-up exception is noted where it applies).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Host-side argument checks happen before anything is launched and return
+ *     a moe_status other than MOE_OK; nothing is enqueued in that case.
+ *   - `dev_status` (nullable) is a device int32 that kernels OR bit flags into:
+ *     bit (1 << MOE_ERR_EXPERT_ID) when a top-k id lies outside [0, E) (that
+ *     assignment is dropped and contributes 0), bit (1 << MOE_ERR_TIMEOUT) when
+ *     a bounded on-chip wait gave up.  moe_align / moe_forward clear it to 0 at
+ *     the start of their first kernel.  Read it after your own synchronisation.
+ *   - A launch error reported by the CUDA runtime maps to MOE_ERR_CUDA.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = 1,        /* null pointer or bad enum value */
+  MOE_ERR_SHAPE = 2,      /* unsupported or inconsistent sizes */
+  MOE_ERR_DTYPE = 3,      /* unsupported mode / output dtype */
+  MOE_ERR_ALIGN = 4,      /* pointer not 16-byte aligned */
+  MOE_ERR_WORKSPACE = 5,  /* workspace too small */
+  MOE_ERR_EXPERT_ID = 6,  /* device flag: an id outside [0, E) was dropped */
+  MOE_ERR_TIMEOUT = 7,    /* device flag: a bounded wait gave up */
+  MOE_ERR_CUDA = 8        /* CUDA runtime / driver error */
+} moe_status;
+
+typedef enum { MOE_BF16 = 0, MOE_FP8_W8A8 = 1 } moe_mode;
+typedef enum { MOE_OUT_F32 = 0, MOE_OUT_BF16 = 1 } moe_out;
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+
+/* Problem sizes.  T tokens, hidden size H, intermediate size I, E experts,
+ * top-k = k.  block_m is the row-tile height of the index and of both expert
+ * GEMMs (the token tile): 0 lets the planner choose, otherwise one of
+ * 16, 32, 64, 128, 256 (FP8: at most 128).
+ * Supported: T >= 1, 1 <= k <= E <= 512, H % 128 == 0, I % 64 == 0
+ * (FP8: I % 128 == 0), T*k < 2^31. */
+typedef struct {
+  int32_t T, H, I, E, k;
+  int32_t block_m;
+  int32_t mode;       /* moe_mode */
+  int32_t out_dtype;  /* moe_out */
+} moe_shape;
+
+/* The routing index ("routing and index build", HPC-Ops × SGLang, section MoE).
+ * Every field is a caller-owned device buffer.  With a = t*k + j the flat
+ * assignment number, Tk = T*k, bm = block_m:
+ *   counts[E]        assignments per expert (invalid ids not counted)
+ *   offsets[E+1]     exclusive prefix of counts rounded up to multiples of bm
+ *   sorted_ids[rows_cap]   expert e's interval [offsets[e], offsets[e+1])
+ *                    holds its assignments a in ascending order, then the
+ *                    sentinel Tk; every row from offsets[E] on holds Tk
+ *   tile_expert[tiles_cap] expert of row tile q (rows q*bm .. q*bm+bm-1), -1
+ *                    for q >= num_tiles
+ *   tiles[tiles_cap][4]    task map {expert, row_start, rows_valid, 0};
+ *                    {-1, q*bm, 0, 0} for q >= num_tiles
+ *   inv_pos[Tk]      row that holds assignment a, -1 if its id was invalid
+ *   num_tiles[1]     offsets[E] / bm
+ * with tiles_cap = ceil(Tk/bm) + min(E, Tk) and rows_cap = tiles_cap*bm. */
+typedef struct {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_ids;
+  int32_t* tile_expert;
+  int32_t* tiles;
+  int32_t* inv_pos;
+  int32_t* num_tiles;
+} moe_index;
+
+/* FP8 block scales (FP8 mode only): one fp32 per 128x128 weight block, so that
+ * W13 ~= e4m3(W13q) * w13_scale[e][row/128][col/128]
+ * ("block_shape [128, 128]", SGLang MoE Triton tuning guide, section 4.1). */
+typedef struct {
+  const float* w13_scale;  /* [E][2I/128][H/128] */
+  const float* w2_scale;   /* [E][H/128][I/128]  */
+} moe_scales;
+
+/* Options of moe_forward_ex (zero-initialised = defaults of moe_forward). */
+typedef struct {
+  int32_t disable_pdl;      /* 1: plain stream order instead of PDL chaining */
+  int32_t split_gateup;     /* 0: planner; else forced split-K count, Gate-Up */
+  int32_t split_down;       /* 0: planner; else forced split-K count, Down    */
+  int32_t grid_ctas;        /* 0: planner; else CTAs of the persistent GEMMs  */
+  /* Optional cudaEvent_t handles recorded on `stream` before stage s
+   * (0 align, 1 x-quant, 2 Gate-Up, 3 act, 4 Down, 5 combine) and after the
+   * last one (index 6).  NULL entries are skipped.  Recording events between
+   * stages serialises them (PDL overlap is lost); use for profiling only. */
+  void* stage_events[8];
+} moe_forward_opts;
+
+/* Where moe_forward keeps its intermediates inside the caller's workspace
+ * (byte offsets from the workspace base) and the plan it runs. */
+typedef struct {
+  int32_t block_m, tiles_cap, rows_cap;
+  int32_t split_gateup, split_down;    /* split-K counts S1, S2 */
+  int32_t grid_gateup, grid_down;      /* persistent CTAs per GEMM */
+  int32_t reserved;
+  size_t off_counts, off_offsets, off_sorted_ids, off_tile_expert, off_tiles,
+      off_inv_pos, off_num_tiles;
+  size_t off_xq;   /* FP8: e4m3 x            [T][H]                         */
+  size_t off_xs;   /* FP8: fp32 x scales     [T][H/128]                     */
+  size_t off_g;    /* fp32 Gate-Up partials  [S1][rows_cap][2I]             */
+  size_t off_a;    /* activation: bf16 [rows_cap][I] or e4m3 [rows_cap][I]  */
+  size_t off_as;   /* FP8: fp32 act scales   [rows_cap][I/128]              */
+  size_t off_y;    /* fp32 Down partials     [S2][rows_cap][H] (sorted rows)*/
+  size_t total_bytes;
+} moe_workspace_layout;
+
+/* tiles_cap of the index for these sizes (0 on invalid arguments). */
+size_t moe_index_tiles_cap(int32_t T, int32_t k, int32_t E, int32_t block_m);
+
+/* Resolve the plan moe_forward(_ex) will run for `shape` (opts nullable) and
+ * the layout of its workspace.  Pure host computation. */
+moe_status moe_plan(const moe_shape* shape, const moe_forward_opts* opts,
+                    moe_workspace_layout* layout);
+
+/* Workspace bytes moe_forward(_ex) needs (0 on invalid arguments). */
+size_t moe_workspace_bytes(const moe_shape* shape, const moe_forward_opts* opts);
+
+/* Routing and index build ("routing and index build", HPC-Ops × SGLang,
+ * section MoE): a shared-memory counting pass and scan that place every
+ * assignment a = t*k + j of topk_ids[T][k] (int32) into its expert's
+ * contiguous interval, stable in a, with no global atomics on the ordering
+ * path; also writes the per-tile task map.  Layout of every output: moe_index.
+ * block_m must be one of 16, 32, 64, 128, 256.  Invalid ids are dropped and
+ * flagged in dev_status.  Errors: MOE_ERR_ARG (null idx field / topk_ids),
+ * MOE_ERR_SHAPE (sizes), MOE_ERR_CUDA. */
+moe_status moe_align(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+                     int32_t block_m, const moe_index* idx, int32_t* dev_status,
+                     void* stream);
+
+/* The whole layer.  Inputs:
+ *   x        bf16 [T][H]
+ *   w13      bf16 [E][2I][H] (FP8: e4m3 bytes), rows 0..I-1 gate, I..2I-1 up
+ *   w2       bf16 [E][H][I]  (FP8: e4m3 bytes)
+ *   topk_ids int32 [T][k];  topk_w fp32 [T][k] (used as given)
+ *   scales   FP8 only (NULL in BF16 mode)
+ *   out      [T][H], fp32 or bf16 per shape->out_dtype
+ *   workspace, ws_bytes  >= moe_workspace_bytes(shape, NULL), 256-byte aligned
+ * FP8 mode quantises x per token per 128 channels (s = amax/448, 1 if amax is
+ * 0; q = e4m3 RNE-satfinite(x/s)) and the activation per row per 128 channels
+ * by the same rule.  Stages: align, [x-quant], Gate-Up, act, Down, combine,
+ * launched on `stream` with PDL.  Errors: MOE_ERR_ARG, MOE_ERR_SHAPE,
+ * MOE_ERR_DTYPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ * The first call on a device (per weight-pointer set) encodes TMA descriptors
+ * on the host; nothing is allocated. */
+moe_status moe_forward(const moe_shape* shape, const void* x, const void* w13,
+                       const void* w2, const int32_t* topk_ids,
+                       const float* topk_w, const moe_scales* scales, void* out,
+                       void* workspace, size_t ws_bytes, int32_t* dev_status,
+                       void* stream);
+
+/* moe_forward with options (opts nullable = defaults).  The workspace must be
+ * sized with the same opts. */
+moe_status moe_forward_ex(const moe_shape* shape, const void* x,
+                          const void* w13, const void* w2,
+                          const int32_t* topk_ids, const float* topk_w,
+                          const moe_scales* scales, void* out, void* workspace,
+                          size_t ws_bytes, int32_t* dev_status, void* stream,
+                          const moe_forward_opts* opts);
+
+/* Top-k weighted reduction back to token order (HPC-Ops × SGLang, section MoE,
+ * "PDL-chained stages": the final top-k weighted reduce):
+ *   out[t][h] = sum_{j=0..k-1, ascending} topk_w[t][j] *
+ *               sum_{s=0..splits-1, ascending} y[s][inv_pos[t*k+j]][h]
+ * in fp32, assignments with inv_pos = -1 contributing 0; no atomics, so the
+ * result is bitwise reproducible.  y is fp32 [splits][rows_cap][H] in sorted
+ * (expert-grouped) row order.  out is [T][H] fp32 or bf16 (shape->out_dtype);
+ * only shape->T, H, k, out_dtype are read.  Errors: MOE_ERR_ARG,
+ * MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_CUDA. */
+moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t rows_cap,
+                       const float* y, const int32_t* inv_pos,
+                       const float* topk_w, void* out, void* stream);
+
+/* Router weight preparation ("a precision-aware BF16 formulation", HPC-Ops ×
+ * SGLang, section Router GEMM): from fp32 wr[E][H] writes bf16
+ * hi_lo[2E][H]: rows 0..E-1 hi = wr truncated to bf16, rows E..2E-1
+ * lo = bf16_rne((wr - hi) * 256).  Run once per weight set (untimed prep).
+ * Errors: MOE_ERR_ARG, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_CUDA. */
+moe_status moe_router_prepare(const float* wr, int32_t E, int32_t H,
+                              void* hi_lo, void* stream);
+
+/* Workspace bytes moe_router_topk needs (0 on invalid arguments). */
+size_t moe_router_workspace_bytes(int32_t T, int32_t H, int32_t E);
+
+/* Router GEMM + top-k: scores[t][e] = sum_h x[t][h]*hi[e][h]
+ *   + (sum_h x[t][h]*lo[e][h]) / 256, fp32 accumulation on the tensor cores,
+ * written fp32 [T][E]; then p = softmax over e (score_fn 0) or sigmoid
+ * (score_fn 1); the k largest scores (ties -> lower e) give topk_ids int32
+ * [T][k] (descending score) and topk_w fp32 [T][k] = scale * p_j / sum p_sel.
+ * x bf16 [T][H]; H % 128 == 0, 1 <= k <= E, E % 64 == 0, E <= 512.
+ * Errors: MOE_ERR_ARG, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,
+ * MOE_ERR_CUDA. */
+moe_status moe_router_topk(const void* x, const void* hi_lo, int32_t T,
+                           int32_t H, int32_t E, int32_t k, int32_t score_fn,
+                           float scale, float* scores, int32_t* topk_ids,
+                           float* topk_w, void* workspace, size_t ws_bytes,
+                           void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_str(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */
