@@ -32,6 +32,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -130,15 +136,15 @@ typedef struct {
 } moe_workspace_layout;
 
 /* tiles_cap of the index for these sizes (0 on invalid arguments). */
-size_t moe_index_tiles_cap(int32_t T, int32_t k, int32_t E, int32_t block_m);
+MOE_API size_t moe_index_tiles_cap(int32_t T, int32_t k, int32_t E, int32_t block_m);
 
 /* Resolve the plan moe_forward(_ex) will run for `shape` (opts nullable) and
  * the layout of its workspace.  Pure host computation. */
-moe_status moe_plan(const moe_shape* shape, const moe_forward_opts* opts,
+MOE_API moe_status moe_plan(const moe_shape* shape, const moe_forward_opts* opts,
                     moe_workspace_layout* layout);
 
 /* Workspace bytes moe_forward(_ex) needs (0 on invalid arguments). */
-size_t moe_workspace_bytes(const moe_shape* shape, const moe_forward_opts* opts);
+MOE_API size_t moe_workspace_bytes(const moe_shape* shape, const moe_forward_opts* opts);
 
 /* Routing and index build ("routing and index build", HPC-Ops × SGLang,
  * section MoE): a shared-memory counting pass and scan that place every
@@ -148,7 +154,7 @@ size_t moe_workspace_bytes(const moe_shape* shape, const moe_forward_opts* opts)
  * block_m must be one of 16, 32, 64, 128, 256.  Invalid ids are dropped and
  * flagged in dev_status.  Errors: MOE_ERR_ARG (null idx field / topk_ids),
  * MOE_ERR_SHAPE (sizes), MOE_ERR_CUDA. */
-moe_status moe_align(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+MOE_API moe_status moe_align(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                      int32_t block_m, const moe_index* idx, int32_t* dev_status,
                      void* stream);
 
@@ -167,7 +173,7 @@ moe_status moe_align(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
  * MOE_ERR_DTYPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
  * The first call on a device (per weight-pointer set) encodes TMA descriptors
  * on the host; nothing is allocated. */
-moe_status moe_forward(const moe_shape* shape, const void* x, const void* w13,
+MOE_API moe_status moe_forward(const moe_shape* shape, const void* x, const void* w13,
                        const void* w2, const int32_t* topk_ids,
                        const float* topk_w, const moe_scales* scales, void* out,
                        void* workspace, size_t ws_bytes, int32_t* dev_status,
@@ -175,7 +181,7 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w13,
 
 /* moe_forward with options (opts nullable = defaults).  The workspace must be
  * sized with the same opts. */
-moe_status moe_forward_ex(const moe_shape* shape, const void* x,
+MOE_API moe_status moe_forward_ex(const moe_shape* shape, const void* x,
                           const void* w13, const void* w2,
                           const int32_t* topk_ids, const float* topk_w,
                           const moe_scales* scales, void* out, void* workspace,
@@ -191,7 +197,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x,
  * (expert-grouped) row order.  out is [T][H] fp32 or bf16 (shape->out_dtype);
  * only shape->T, H, k, out_dtype are read.  Errors: MOE_ERR_ARG,
  * MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_CUDA. */
-moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t rows_cap,
+MOE_API moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t rows_cap,
                        const float* y, const int32_t* inv_pos,
                        const float* topk_w, void* out, void* stream);
 
@@ -200,11 +206,11 @@ moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t rows_cap,
  * hi_lo[2E][H]: rows 0..E-1 hi = wr truncated to bf16, rows E..2E-1
  * lo = bf16_rne((wr - hi) * 256).  Run once per weight set (untimed prep).
  * Errors: MOE_ERR_ARG, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_CUDA. */
-moe_status moe_router_prepare(const float* wr, int32_t E, int32_t H,
+MOE_API moe_status moe_router_prepare(const float* wr, int32_t E, int32_t H,
                               void* hi_lo, void* stream);
 
 /* Workspace bytes moe_router_topk needs (0 on invalid arguments). */
-size_t moe_router_workspace_bytes(int32_t T, int32_t H, int32_t E);
+MOE_API size_t moe_router_workspace_bytes(int32_t T, int32_t H, int32_t E);
 
 /* Router GEMM + top-k: scores[t][e] = sum_h x[t][h]*hi[e][h]
  *   + (sum_h x[t][h]*lo[e][h]) / 256, fp32 accumulation on the tensor cores,
@@ -214,14 +220,14 @@ size_t moe_router_workspace_bytes(int32_t T, int32_t H, int32_t E);
  * x bf16 [T][H]; H % 128 == 0, 1 <= k <= E, E % 64 == 0, E <= 512.
  * Errors: MOE_ERR_ARG, MOE_ERR_SHAPE, MOE_ERR_ALIGN, MOE_ERR_WORKSPACE,
  * MOE_ERR_CUDA. */
-moe_status moe_router_topk(const void* x, const void* hi_lo, int32_t T,
+MOE_API moe_status moe_router_topk(const void* x, const void* hi_lo, int32_t T,
                            int32_t H, int32_t E, int32_t k, int32_t score_fn,
                            float scale, float* scores, int32_t* topk_ids,
                            float* topk_w, void* workspace, size_t ws_bytes,
                            void* stream);
 
 /* Static description of a status code. */
-const char* moe_status_str(int32_t status);
+MOE_API const char* moe_status_str(int32_t status);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,88 @@
+// internal.h — declarations shared by the translation units of the library
+// (host side).  Not part of the public C ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+// Which rows feed the MMA's token operand.
+enum BSource : int {
+  kGather = 0,  // rows of x picked through sorted_ids (Gate-Up), gate/up paired
+  kDirect = 1,  // rows row_start.. of a row tile (Down reads the activation)
+  kDense = 2,   // rows 0..dense_rows-1 tiled by BN (router GEMM)
+};
+
+struct GemmParams {
+  int M;             // output columns: 2I (Gate-Up), H (Down), 2E (router)
+  int K;             // reduction length in elements
+  int I;             // Gate-Up pairing offset (up rows start at I)
+  int m_tiles;       // 128-row weight tiles per expert
+  int splits;        // split-K count
+  int kt_per_split;  // K tiles (128 bytes of K each) per split
+  int kt_total;      // K tiles in total
+  const int32_t* tiles;      // [tiles_cap][4] task map (gather / direct)
+  const int32_t* num_tiles;  // device scalar (gather / direct)
+  const int32_t* sorted_ids; // gather: row -> assignment
+  int topk;                  // gather: token = assignment / topk
+  int sentinel;              // gather: T*k marks padding rows
+  int dense_rows;            // dense: number of rows
+  const float* w_scale;      // FP8: [E][M/128][K/128]
+  const float* b_scale;      // FP8: gather [T][K/128]; direct [rows_cap][K/128]
+  float* out;                // [splits][rows_cap][M] fp32 partial sums
+  int rows_cap;              // rows of one split slice of `out`
+  int32_t* dev_status;
+};
+
+// Shared memory bytes and pipeline depth of one GEMM instantiation.
+int gemm_stages(int fp8, int bn);
+size_t gemm_smem_bytes(int fp8, int bn, int kt_per_split);
+
+// Launch the persistent GEMM (defined per mode in k_gemm_{bf16,fp8}.cu).
+cudaError_t launch_gemm_bf16(int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
+                             const CUtensorMap& tmA, const CUtensorMap& tmB,
+                             const GemmParams& p);
+cudaError_t launch_gemm_fp8(int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
+                            const CUtensorMap& tmA, const CUtensorMap& tmB,
+                            const GemmParams& p);
+
+// Index build, pointwise stages (k_align.cu, k_pointwise.cu).
+struct IndexPtrs {
+  int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
+};
+cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
+                         const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st,
+                         bool pdl);
+cudaError_t launch_quant_x(const void* x, int T, int H, uint8_t* xq, float* xs,
+                           cudaStream_t st, bool pdl);
+cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
+                       const int32_t* sorted_ids, int sentinel, void* A, float* As,
+                       cudaStream_t st, bool pdl);
+cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H,
+                           const int32_t* inv_pos, const float* topk_w, int T, int k,
+                           void* out, int out_bf16, cudaStream_t st, bool pdl);
+cudaError_t launch_router_prepare(const float* wr, int E, int H, void* hi_lo,
+                                  cudaStream_t st);
+cudaError_t launch_router_topk(const float* P, int splits, int rows_cap, int T, int E,
+                               int k, int score_fn, float scale, float* scores,
+                               int32_t* ids, float* w, cudaStream_t st, bool pdl);
+
+// Launch helper: plain or PDL-chained launch with dynamic shared memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace moe

@@ -1,0 +1,433 @@
+// k_gemm.cuh — persistent grouped expert GEMM on the 5th-generation tensor
+// cores (tcgen05, accumulators in TMEM, operands staged by TMA).
+//
+// Role in the layer (HPC-Ops × SGLang, section "MoE", fused pipeline): the
+// "Gate-Up GEMM reads the original token rows through the routing index" and
+// the Down GEMM is "the same persistent task-map expert GEMM".  The same
+// kernel also runs the router's two-bf16 GEMM (section "Router GEMM").
+//
+// Orientation ("swap-AB"): the MMA's M side is always 128 weight rows, the N
+// side (BN = block_m) is the token tile.  A decode-sized expert group of a
+// few tokens then costs a narrow N, not a padded 128-row M.
+//
+// For weight tile mt, split ks and row tile q (one work unit), with e the
+// tile's expert:
+//   out[ks][row0 + n][col(m)] = sum_{k in split ks} W[e][row(m)][k] * B[n][k]
+// where B[n] is x[sorted_ids[row0+n] / topk] (gather), row row0+n of the
+// activation (direct) or row q*BN+n of x (dense).  Gate-Up pairs the tile:
+// TMEM lanes 0..63 hold gate rows mt*64.., lanes 64..127 the matching up rows
+// I + mt*64.., so a later fused SiLU-and-mul epilogue finds both halves in one
+// tile.  Split-K partial sums are written in fp32 and reduced, in a fixed
+// order, by the next stage (act or combine): nothing is accumulated with
+// atomics.
+//
+// FP8 (e4m3, kind::f8f6f4): every 128-wide K block is its own MMA group into
+// one of two TMEM buffers; the epilogue warps read it and add
+// partial * w_scale[e][row/128][kb] * b_scale[token][kb] into fp32 registers
+// (block scales are fp32, so the product cannot be folded into the MMA).
+//
+// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 (one thread)
+// issues MMAs, warps 2..5 drain TMEM.  With the accumulator in TMEM instead of
+// registers, this split costs no registers, so the Hopper argument for one
+// warp group doing everything ("occupancy first, no warp specialisation")
+// does not carry over.  Every wait is bounded (kWaitLimitNs); on a timeout
+// the kernel ORs kStatusTimeout into dev_status, drains its own copies and
+// MMAs, frees TMEM and returns.
+#pragma once
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int kGemmThreads = 192;
+constexpr int kTileM = 128;                 // weight rows per tile (MMA M)
+constexpr int kKBytes = 128;                // K bytes per pipeline stage
+constexpr int kABytes = kTileM * kKBytes;   // 16 KB weight tile per stage
+
+__host__ __device__ constexpr int stages_for(int fp8, int bn) {
+  return bn <= 32 ? 8 : bn == 64 ? (fp8 ? 7 : 8) : bn == 128 ? (fp8 ? 5 : 6) : 4;
+}
+
+template <int FP8, int BN>
+struct GemmShape {
+  static constexpr int kStages = stages_for(FP8, BN);
+  static constexpr int kBBytes = BN * kKBytes;
+  static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  static constexpr int kElemsPerStage = FP8 ? 128 : 64;
+  static constexpr uint32_t kIdesc = mma_idesc(FP8 ? 0u : 1u, kTileM, BN);
+  static constexpr int kOffB = kStages * kABytes;
+  static constexpr int kOffBar = kOffB + kStages * kBBytes;
+  static constexpr int kNumBars = 2 * kStages + 5;  // full, empty, acc_full[2], acc_empty[2], drain
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr size_t kSmemBytes = 1024 + kOffMisc + 16;
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0");
+};
+
+struct WorkUnit {
+  int mt, ks, e, row0, rows, kt0, kt1;
+};
+
+template <int BN, int BSRC>
+__device__ __forceinline__ WorkUnit decode_unit(int u, int num_tiles, const GemmParams& p) {
+  WorkUnit w;
+  const int q = u % num_tiles;
+  const int r = u / num_tiles;
+  w.ks = r % p.splits;
+  w.mt = r / p.splits;
+  if (BSRC == kDense) {
+    w.e = 0;
+    w.row0 = q * BN;
+    w.rows = min(BN, p.dense_rows - w.row0);
+  } else {
+    const int4 t = __ldg(reinterpret_cast<const int4*>(p.tiles) + q);
+    w.e = t.x;
+    w.row0 = t.y;
+    w.rows = t.z;
+  }
+  w.kt0 = w.ks * p.kt_per_split;
+  w.kt1 = min(p.kt_total, w.kt0 + p.kt_per_split);
+  return w;
+}
+
+__device__ __forceinline__ void report_timeout(const GemmParams& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  if (p.dev_status) atomicOr(p.dev_status, kStatusTimeout);
+}
+
+template <int FP8, int BN, int BSRC>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using S = GemmShape<FP8, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sA = smem_u32(smem);
+  const uint32_t sB = sA + S::kOffB;
+  const uint32_t bar_full = sA + S::kOffBar;
+  const uint32_t bar_empty = bar_full + 8 * S::kStages;
+  const uint32_t bar_accf = bar_empty + 8 * S::kStages;
+  const uint32_t bar_acce = bar_accf + 16;
+  const uint32_t bar_drain = bar_acce + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_accf + 8 * b, 1);
+      mbar_init(bar_acce + 8 * b, 4);  // one arrival per epilogue warp
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), S::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Everything above overlapped the previous stage; from here on we read
+  // what it wrote.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int num_tiles = (BSRC == kDense) ? (p.dense_rows + BN - 1) / BN : __ldg(p.num_tiles);
+  const int units = num_tiles * p.m_tiles * p.splits;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    constexpr int kGroups = BN / 4;  // gather4 row groups per tile
+    constexpr int kGPerLane = (kGroups + 31) / 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    long issued = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      if (*abort_flag) break;
+      const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
+      int rows_tok[kGPerLane][4];
+      const int ngroups = (w.rows + 3) >> 2;
+      if (BSRC == kGather) {
+#pragma unroll
+        for (int gi = 0; gi < kGPerLane; ++gi) {
+          const int g = lane + 32 * gi;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            int tok = 0;
+            if (g < ngroups) {
+              const int n = (4 * g + r < w.rows) ? 4 * g + r : 4 * g;  // pad: repeat a valid row
+              tok = __ldg(p.sorted_ids + w.row0 + n) / p.topk;
+            }
+            rows_tok[gi][r] = tok;
+          }
+        }
+      }
+      const uint32_t bytes =
+          kABytes + (BSRC == kGather ? static_cast<uint32_t>(ngroups) * 4u * kKBytes : S::kBBytes);
+      for (int kt = w.kt0; kt < w.kt1; ++kt) {
+        if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u)) {
+          report_timeout(p, abort_flag);
+          ok = false;
+          break;
+        }
+        const uint32_t full = bar_full + 8 * stage;
+        const uint32_t a_dst = sA + stage * kABytes;
+        const uint32_t b_dst = sB + stage * S::kBBytes;
+        const int kc = kt * S::kElemsPerStage;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, bytes);
+          if (BSRC == kGather) {
+            tma_load_3d(a_dst, &tmA, full, kc, w.mt * 64, w.e);
+            tma_load_3d(a_dst + 64 * kKBytes, &tmA, full, kc, p.I + w.mt * 64, w.e);
+          } else {
+            tma_load_3d(a_dst, &tmA, full, kc, w.mt * kTileM, w.e);
+            tma_load_2d(b_dst, &tmB, full, kc, w.row0);
+          }
+        }
+        __syncwarp();
+        if (BSRC == kGather) {
+#pragma unroll
+          for (int gi = 0; gi < kGPerLane; ++gi) {
+            const int g = lane + 32 * gi;
+            if (g < ngroups)
+              tma_gather4(b_dst + g * 4 * kKBytes, &tmB, full, kc, rows_tok[gi][0],
+                          rows_tok[gi][1], rows_tok[gi][2], rows_tok[gi][3]);
+          }
+        }
+        ++issued;
+        if (++stage == S::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (*abort_flag) {
+      // Let our own copies land before the CTA can exit.
+      const long first = issued > S::kStages ? issued - S::kStages : 0;
+      for (long i = first; i < issued; ++i)
+        mbar_wait(bar_full + 8 * static_cast<int>(i % S::kStages),
+                  static_cast<uint32_t>((i / S::kStages) & 1));
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int ab = 0;
+      uint32_t aph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        if (*abort_flag) break;
+        const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
+        if (!FP8) {
+          if (!mbar_wait(bar_acce + 8 * ab, aph ^ 1u)) {
+            report_timeout(p, abort_flag);
+            break;
+          }
+          tc_fence_after();
+        }
+        for (int kt = w.kt0; kt < w.kt1; ++kt) {
+          if (FP8) {
+            if (!mbar_wait(bar_acce + 8 * ab, aph ^ 1u)) {
+              report_timeout(p, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!mbar_wait(bar_full + 8 * stage, phase)) {
+            report_timeout(p, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
+          const uint64_t adesc = smem_desc_sw128(sA + stage * kABytes);
+          const uint64_t bdesc = smem_desc_sw128(sB + stage * S::kBBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
+            const uint32_t acc = FP8 ? (k > 0) : (kt > w.kt0 || k > 0);
+            if (FP8)
+              mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, S::kIdesc, acc);
+            else
+              mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, S::kIdesc, acc);
+          }
+          tc_commit(bar_empty + 8 * stage);
+          if (++stage == S::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (FP8) {
+            tc_commit(bar_accf + 8 * ab);
+            ab ^= 1;
+            if (ab == 0) aph ^= 1u;
+          }
+        }
+        if (!FP8 && ok) {
+          tc_commit(bar_accf + 8 * ab);
+          ab ^= 1;
+          if (ab == 0) aph ^= 1u;
+        }
+      }
+      if (*abort_flag) {
+        tc_commit(bar_drain);  // wait for our own MMAs before TMEM is freed
+        mbar_wait(bar_drain, 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int qd = warp & 3;          // TMEM lane quadrant this warp may read
+    const int r = qd * 32 + lane;     // row of the 128-row weight tile
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
+    int ab = 0;
+    uint32_t aph = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
+      int col;
+      bool col_ok = true;
+      if (BSRC == kGather) {
+        col = (r < 64) ? (w.mt * 64 + r) : (p.I + w.mt * 64 + (r - 64));
+      } else {
+        col = w.mt * kTileM + r;
+        col_ok = col < p.M;
+      }
+      float* outp = p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0) * p.M + col;
+      if (!FP8) {
+        if (!mbar_wait(bar_accf + 8 * ab, aph)) {
+          report_timeout(p, abort_flag);
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BN / 16; ++c) {
+          if (c * 16 < w.rows) {
+            uint32_t v[16];
+            tmem_ld16(t_lane + static_cast<uint32_t>(ab * BN + c * 16), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int n = c * 16 + j;
+              if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = __uint_as_float(v[j]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
+        ab ^= 1;
+        if (ab == 0) aph ^= 1u;
+      } else {
+        // Per-column scale rows: lane l serves columns l, l+32, ...
+        constexpr int kCPerLane = BN / 32 > 0 ? BN / 32 : 1;
+        const int KB = p.kt_total;
+        int srow[kCPerLane];
+#pragma unroll
+        for (int i = 0; i < kCPerLane; ++i) {
+          const int n = lane + 32 * i;
+          int row = -1;
+          if (n < w.rows && n < BN)
+            row = (BSRC == kGather) ? __ldg(p.sorted_ids + w.row0 + n) / p.topk : w.row0 + n;
+          srow[i] = row;
+        }
+        const int blk = (BSRC == kGather) ? ((r < 64 ? w.mt * 64 : p.I + w.mt * 64) >> 7) : w.mt;
+        const float* wsp = p.w_scale + (static_cast<size_t>(w.e) * (p.M >> 7) + blk) * KB;
+        float acc[BN];
+#pragma unroll
+        for (int j = 0; j < BN; ++j) acc[j] = 0.f;
+        bool ok = true;
+        for (int kt = w.kt0; kt < w.kt1; ++kt) {
+          const float sw = __ldg(wsp + kt);
+          float sx[kCPerLane];
+#pragma unroll
+          for (int i = 0; i < kCPerLane; ++i)
+            sx[i] = srow[i] >= 0 ? __ldg(p.b_scale + static_cast<size_t>(srow[i]) * KB + kt) : 0.f;
+          if (!mbar_wait(bar_accf + 8 * ab, aph)) {
+            report_timeout(p, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < BN / 16; ++c) {
+            if (c * 16 < w.rows) {
+              uint32_t v[16];
+              tmem_ld16(t_lane + static_cast<uint32_t>(ab * BN + c * 16), v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int n = c * 16 + j;
+                const float s = sw * __shfl_sync(0xffffffffu, sx[n >> 5], n & 31);
+                acc[n] = fmaf(__uint_as_float(v[j]), s, acc[n]);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
+          ab ^= 1;
+          if (ab == 0) aph ^= 1u;
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int n = 0; n < BN; ++n)
+          if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = acc[n];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::kTmemCols);
+  }
+}
+
+template <int FP8, int BN, int BSRC>
+cudaError_t launch_gemm_inst(int grid, cudaStream_t st, bool pdl, const CUtensorMap& a,
+                             const CUtensorMap& b, const GemmParams& p) {
+  using S = GemmShape<FP8, BN>;
+  auto kern = moe_gemm_kernel<FP8, BN, BSRC>;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !configured[dev]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(S::kSmemBytes));
+    if (err != cudaSuccess) return err;
+    configured[dev] = 1;
+  }
+  return launch_kernel(kern, dim3(grid), dim3(kGemmThreads), S::kSmemBytes, st, pdl, a, b, p);
+}
+
+template <int FP8, int BSRC>
+cudaError_t launch_gemm_bn(int bn, int grid, cudaStream_t st, bool pdl, const CUtensorMap& a,
+                           const CUtensorMap& b, const GemmParams& p) {
+  switch (bn) {
+    case 16: return launch_gemm_inst<FP8, 16, BSRC>(grid, st, pdl, a, b, p);
+    case 32: return launch_gemm_inst<FP8, 32, BSRC>(grid, st, pdl, a, b, p);
+    case 64: return launch_gemm_inst<FP8, 64, BSRC>(grid, st, pdl, a, b, p);
+    case 128: return launch_gemm_inst<FP8, 128, BSRC>(grid, st, pdl, a, b, p);
+    case 256:
+      if constexpr (!FP8) return launch_gemm_inst<FP8, 256, BSRC>(grid, st, pdl, a, b, p);
+      return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

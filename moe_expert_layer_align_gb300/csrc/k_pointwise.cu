@@ -1,0 +1,302 @@
+// k_pointwise.cu — the bandwidth-bound stages around the expert GEMMs:
+// activation quantisation, the fused SiLU-and-mul (+ FP8 requantisation),
+// the top-k weighted combine, and the router's weight split and top-k.
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+
+// FP8 rule for one group of 128 channels held 4 per lane by a warp:
+// s = amax/448 (1 when amax is 0); q = e4m3 RNE-satfinite(v / s) (IEEE fp32
+// division).  Returns the 4 codes packed little-endian; writes s via *scale.
+__device__ __forceinline__ uint32_t quant_group4(const float (&v)[4], float* scale) {
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+  *scale = s;
+  const uint16_t lo = cvt_e4m3x2(__fdiv_rn(v[1], s), __fdiv_rn(v[0], s));
+  const uint16_t hi = cvt_e4m3x2(__fdiv_rn(v[3], s), __fdiv_rn(v[2], s));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// ---------------------------------------------------------------- x quant
+// x bf16 [T][H] -> xq e4m3 [T][H], xs [T][H/128]; one warp per group.
+__global__ void __launch_bounds__(128) moe_quant_x_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          int T, int H, uint8_t* __restrict__ xq,
+                                                          float* __restrict__ xs) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x;
+  const int g = blockIdx.y * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (g >= H / 128) return;
+  const size_t base = static_cast<size_t>(t) * H + g * 128 + lane * 4;
+  const uint2 raw = *reinterpret_cast<const uint2*>(x + base);
+  const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+  const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+  float v[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
+  float s;
+  const uint32_t q = quant_group4(v, &s);
+  *reinterpret_cast<uint32_t*>(xq + base) = q;
+  if (lane == 0) xs[static_cast<size_t>(t) * (H / 128) + g] = s;
+}
+
+cudaError_t launch_quant_x(const void* x, int T, int H, uint8_t* xq, float* xs, cudaStream_t st,
+                           bool pdl) {
+  const dim3 grid(T, (H / 128 + 3) / 4);
+  return launch_kernel(moe_quant_x_kernel, grid, dim3(128), 0, st, pdl,
+                       static_cast<const __nv_bfloat16*>(x), T, H, xq, xs);
+}
+
+// ---------------------------------------------------------------- act
+// HPC-Ops × SGLang, section "MoE", "Gate-Up and activation": SiLU-and-mul and
+// FP8 requantisation run as one fused kernel whose output Down reads as is.
+// For each index row p that holds an assignment:
+//   g = sum_s G[s][p][i], u = sum_s G[s][p][I + i] (split-K partials in order)
+//   a = SiLU(g) * u = g / (1 + exp(-g)) * u
+// BF16: A[p][i] = bf16(a).  FP8: per 128 channels s = amax/448, codes e4m3.
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <int FP8>
+__global__ void __launch_bounds__(128)
+    moe_act_kernel(const float* __restrict__ G, int splits, int rows_cap, int I,
+                   const int32_t* __restrict__ sorted_ids, int sentinel, void* __restrict__ A,
+                   float* __restrict__ As) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int p = blockIdx.x;
+  if (__ldg(sorted_ids + p) >= sentinel) return;  // padding row
+  const int i = (blockIdx.y * 128 + threadIdx.x) * 4;
+  // FP8: a warp covers one whole 128-channel group, so this exit is
+  // warp-uniform and the group's shuffles stay complete.
+  if (i >= I) return;
+  const size_t two_i = 2 * static_cast<size_t>(I);
+  const size_t slice = static_cast<size_t>(rows_cap) * two_i;
+  float v[4];
+  {
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    const float* row = G + static_cast<size_t>(p) * two_i;
+    for (int s = 0; s < splits; ++s) {
+      const float4 gs = __ldg(reinterpret_cast<const float4*>(row + s * slice + i));
+      const float4 us = __ldg(reinterpret_cast<const float4*>(row + s * slice + I + i));
+      g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
+      u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
+    }
+    v[0] = silu_mul(g.x, u.x);
+    v[1] = silu_mul(g.y, u.y);
+    v[2] = silu_mul(g.z, u.z);
+    v[3] = silu_mul(g.w, u.w);
+  }
+  if (FP8) {
+    float s;
+    const uint32_t q = quant_group4(v, &s);
+    uint8_t* Aq = static_cast<uint8_t*>(A);
+    *reinterpret_cast<uint32_t*>(Aq + static_cast<size_t>(p) * I + i) = q;
+    if ((threadIdx.x & 31) == 0) As[static_cast<size_t>(p) * (I / 128) + i / 128] = s;
+  } else {
+    __nv_bfloat16* Ab = static_cast<__nv_bfloat16*>(A) + static_cast<size_t>(p) * I + i;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(Ab) = packed;
+  }
+}
+
+cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
+                       const int32_t* sorted_ids, int sentinel, void* A, float* As,
+                       cudaStream_t st, bool pdl) {
+  // 128 threads x 4 channels per block column; FP8 needs I % 128 == 0 so that
+  // every warp holds one whole 128-channel group.
+  const dim3 grid(rows_cap, (I + 511) / 512);
+  if (fp8)
+    return launch_kernel(moe_act_kernel<1>, grid, dim3(128), 0, st, pdl, G, splits, rows_cap, I,
+                         sorted_ids, sentinel, A, As);
+  return launch_kernel(moe_act_kernel<0>, grid, dim3(128), 0, st, pdl, G, splits, rows_cap, I,
+                       sorted_ids, sentinel, A, As);
+}
+
+// ---------------------------------------------------------------- combine
+// HPC-Ops × SGLang, section "MoE", "PDL-chained stages": the final top-k
+// weighted reduction restores expert outputs to token order.
+//   out[t][h] = sum_{j ascending} w[t][j] * sum_{s ascending} Y[s][inv_pos[t*k+j]][h]
+// fp32, fixed order, no atomics.
+__global__ void __launch_bounds__(128)
+    moe_combine_kernel(const float* __restrict__ Y, int splits, int rows_cap, int H,
+                       const int32_t* __restrict__ inv_pos, const float* __restrict__ topk_w,
+                       int T, int k, void* __restrict__ out, int out_bf16) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x;
+  const int h = (blockIdx.y * 128 + threadIdx.x) * 4;
+  if (h >= H) return;
+  const size_t slice = static_cast<size_t>(rows_cap) * H;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const int pos = __ldg(inv_pos + static_cast<size_t>(t) * k + j);
+    if (pos < 0) continue;
+    const float w = __ldg(topk_w + static_cast<size_t>(t) * k + j);
+    const float* row = Y + static_cast<size_t>(pos) * H + h;
+    float4 y = __ldg(reinterpret_cast<const float4*>(row));
+    for (int s = 1; s < splits; ++s) {
+      const float4 ys = __ldg(reinterpret_cast<const float4*>(row + s * slice));
+      y.x += ys.x; y.y += ys.y; y.z += ys.z; y.w += ys.w;
+    }
+    acc.x = fmaf(w, y.x, acc.x);
+    acc.y = fmaf(w, y.y, acc.y);
+    acc.z = fmaf(w, y.z, acc.z);
+    acc.w = fmaf(w, y.w, acc.w);
+  }
+  const size_t o = static_cast<size_t>(t) * H + h;
+  if (out_bf16) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + o) = packed;
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = acc;
+  }
+}
+
+cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H, const int32_t* inv_pos,
+                           const float* topk_w, int T, int k, void* out, int out_bf16,
+                           cudaStream_t st, bool pdl) {
+  const dim3 grid(T, (H / 4 + 127) / 128);
+  return launch_kernel(moe_combine_kernel, grid, dim3(128), 0, st, pdl, Y, splits, rows_cap, H,
+                       inv_pos, topk_w, T, k, out, out_bf16);
+}
+
+// ---------------------------------------------------------------- router
+// HPC-Ops × SGLang, section "Router GEMM", "a precision-aware BF16
+// formulation": the fp32 weight is split into two bf16 parts, the high part
+// by plain truncation and the low part from the residual scaled by 256, so
+// that W ~= hi + lo/256 and the router GEMM runs as two bf16 GEMMs.
+__global__ void moe_router_prepare_kernel(const float* __restrict__ wr, size_t n,
+                                          __nv_bfloat16* __restrict__ hi_lo) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float w = wr[i];
+    const uint32_t bits = __float_as_uint(w) & 0xFFFF0000u;   // truncation
+    const float hi = __uint_as_float(bits);
+    const float lo = (w - hi) * 256.0f;                        // exact
+    hi_lo[i] = __ushort_as_bfloat16(static_cast<unsigned short>(bits >> 16));
+    hi_lo[n + i] = __float2bfloat16_rn(lo);
+  }
+}
+
+cudaError_t launch_router_prepare(const float* wr, int E, int H, void* hi_lo, cudaStream_t st) {
+  const size_t n = static_cast<size_t>(E) * H;
+  const int blocks = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  moe_router_prepare_kernel<<<blocks, 256, 0, st>>>(wr, n, static_cast<__nv_bfloat16*>(hi_lo));
+  return cudaGetLastError();
+}
+
+// One warp per token: scores from the split-K partials of the two GEMMs
+// (P[s][t][0..E) = x.hi, P[s][t][E..2E) = x.lo), score = acc_hi + acc_lo/256;
+// softmax (or sigmoid); k rounds of warp arg-max over the raw scores (ties to
+// the lower id); weights renormalised over the selected ids, times `scale`.
+constexpr int kRouterMaxE = 512;
+
+__global__ void __launch_bounds__(128)
+    moe_router_topk_kernel(const float* __restrict__ P, int splits, int rows_cap, int T, int E,
+                           int k, int score_fn, float scale, float* __restrict__ scores,
+                           int32_t* __restrict__ ids, float* __restrict__ w) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  constexpr int kPer = kRouterMaxE / 32;
+  float s[kPer];
+  const size_t slice = static_cast<size_t>(rows_cap) * 2 * E;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    float v = -INFINITY;
+    if (e < E) {
+      float hi = 0.f, lo = 0.f;
+      const float* row = P + static_cast<size_t>(t) * 2 * E;
+      for (int sp = 0; sp < splits; ++sp) {
+        hi += row[sp * slice + e];
+        lo += row[sp * slice + E + e];
+      }
+      v = hi + lo * (1.0f / 256.0f);
+      scores[static_cast<size_t>(t) * E + e] = v;
+    }
+    s[i] = v;
+    mx = fmaxf(mx, v);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+  float prob[kPer];
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    float pv = 0.f;
+    if (e < E) pv = score_fn == 0 ? expf(s[i] - mx) : 1.0f / (1.0f + expf(-s[i]));
+    prob[i] = pv;
+    z += pv;
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+  float psel = 0.f, my_p = 0.f;
+  int my_id = -1;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && (s[i] > bv || (s[i] == bv && e < bi))) {
+        bv = s[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    // owner lane removes the winner and reports its probability
+    float pw = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (lane + 32 * i == bi) {
+        pw = score_fn == 0 ? prob[i] / z : prob[i];
+        s[i] = -INFINITY;
+      }
+    const int owner = bi & 31;
+    pw = __shfl_sync(0xffffffffu, pw, owner);
+    psel += pw;
+    if (lane == j) {
+      my_id = bi;
+      my_p = pw;
+    }
+  }
+  if (lane < k) {
+    ids[static_cast<size_t>(t) * k + lane] = my_id;
+    w[static_cast<size_t>(t) * k + lane] = scale * (my_p / psel);
+  }
+}
+
+cudaError_t launch_router_topk(const float* P, int splits, int rows_cap, int T, int E, int k,
+                               int score_fn, float scale, float* scores, int32_t* ids, float* w,
+                               cudaStream_t st, bool pdl) {
+  return launch_kernel(moe_router_topk_kernel, dim3((T + 3) / 4), dim3(128), 0, st, pdl, P, splits,
+                       rows_cap, T, E, k, score_fn, scale, scores, ids, w);
+}
+
+}  // namespace moe

@@ -1,0 +1,517 @@
+// moe_api.cu — the C ABI (include/moe.h): argument checks, the planner that
+// picks the row tile and split-K counts, workspace layout, TMA descriptors,
+// and the PDL-chained launch of the stages.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// The split-K choice is planned for this many persistent CTAs so that the
+// plan, and with it the workspace size, is a function of the shape alone.
+constexpr int kPlanCtas = 152;
+constexpr int kMaxSplits = 32;
+
+struct Plan {
+  int T, H, I, E, k, bm, fp8, out_bf16;
+  int tiles_cap, rows_cap;
+  int s1, kts1, kt1, mt1;  // Gate-Up: splits, k-tiles per split, k-tiles, weight tiles
+  int s2, kts2, kt2, mt2;  // Down
+  size_t off[13];
+  size_t total;
+};
+
+enum {
+  kOffCounts, kOffOffsets, kOffSorted, kOffTileExpert, kOffTiles, kOffInvPos, kOffNumTiles,
+  kOffXq, kOffXs, kOffG, kOffA, kOffAs, kOffY
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool valid_bm(int bm, int fp8) {
+  return bm == 16 || bm == 32 || bm == 64 || bm == 128 || (bm == 256 && !fp8);
+}
+
+int64_t tiles_cap_of(int64_t T, int64_t k, int64_t E, int64_t bm) {
+  const int64_t tk = T * k;
+  return (tk + bm - 1) / bm + std::min(E, tk);
+}
+
+// Row tile: the smallest of 16..256 (FP8: ..128) that holds 1.5x the mean
+// rows of an active expert, so that most experts occupy one tile.
+int auto_bm(int T, int k, int E, int fp8) {
+  const double tk = static_cast<double>(T) * k;
+  const double active = E * (1.0 - std::pow(1.0 - static_cast<double>(k) / E, T));
+  const double mean = tk / std::max(1.0, std::min(active, tk));
+  const int cap = fp8 ? 128 : 256;
+  int bm = 16;
+  while (bm < cap && bm < 1.5 * mean) bm *= 2;
+  return bm;
+}
+
+// Expected number of row tiles under uniform routing (a planning estimate;
+// the kernels read the true count from the index).
+int est_tiles(int T, int k, int E, int bm, int tiles_cap) {
+  const double tk = static_cast<double>(T) * k;
+  const double active = E * (1.0 - std::pow(1.0 - static_cast<double>(k) / E, T));
+  const double per = tk / std::max(1.0, active);
+  const double est = std::max(1.0, active) * std::ceil(per / bm);
+  return static_cast<int>(std::min<double>(tiles_cap, std::max(1.0, std::round(est))));
+}
+
+// Split-K count minimising (waves of units) x (k-tiles per unit) plus the
+// cost of writing and re-reading fp32 partial rows, in k-tile units.
+void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int* kts_out) {
+  double best = 1e300;
+  int bs = 1, bk = kt_total;
+  for (int s = 1; s <= std::min(kMaxSplits, kt_total); ++s) {
+    const int kts = (kt_total + s - 1) / s;
+    const int se = (kt_total + kts - 1) / kts;
+    if (se != s) continue;            // same as a smaller count
+    if (s > 1 && kts < 4) break;      // keep the pipeline at least 4 stages deep
+    const double units = static_cast<double>(m_tiles) * se * tiles;
+    const double grid = std::min<double>(kPlanCtas, units);
+    const double waves = std::ceil(units / grid);
+    const double extra = se > 1 ? 0.5 * units * bn / 16.0 / kPlanCtas : 0.0;
+    const double cost = waves * kts + extra;
+    if (cost < best - 1e-9) {
+      best = cost;
+      bs = se;
+      bk = kts;
+    }
+  }
+  *s_out = bs;
+  *kts_out = bk;
+}
+
+moe_status check_shape(const moe_shape* s) {
+  if (!s) return MOE_ERR_ARG;
+  if (s->mode != MOE_BF16 && s->mode != MOE_FP8_W8A8) return MOE_ERR_DTYPE;
+  if (s->out_dtype != MOE_OUT_F32 && s->out_dtype != MOE_OUT_BF16) return MOE_ERR_DTYPE;
+  const int fp8 = s->mode == MOE_FP8_W8A8;
+  if (s->T < 1 || s->H < 128 || s->I < 64 || s->E < 1 || s->E > 512 || s->k < 1 || s->k > s->E)
+    return MOE_ERR_SHAPE;
+  if (s->H % 128 || s->I % (fp8 ? 128 : 64)) return MOE_ERR_SHAPE;
+  if (static_cast<int64_t>(s->T) * s->k >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
+  if (s->block_m != 0 && !valid_bm(s->block_m, fp8)) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  std::memset(p, 0, sizeof(*p));
+  p->T = s->T, p->H = s->H, p->I = s->I, p->E = s->E, p->k = s->k;
+  p->fp8 = s->mode == MOE_FP8_W8A8;
+  p->out_bf16 = s->out_dtype == MOE_OUT_BF16;
+  p->bm = s->block_m ? s->block_m : auto_bm(s->T, s->k, s->E, p->fp8);
+  const int64_t tc = tiles_cap_of(s->T, s->k, s->E, p->bm);
+  if (tc * p->bm >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
+  p->tiles_cap = static_cast<int>(tc);
+  p->rows_cap = static_cast<int>(tc * p->bm);
+  const int kstage = p->fp8 ? 128 : 64;
+  p->kt1 = s->H / kstage;
+  p->mt1 = s->I / 64;
+  p->kt2 = s->I / kstage;
+  p->mt2 = s->H / 128;
+  const int est = est_tiles(s->T, s->k, s->E, p->bm, p->tiles_cap);
+  choose_split(p->mt1, p->kt1, est, p->bm, &p->s1, &p->kts1);
+  choose_split(p->mt2, p->kt2, est, p->bm, &p->s2, &p->kts2);
+  if (o && o->split_gateup > 0) {
+    p->kts1 = (p->kt1 + o->split_gateup - 1) / o->split_gateup;
+    p->s1 = (p->kt1 + p->kts1 - 1) / p->kts1;
+  }
+  if (o && o->split_down > 0) {
+    p->kts2 = (p->kt2 + o->split_down - 1) / o->split_down;
+    p->s2 = (p->kt2 + p->kts2 - 1) / p->kts2;
+  }
+  // workspace layout
+  const size_t tk = static_cast<size_t>(s->T) * s->k;
+  const size_t rc = p->rows_cap;
+  const size_t sizes[13] = {
+      4u * s->E,
+      4u * (s->E + 1),
+      4 * rc,
+      4u * p->tiles_cap,
+      16u * p->tiles_cap,
+      4 * tk,
+      4,
+      p->fp8 ? static_cast<size_t>(s->T) * s->H : 0,
+      p->fp8 ? 4 * static_cast<size_t>(s->T) * (s->H / 128) : 0,
+      4 * static_cast<size_t>(p->s1) * rc * 2 * s->I,
+      rc * s->I * (p->fp8 ? 1 : 2),
+      p->fp8 ? 4 * rc * (s->I / 128) : 0,
+      4 * static_cast<size_t>(p->s2) * rc * s->H,
+  };
+  size_t cur = 0;
+  for (int i = 0; i < 13; ++i) {
+    p->off[i] = cur;
+    cur = align_up(cur + sizes[i], 256);
+  }
+  p->total = cur;
+  return MOE_OK;
+}
+
+void fill_layout(const Plan& p, moe_workspace_layout* L) {
+  std::memset(L, 0, sizeof(*L));
+  L->block_m = p.bm;
+  L->tiles_cap = p.tiles_cap;
+  L->rows_cap = p.rows_cap;
+  L->split_gateup = p.s1;
+  L->split_down = p.s2;
+  L->grid_gateup = kPlanCtas;
+  L->grid_down = kPlanCtas;
+  L->off_counts = p.off[kOffCounts];
+  L->off_offsets = p.off[kOffOffsets];
+  L->off_sorted_ids = p.off[kOffSorted];
+  L->off_tile_expert = p.off[kOffTileExpert];
+  L->off_tiles = p.off[kOffTiles];
+  L->off_inv_pos = p.off[kOffInvPos];
+  L->off_num_tiles = p.off[kOffNumTiles];
+  L->off_xq = p.off[kOffXq];
+  L->off_xs = p.off[kOffXs];
+  L->off_g = p.off[kOffG];
+  L->off_a = p.off[kOffA];
+  L->off_as = p.off[kOffAs];
+  L->off_y = p.off[kOffY];
+  L->total_bytes = p.total;
+}
+
+// ---------------------------------------------------------------- devices
+int device_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return kPlanCtas;
+  if (!sms[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = kPlanCtas;
+    sms[dev] = v;
+  }
+  return sms[dev];
+}
+
+// ---------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D K-major map [rows][cols] of `esize`-byte elements, box {128 bytes of
+// K, box_rows}, 128-byte swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, int esize, uint64_t cols, uint64_t rows,
+                 uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * esize};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D K-major map [experts][rows][cols], box {128 bytes of K, box_rows, 1}.
+bool make_map_3d(CUtensorMap* m, const void* base, int esize, uint64_t cols, uint64_t rows,
+                 uint64_t experts, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cols, rows, experts};
+  const cuuint64_t strides[2] = {cols * esize, cols * rows * esize};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+void record(const moe_forward_opts* o, int i, cudaStream_t st) {
+  if (o && o->stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(o->stage_events[i]), st);
+}
+
+cudaError_t launch_gemm(int fp8, int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
+                        const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p) {
+  return fp8 ? launch_gemm_fp8(bn, bsrc, grid, st, pdl, a, b, p)
+             : launch_gemm_bf16(bn, bsrc, grid, st, pdl, a, b, p);
+}
+
+// Router plan: row tile, split-K count and workspace for the partial sums.
+struct RouterPlan {
+  int bn, rows_cap, splits, kts, kt, mt;
+  size_t bytes;
+};
+
+bool router_plan(int T, int H, int E, RouterPlan* r) {
+  if (T < 1 || H < 128 || H % 128 || E < 64 || E > 512 || E % 64) return false;
+  r->bn = T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128;
+  r->rows_cap = (T + r->bn - 1) / r->bn * r->bn;
+  r->kt = H / 64;
+  r->mt = 2 * E / 128;
+  choose_split(r->mt, r->kt, r->rows_cap / r->bn, r->bn, &r->splits, &r->kts);
+  r->bytes = 4ull * r->splits * r->rows_cap * 2 * E;
+  return true;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_index_tiles_cap(int32_t T, int32_t k, int32_t E, int32_t block_m) {
+  if (T < 1 || k < 1 || E < 1 || block_m < 1) return 0;
+  return static_cast<size_t>(tiles_cap_of(T, k, E, block_m));
+}
+
+moe_status moe_plan(const moe_shape* shape, const moe_forward_opts* opts,
+                    moe_workspace_layout* layout) {
+  if (!layout) return MOE_ERR_ARG;
+  Plan p;
+  const moe_status st = make_plan(shape, opts, &p);
+  if (st != MOE_OK) return st;
+  fill_layout(p, layout);
+  return MOE_OK;
+}
+
+size_t moe_workspace_bytes(const moe_shape* shape, const moe_forward_opts* opts) {
+  Plan p;
+  return make_plan(shape, opts, &p) == MOE_OK ? p.total : 0;
+}
+
+moe_status moe_align(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E, int32_t block_m,
+                     const moe_index* idx, int32_t* dev_status, void* stream) {
+  if (!topk_ids || !idx || !idx->counts || !idx->offsets || !idx->sorted_ids ||
+      !idx->tile_expert || !idx->tiles || !idx->inv_pos || !idx->num_tiles)
+    return MOE_ERR_ARG;
+  if (T < 1 || k < 1 || E < 1 || E > 512 || k > E || !valid_bm(block_m, 0))
+    return MOE_ERR_SHAPE;
+  if (static_cast<int64_t>(T) * k >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
+  if (!aligned(idx->tiles, 16)) return MOE_ERR_ALIGN;
+  IndexPtrs ip{idx->counts, idx->offsets, idx->sorted_ids, idx->tile_expert,
+               idx->tiles,  idx->inv_pos,  idx->num_tiles};
+  const int tc = static_cast<int>(tiles_cap_of(T, k, E, block_m));
+  return cuda_status(launch_align(topk_ids, T, k, E, block_m, tc, ip, dev_status,
+                                  static_cast<cudaStream_t>(stream), false));
+}
+
+moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13, const void* w2,
+                          const int32_t* topk_ids, const float* topk_w, const moe_scales* scales,
+                          void* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                          void* stream, const moe_forward_opts* opts) {
+  Plan p;
+  moe_status st = make_plan(shape, opts, &p);
+  if (st != MOE_OK) return st;
+  if (!x || !w13 || !w2 || !topk_ids || !topk_w || !out || !workspace) return MOE_ERR_ARG;
+  if (p.fp8 && (!scales || !scales->w13_scale || !scales->w2_scale)) return MOE_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
+      !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(workspace, 256))
+    return MOE_ERR_ALIGN;
+  if (p.fp8 && (!aligned(scales->w13_scale, 4) || !aligned(scales->w2_scale, 4)))
+    return MOE_ERR_ALIGN;
+  if (ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool pdl = !(opts && opts->disable_pdl);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto at = [&](int i) { return ws + p.off[i]; };
+  IndexPtrs ip{reinterpret_cast<int32_t*>(at(kOffCounts)),     reinterpret_cast<int32_t*>(at(kOffOffsets)),
+               reinterpret_cast<int32_t*>(at(kOffSorted)),     reinterpret_cast<int32_t*>(at(kOffTileExpert)),
+               reinterpret_cast<int32_t*>(at(kOffTiles)),      reinterpret_cast<int32_t*>(at(kOffInvPos)),
+               reinterpret_cast<int32_t*>(at(kOffNumTiles))};
+  uint8_t* xq = at(kOffXq);
+  float* xs = reinterpret_cast<float*>(at(kOffXs));
+  float* G = reinterpret_cast<float*>(at(kOffG));
+  void* A = at(kOffA);
+  float* As = reinterpret_cast<float*>(at(kOffAs));
+  float* Y = reinterpret_cast<float*>(at(kOffY));
+  const int esize = p.fp8 ? 1 : 2;
+  const int tk = p.T * p.k;
+
+  CUtensorMap tmW13, tmX, tmW2, tmA;
+  if (!make_map_3d(&tmW13, w13, esize, p.H, 2ull * p.I, p.E, 64) ||
+      !make_map_2d(&tmX, p.fp8 ? static_cast<const void*>(xq) : x, esize, p.H, p.T, 1) ||
+      !make_map_3d(&tmW2, w2, esize, p.I, p.H, p.E, 128) ||
+      !make_map_2d(&tmA, A, esize, p.I, p.rows_cap, p.bm))
+    return MOE_ERR_CUDA;
+
+  const int sms = device_sms();
+  const int grid_cap = opts && opts->grid_ctas > 0 ? opts->grid_ctas : sms;
+  cudaError_t e;
+
+  record(opts, 0, s);
+  e = launch_align(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s, false);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  record(opts, 1, s);
+  if (p.fp8) {
+    e = launch_quant_x(x, p.T, p.H, xq, xs, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+
+  record(opts, 2, s);
+  GemmParams g1 = {};
+  g1.M = 2 * p.I;
+  g1.K = p.H;
+  g1.I = p.I;
+  g1.m_tiles = p.mt1;
+  g1.splits = p.s1;
+  g1.kt_per_split = p.kts1;
+  g1.kt_total = p.kt1;
+  g1.tiles = ip.tiles;
+  g1.num_tiles = ip.num_tiles;
+  g1.sorted_ids = ip.sorted_ids;
+  g1.topk = p.k;
+  g1.sentinel = tk;
+  g1.w_scale = p.fp8 ? scales->w13_scale : nullptr;
+  g1.b_scale = p.fp8 ? xs : nullptr;
+  g1.out = G;
+  g1.rows_cap = p.rows_cap;
+  g1.dev_status = dev_status;
+  const int units1 = p.mt1 * p.s1 * p.tiles_cap;
+  e = launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, pdl, tmW13, tmX, g1);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  record(opts, 3, s);
+  e = launch_act(p.fp8, G, p.s1, p.rows_cap, p.I, ip.sorted_ids, tk, A, As, s, pdl);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  record(opts, 4, s);
+  GemmParams g2 = {};
+  g2.M = p.H;
+  g2.K = p.I;
+  g2.I = 0;
+  g2.m_tiles = p.mt2;
+  g2.splits = p.s2;
+  g2.kt_per_split = p.kts2;
+  g2.kt_total = p.kt2;
+  g2.tiles = ip.tiles;
+  g2.num_tiles = ip.num_tiles;
+  g2.sorted_ids = ip.sorted_ids;
+  g2.topk = p.k;
+  g2.sentinel = tk;
+  g2.w_scale = p.fp8 ? scales->w2_scale : nullptr;
+  g2.b_scale = p.fp8 ? As : nullptr;
+  g2.out = Y;
+  g2.rows_cap = p.rows_cap;
+  g2.dev_status = dev_status;
+  const int units2 = p.mt2 * p.s2 * p.tiles_cap;
+  e = launch_gemm(p.fp8, p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  record(opts, 5, s);
+  e = launch_combine(Y, p.s2, p.rows_cap, p.H, ip.inv_pos, topk_w, p.T, p.k, out, p.out_bf16, s,
+                     pdl);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  record(opts, 6, s);
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_shape* shape, const void* x, const void* w13, const void* w2,
+                       const int32_t* topk_ids, const float* topk_w, const moe_scales* scales,
+                       void* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                       void* stream) {
+  return moe_forward_ex(shape, x, w13, w2, topk_ids, topk_w, scales, out, workspace, ws_bytes,
+                        dev_status, stream, nullptr);
+}
+
+moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t rows_cap, const float* y,
+                       const int32_t* inv_pos, const float* topk_w, void* out, void* stream) {
+  if (!shape || !y || !inv_pos || !topk_w || !out) return MOE_ERR_ARG;
+  if (shape->out_dtype != MOE_OUT_F32 && shape->out_dtype != MOE_OUT_BF16) return MOE_ERR_DTYPE;
+  if (shape->T < 1 || shape->k < 1 || shape->H < 4 || shape->H % 4 || splits < 1 || rows_cap < 1)
+    return MOE_ERR_SHAPE;
+  if (!aligned(y, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
+  return cuda_status(launch_combine(y, splits, rows_cap, shape->H, inv_pos, topk_w, shape->T,
+                                    shape->k, out, shape->out_dtype == MOE_OUT_BF16,
+                                    static_cast<cudaStream_t>(stream), false));
+}
+
+moe_status moe_router_prepare(const float* wr, int32_t E, int32_t H, void* hi_lo, void* stream) {
+  if (!wr || !hi_lo) return MOE_ERR_ARG;
+  if (E < 1 || H < 1) return MOE_ERR_SHAPE;
+  if (!aligned(hi_lo, 2) || !aligned(wr, 4)) return MOE_ERR_ALIGN;
+  return cuda_status(launch_router_prepare(wr, E, H, hi_lo, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_router_workspace_bytes(int32_t T, int32_t H, int32_t E) {
+  RouterPlan r;
+  return router_plan(T, H, E, &r) ? r.bytes : 0;
+}
+
+moe_status moe_router_topk(const void* x, const void* hi_lo, int32_t T, int32_t H, int32_t E,
+                           int32_t k, int32_t score_fn, float scale, float* scores,
+                           int32_t* topk_ids, float* topk_w, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  if (!x || !hi_lo || !scores || !topk_ids || !topk_w || !workspace) return MOE_ERR_ARG;
+  if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_ARG;
+  RouterPlan r;
+  if (!router_plan(T, H, E, &r) || k < 1 || k > E || k > 32) return MOE_ERR_SHAPE;
+  if (!aligned(x, 16) || !aligned(hi_lo, 16) || !aligned(workspace, 16)) return MOE_ERR_ALIGN;
+  if (ws_bytes < r.bytes) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap tmW, tmX;
+  if (!make_map_3d(&tmW, hi_lo, 2, H, 2ull * E, 1, 128) ||
+      !make_map_2d(&tmX, x, 2, H, T, r.bn))
+    return MOE_ERR_CUDA;
+  GemmParams g = {};
+  g.M = 2 * E;
+  g.K = H;
+  g.m_tiles = r.mt;
+  g.splits = r.splits;
+  g.kt_per_split = r.kts;
+  g.kt_total = r.kt;
+  g.dense_rows = T;
+  g.out = static_cast<float*>(workspace);
+  g.rows_cap = r.rows_cap;
+  const int units = r.mt * r.splits * (r.rows_cap / r.bn);
+  cudaError_t e = launch_gemm_bf16(r.bn, kDense, std::min(device_sms(), units), s, false, tmW,
+                                   tmX, g);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_router_topk(static_cast<const float*>(workspace), r.splits, r.rows_cap,
+                                        T, E, k, score_fn, scale, scores, topk_ids, topk_w, s,
+                                        true));
+}
+
+const char* moe_status_str(int32_t status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument (null pointer or bad enum)";
+    case MOE_ERR_SHAPE: return "unsupported or inconsistent sizes";
+    case MOE_ERR_DTYPE: return "unsupported mode or output dtype";
+    case MOE_ERR_ALIGN: return "pointer not suitably aligned";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_EXPERT_ID: return "an expert id outside [0, E) was dropped";
+    case MOE_ERR_TIMEOUT: return "a bounded on-chip wait gave up";
+    case MOE_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

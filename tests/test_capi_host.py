@@ -1,0 +1,123 @@
+"""Host-side checks of the C ABI, no GPU needed: the library loads, exports
+every symbol include/moe.h declares, the planner is self-consistent, and bad
+arguments are rejected before anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_expert_layer_align_gb300 as moe
+from moe_expert_layer_align_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_symbols()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(B.lib, n), n
+        assert n in B.SYMBOLS, n
+
+
+def test_status_strings():
+    for s in range(9):
+        assert moe.moe_status_str(s) and moe.moe_status_str(s) != "unknown status"
+    assert moe.moe_status_str(99) == "unknown status"
+
+
+@pytest.mark.parametrize("T,H,I,E,k,fp8", [
+    (8, 256, 512, 8, 2, False), (64, 4096, 14336, 8, 2, False), (1, 2048, 768, 128, 8, False),
+    (4096, 2048, 768, 128, 8, False), (64, 7168, 2048, 256, 8, True), (4096, 7168, 2048, 256, 8, True),
+])
+def test_plan_is_consistent(T, H, I, E, k, fp8):
+    s = moe.make_shape(T, H, I, E, k, 0, fp8, True)
+    L = moe.moe_plan(s)
+    assert L.block_m in (16, 32, 64, 128, 256) and (not fp8 or L.block_m <= 128)
+    assert L.tiles_cap == moe.moe_index_tiles_cap(T, k, E, L.block_m)
+    assert L.tiles_cap == -(-T * k // L.block_m) + min(E, T * k)
+    assert L.rows_cap == L.tiles_cap * L.block_m
+    assert L.split_gateup >= 1 and L.split_down >= 1
+    offs = [L.off_counts, L.off_offsets, L.off_sorted_ids, L.off_tile_expert, L.off_tiles,
+            L.off_inv_pos, L.off_num_tiles, L.off_xq, L.off_xs, L.off_g, L.off_a, L.off_as,
+            L.off_y]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert L.off_y + 4 * L.split_down * L.rows_cap * H <= L.total_bytes
+    assert moe.moe_workspace_bytes(s) == L.total_bytes
+    # forced splits are honoured and resize the workspace
+    o = moe.make_opts(split_gateup=2, split_down=3)
+    L2 = moe.moe_plan(s, o)
+    assert L2.split_gateup == 2 and L2.split_down == 3
+
+
+def test_rejects_bad_shapes_without_launching():
+    bad = [
+        moe.make_shape(0, 256, 512, 8, 2),      # T
+        moe.make_shape(8, 200, 512, 8, 2),      # H % 128
+        moe.make_shape(8, 256, 500, 8, 2),      # I % 64
+        moe.make_shape(8, 256, 512, 8, 9),      # k > E
+        moe.make_shape(8, 256, 512, 600, 2),    # E > 512
+        moe.make_shape(8, 256, 576, 8, 2, 0, True),   # FP8 needs I % 128
+        moe.make_shape(8, 256, 512, 8, 2, 24),  # block_m
+        moe.make_shape(8, 256, 512, 8, 2, 256, True),  # FP8 block_m <= 128
+    ]
+    for s in bad:
+        assert moe.moe_workspace_bytes(s) == 0
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_plan(s)
+        assert ei.value.status == moe.MOE_ERR_SHAPE
+    s = moe.make_shape(8, 256, 512, 8, 2)
+    s.mode = 7
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_plan(s)
+    assert ei.value.status == moe.MOE_ERR_DTYPE
+
+
+def _fwd(shape, ptrs, ws_bytes, scales=None):
+    x, w13, w2, ids, w, out, ws = ptrs
+    return B.lib.moe_forward(ctypes.byref(shape), x, w13, w2, ids, w,
+                             ctypes.byref(scales) if scales else None, out, ws, ws_bytes, None,
+                             None)
+
+
+def test_forward_argument_errors_precede_any_launch():
+    # Fake (never dereferenced) addresses: every call below must fail in the
+    # host checks, before a CUDA call is made.
+    s = moe.make_shape(8, 256, 512, 8, 2)
+    need = moe.moe_workspace_bytes(s)
+    good = [0x100000 * (i + 1) for i in range(7)]
+    assert _fwd(s, [None] + good[1:], need) == moe.MOE_ERR_ARG
+    assert _fwd(s, good[:6] + [None], need) == moe.MOE_ERR_ARG
+    mis = list(good)
+    mis[0] += 8
+    assert _fwd(s, mis, need) == moe.MOE_ERR_ALIGN
+    mis = list(good)
+    mis[6] += 128
+    assert _fwd(s, mis, need) == moe.MOE_ERR_ALIGN
+    assert _fwd(s, good, need - 1) == moe.MOE_ERR_WORKSPACE
+    f = moe.make_shape(8, 256, 512, 8, 2, 0, True)
+    assert _fwd(f, good, moe.moe_workspace_bytes(f)) == moe.MOE_ERR_ARG   # FP8 without scales
+    assert B.lib.moe_align(None, 8, 2, 8, 16, None, None, None) == moe.MOE_ERR_ARG
+    idx = B.moe_index(*good)
+    assert B.lib.moe_align(good[0], 8, 2, 8, 24, ctypes.byref(idx), None, None) == moe.MOE_ERR_SHAPE
+    idx.tiles = good[4] + 4
+    assert B.lib.moe_align(good[0], 8, 2, 8, 16, ctypes.byref(idx), None, None) == moe.MOE_ERR_ALIGN
+
+
+def test_router_host_checks():
+    assert moe.moe_router_workspace_bytes(64, 2048, 128) > 0
+    assert moe.moe_router_workspace_bytes(64, 2000, 128) == 0
+    assert moe.moe_router_workspace_bytes(64, 2048, 100) == 0
+    g = [0x100000 * (i + 1) for i in range(7)]
+    assert B.lib.moe_router_topk(g[0], g[1], 64, 2048, 128, 33, 0, 1.0, g[2], g[3], g[4], g[5],
+                                 1 << 30, None) == moe.MOE_ERR_SHAPE
+    assert B.lib.moe_router_topk(g[0], g[1], 64, 2048, 128, 8, 5, 1.0, g[2], g[3], g[4], g[5],
+                                 1 << 30, None) == moe.MOE_ERR_ARG
+    assert B.lib.moe_router_topk(g[0], g[1], 64, 2048, 128, 8, 0, 1.0, g[2], g[3], g[4], g[5],
+                                 16, None) == moe.MOE_ERR_WORKSPACE

@@ -1,0 +1,77 @@
+"""The router (moe_router_prepare + moe_router_topk through the C ABI) against
+the oracle: the hi/lo split bit-exact, scores within 2e-3 of the fp64
+reference, top-k ids equal except where the oracle's scores are within 1e-5
+of a tie, and the FP8 layer fed by that routing within tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_layer_align_gb300 import workloads
+from helpers import assert_layer_close, bits16, oracle_layer, run_layer
+
+pytestmark = pytest.mark.gpu
+
+SCORE_TOL = 2e-3
+TIE_GAP = 1e-5
+
+
+def check_topk(ids_gpu, ids_ref, scores_ref, k):
+    for t in range(ids_ref.shape[0]):
+        if set(ids_gpu[t]) == set(ids_ref[t]) and np.array_equal(ids_gpu[t], ids_ref[t]):
+            continue
+        s = np.sort(scores_ref[t])[::-1]
+        # a difference is allowed only where the ranking is within TIE_GAP
+        gaps = np.abs(scores_ref[t][ids_gpu[t]] - scores_ref[t][ids_ref[t]])
+        assert gaps.max() < TIE_GAP or s[k - 1] - s[k] < TIE_GAP, (t, ids_gpu[t], ids_ref[t])
+
+
+@pytest.mark.parametrize("T", [4, 16, 64, 256, 300])
+def test_router_matches_oracle(T):
+    import moe_expert_layer_align_gb300 as moe
+    wl = workloads.make(5, T, "cpu")
+    x = wl.x.cuda()
+    wr = wl.wr.cuda()
+    hi_lo = moe.moe_router_prepare(wr)
+    scores, ids, w = moe.moe_router_topk(x, hi_lo, wl.k, moe.MOE_SCORE_SOFTMAX, 1.0)
+    torch.cuda.synchronize()
+    hi, lo = oracle.router_split(wl.wr.numpy())
+    hl = bits16(hi_lo)
+    np.testing.assert_array_equal(hl[: wl.E], hi)
+    np.testing.assert_array_equal(hl[wl.E:], lo)
+    ref_s = oracle.router_scores(bits16(wl.x), wl.wr.numpy())
+    err = np.abs(scores.cpu().numpy() - ref_s).max()
+    assert err <= SCORE_TOL, err
+    ref_ids, ref_w = oracle.router_topk(ref_s, wl.k, 0, 1.0)
+    g_ids = ids.cpu().numpy()
+    check_topk(g_ids, ref_ids, ref_s, wl.k)
+    same = np.all(g_ids == ref_ids, axis=1)
+    np.testing.assert_allclose(w.cpu().numpy()[same], ref_w[same], rtol=2e-4, atol=1e-6)
+    np.testing.assert_allclose(w.sum(1).cpu().numpy(), 1.0, rtol=1e-5)
+
+
+def test_sigmoid_scaled_router():
+    import moe_expert_layer_align_gb300 as moe
+    g = torch.Generator().manual_seed(5)
+    T, H, E, k = 33, 1024, 64, 6
+    x = torch.randn(T, H, generator=g).bfloat16()
+    wr = torch.randn(E, H, generator=g) / 32
+    hi_lo = moe.moe_router_prepare(wr.cuda())
+    scores, ids, w = moe.moe_router_topk(x.cuda(), hi_lo, k, moe.MOE_SCORE_SIGMOID, 2.5)
+    torch.cuda.synchronize()
+    ref_s = oracle.router_scores(bits16(x), wr.numpy())
+    assert np.abs(scores.cpu().numpy() - ref_s).max() <= SCORE_TOL
+    ref_ids, ref_w = oracle.router_topk(ref_s, k, 1, 2.5)
+    check_topk(ids.cpu().numpy(), ref_ids, ref_s, k)
+    np.testing.assert_allclose(w.sum(1).cpu().numpy(), 2.5, rtol=1e-5)
+
+
+@pytest.mark.parametrize("T", [4, 64])
+def test_routed_fp8_layer(T):
+    import moe_expert_layer_align_gb300 as moe
+    wl = workloads.make(5, T, "cpu", H=512, I=256, E=64).to("cuda")
+    hi_lo = moe.moe_router_prepare(wl.wr)
+    _, ids, w = moe.moe_router_topk(wl.x, hi_lo, wl.k)
+    got = run_layer(wl, topk_ids=ids, topk_w=w).float().cpu().numpy()
+    ref = oracle_layer(wl, topk_ids=ids.cpu(), topk_w=w.cpu())
+    assert_layer_close(got, ref, "fp8", f"routed T={T}")
