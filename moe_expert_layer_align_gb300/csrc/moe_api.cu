@@ -251,8 +251,15 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Stage events.  Under stream capture a plain record only orders work inside
+// the graph; the external flag makes it a real timestamp node.
 void record(const moe_forward_opts* o, int i, cudaStream_t st) {
-  if (o && o->stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(o->stage_events[i]), st);
+  if (!o || !o->stage_events[i]) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  cudaEventRecordWithFlags(static_cast<cudaEvent_t>(o->stage_events[i]), st,
+                           cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                               : cudaEventRecordDefault);
 }
 
 cudaError_t launch_gemm(int fp8, int bn, int bsrc, int grid, cudaStream_t st, bool pdl,

@@ -44,7 +44,7 @@ def test_layer_matches_oracle(cfg, T, kw):
 def test_every_block_m(bm, mode_cfg):
     if mode_cfg == 4 and bm == 256:
         pytest.skip("FP8 tiles stop at 128 rows")
-    kw = dict(H=256, I=256, E=6) if mode_cfg == 4 else dict(H=256, I=192, E=6)
+    kw = dict(H=256, I=256, E=6, k=4) if mode_cfg == 4 else dict(H=256, I=192, E=6)
     wl = small(mode_cfg, 150, **kw)
     got = run_layer(wl, block_m=bm).float().cpu().numpy()
     assert_layer_close(got, oracle_layer(wl), wl.mode, f"bm={bm}")
@@ -87,7 +87,7 @@ def test_intermediates_bf16():
 
 def test_intermediates_fp8_codes():
     import moe_expert_layer_align_gb300 as moe
-    wl = small(4, 20, H=512, I=256, E=6)
+    wl = small(4, 20, H=512, I=256, E=6, k=3)
     shape = moe.layer_shape(wl.x, wl.w13q, wl.topk_ids, 0, torch.bfloat16)
     ws = torch.zeros(moe.moe_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
     got = run_layer(wl, workspace=ws).float().cpu().numpy()
