@@ -226,6 +226,36 @@ MOE_API moe_status moe_router_topk(const void* x, const void* hi_lo, int32_t T,
                            float* topk_w, void* workspace, size_t ws_bytes,
                            void* stream);
 
+/* Largest workspace moe_forward_static can serve (128 MiB): for example the
+ * Mixtral-shaped bf16 layer up to T=64 or the Qwen3-30B-A3B-shaped layer up
+ * to T=256. */
+#define MOE_STATIC_SCRATCH_BYTES ((size_t)128 << 20)
+
+/* moe_forward without a workspace argument, for callers that cannot allocate
+ * device memory: code running while a stream is captured into a CUDA graph in
+ * the global capture mode (cudaMalloc is rejected there), serving engines
+ * that reserve all device memory at start-up and forbid later allocation, and
+ * plain-C hosts with no device allocator of their own.  No counterpart on the
+ * pages: it is an interface convenience of this library.
+ *   The intermediates live in one file-scope device array of
+ *   MOE_STATIC_SCRATCH_BYTES that the CUDA loader reserves on every GPU that
+ *   loads this library and that stays reserved until the process exits.  The
+ *   call itself allocates nothing (no cudaMalloc / cudaFree, no allocating
+ *   library routine).
+ *   The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents (nothing
+ *   in it needs to start at zero): calls that overlap on the GPU race and must
+ *   be serialised by the caller.
+ * Arguments, layouts and device-status behaviour are those of moe_forward.
+ * Errors: those of moe_forward; MOE_ERR_WORKSPACE when the shape needs more
+ * than MOE_STATIC_SCRATCH_BYTES (moe_workspace_bytes(shape, NULL) tells). */
+MOE_API moe_status moe_forward_static(const moe_shape* shape, const void* x,
+                                      const void* w13, const void* w2,
+                                      const int32_t* topk_ids, const float* topk_w,
+                                      const moe_scales* scales, void* out,
+                                      int32_t* dev_status, void* stream);
+
 /* Static description of a status code. */
 MOE_API const char* moe_status_str(int32_t status);
 

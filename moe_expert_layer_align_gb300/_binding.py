@@ -77,6 +77,8 @@ def _load() -> ctypes.CDLL:
         "moe_router_workspace_bytes": (_sz, [_i32, _i32, _i32]),
         "moe_router_topk": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
                                    _vp, _vp, _vp, _vp, _sz, _vp]),
+        "moe_forward_static": (_i32, [P(moe_shape), _vp, _vp, _vp, _vp, _vp, P(moe_scales),
+                                      _vp, _vp, _vp]),
         "moe_status_str": (ctypes.c_char_p, [_i32]),
     }
     for name, (res, args) in sig.items():
@@ -89,7 +91,9 @@ def _load() -> ctypes.CDLL:
 lib = _load()
 SYMBOLS = ("moe_index_tiles_cap", "moe_plan", "moe_workspace_bytes", "moe_align", "moe_forward",
            "moe_forward_ex", "moe_combine", "moe_router_prepare", "moe_router_workspace_bytes",
-           "moe_router_topk", "moe_status_str")
+           "moe_router_topk", "moe_forward_static", "moe_status_str")
+# Largest workspace moe_forward_static can serve (MOE_STATIC_SCRATCH_BYTES).
+STATIC_SCRATCH_BYTES = 128 << 20
 
 
 class MoeError(RuntimeError):
@@ -204,6 +208,24 @@ def moe_forward(x, w13, w2, topk_ids, topk_w, *, scales=None, out=None, out_dtyp
         _check(lib.moe_forward(*args), "moe_forward")
     else:
         _check(lib.moe_forward_ex(*args, ctypes.byref(opts)), "moe_forward_ex")
+    return out
+
+
+def moe_forward_static(x, w13, w2, topk_ids, topk_w, *, scales=None, out=None, out_dtype=None,
+                       dev_status=None, stream=None):
+    """moe_forward for callers that cannot allocate device memory: the
+    intermediates live in the library's own static device scratch
+    (STATIC_SCRATCH_BYTES, shared by all calls, so calls must not overlap on
+    the GPU).  Only `out` is allocated here when not given."""
+    shape = layer_shape(x, w13, topk_ids, 0, out.dtype if out is not None else out_dtype)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16 if shape.out_dtype else torch.float32,
+                          device=x.device)
+    sc = moe_scales(_ptr(scales[0]), _ptr(scales[1])) if scales is not None else None
+    _check(lib.moe_forward_static(ctypes.byref(shape), _ptr(x), _ptr(w13), _ptr(w2),
+                                  _ptr(topk_ids), _ptr(topk_w), ctypes.byref(sc) if sc else None,
+                                  _ptr(out), _ptr(dev_status), _stream(stream)),
+           "moe_forward_static")
     return out
 
 
