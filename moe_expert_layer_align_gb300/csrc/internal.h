@@ -25,6 +25,8 @@ struct GemmParams {
   const int32_t* tiles;      // [tiles_cap][4] task map (gather / direct)
   const int32_t* num_tiles;  // device scalar (gather / direct)
   const int32_t* sorted_ids; // gather: row -> assignment
+  const void* b_rows;        // gather: token rows (x or its e4m3 copy), row-major
+  int b_row_bytes;           // gather: bytes per token row
   int topk;                  // gather: token = assignment / topk
   int sentinel;              // gather: T*k marks padding rows
   int dense_rows;            // dense: number of rows

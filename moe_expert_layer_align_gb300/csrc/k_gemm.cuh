@@ -26,11 +26,16 @@
 // partial * w_scale[e][row/128][kb] * b_scale[token][kb] into fp32 registers
 // (block scales are fp32, so the product cannot be folded into the MMA).
 //
-// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 (one thread)
-// issues MMAs, warps 2..5 drain TMEM.  With the accumulator in TMEM instead of
-// registers, this split costs no registers, so the Hopper argument for one
-// warp group doing everything ("occupancy first, no warp specialisation")
-// does not carry over.  Every wait is bounded (kWaitLimitNs); on a timeout
+// Warp roles: warp 0 issues the TMA loads (weights; the token tile too when
+// its rows are contiguous), warp 1 (one thread) issues MMAs, warps 2..5 drain
+// TMEM, and for the gathered token operand warps 6.. copy the token rows with
+// 16-byte cp.async into the 128-byte-swizzled layout, each thread arriving on
+// the stage barrier when its copies land.  (TMA's four-row gather was tried
+// first: at one op per ~40 ns it capped the prefill Gate-Up at a third of the
+// rate of a dense load of the same bytes.)  With the accumulator in TMEM
+// instead of registers this split costs no registers, so the Hopper argument
+// for one warp group doing everything ("occupancy first, no warp
+// specialisation") does not carry over.  Every wait is bounded (kWaitLimitNs); on a timeout
 // the kernel ORs kStatusTimeout into dev_status, drains its own copies and
 // MMAs, frees TMEM and returns.
 #pragma once
@@ -39,7 +44,7 @@
 
 namespace moe {
 
-constexpr int kGemmThreads = 192;
+constexpr int kRoleThreads = 192;           // TMA, MMA and 4 epilogue warps
 constexpr int kTileM = 128;                 // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // K bytes per pipeline stage
 constexpr int kABytes = kTileM * kKBytes;   // 16 KB weight tile per stage
@@ -48,9 +53,14 @@ __host__ __device__ constexpr int stages_for(int fp8, int bn) {
   return bn <= 32 ? 8 : bn == 64 ? (fp8 ? 7 : 8) : bn == 128 ? (fp8 ? 5 : 6) : 4;
 }
 
-template <int FP8, int BN>
+template <int FP8, int BN, int BSRC = kDirect>
 struct GemmShape {
   static constexpr int kStages = stages_for(FP8, BN);
+  // token-row gather warps (gathered operand only) and block size
+  static constexpr int kGatherWarps = BSRC == kGather ? (BN >= 128 ? 2 : 1) : 0;
+  static constexpr int kGatherThreads = 32 * kGatherWarps;
+  static constexpr int kThreads = kRoleThreads + kGatherThreads;
+  static constexpr int kRowsPerGatherThread = kGatherWarps ? BN / (4 * kGatherWarps) : 1;
   static constexpr int kBBytes = BN * kKBytes;
   static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
   static constexpr int kElemsPerStage = FP8 ? 128 : 64;
@@ -95,10 +105,10 @@ __device__ __forceinline__ void report_timeout(const GemmParams& p, volatile int
 }
 
 template <int FP8, int BN, int BSRC>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-  using S = GemmShape<FP8, BN>;
+  using S = GemmShape<FP8, BN, BSRC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -117,7 +127,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      // the TMA thread's expect-tx arrival, plus one per gather thread
+      mbar_init(bar_full + 8 * s, 1 + S::kGatherThreads);
       mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -149,64 +160,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    constexpr int kGroups = BN / 4;  // gather4 row groups per tile
-    constexpr int kGPerLane = (kGroups + 31) / 32;
     int stage = 0;
     uint32_t phase = 0;
     long issued = 0;
     bool ok = true;
+    const uint32_t bytes = kABytes + (BSRC == kGather ? 0u : static_cast<uint32_t>(S::kBBytes));
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
       if (*abort_flag) break;
       const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
-      int rows_tok[kGPerLane][4];
-      const int ngroups = (w.rows + 3) >> 2;
-      if (BSRC == kGather) {
-#pragma unroll
-        for (int gi = 0; gi < kGPerLane; ++gi) {
-          const int g = lane + 32 * gi;
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            int tok = 0;
-            if (g < ngroups) {
-              const int n = (4 * g + r < w.rows) ? 4 * g + r : 4 * g;  // pad: repeat a valid row
-              tok = __ldg(p.sorted_ids + w.row0 + n) / p.topk;
-            }
-            rows_tok[gi][r] = tok;
-          }
-        }
-      }
-      const uint32_t bytes =
-          kABytes + (BSRC == kGather ? static_cast<uint32_t>(ngroups) * 4u * kKBytes : S::kBBytes);
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u)) {
           report_timeout(p, abort_flag);
           ok = false;
           break;
         }
-        const uint32_t full = bar_full + 8 * stage;
-        const uint32_t a_dst = sA + stage * kABytes;
-        const uint32_t b_dst = sB + stage * S::kBBytes;
-        const int kc = kt * S::kElemsPerStage;
         if (lane == 0) {
+          const uint32_t full = bar_full + 8 * stage;
+          const uint32_t a_dst = sA + stage * kABytes;
+          const int kc = kt * S::kElemsPerStage;
           mbar_arrive_expect_tx(full, bytes);
           if (BSRC == kGather) {
             tma_load_3d(a_dst, &tmA, full, kc, w.mt * 64, w.e);
             tma_load_3d(a_dst + 64 * kKBytes, &tmA, full, kc, p.I + w.mt * 64, w.e);
           } else {
             tma_load_3d(a_dst, &tmA, full, kc, w.mt * kTileM, w.e);
-            tma_load_2d(b_dst, &tmB, full, kc, w.row0);
+            tma_load_2d(sB + stage * S::kBBytes, &tmB, full, kc, w.row0);
           }
         }
         __syncwarp();
-        if (BSRC == kGather) {
-#pragma unroll
-          for (int gi = 0; gi < kGPerLane; ++gi) {
-            const int g = lane + 32 * gi;
-            if (g < ngroups)
-              tma_gather4(b_dst + g * 4 * kKBytes, &tmB, full, kc, rows_tok[gi][0],
-                          rows_tok[gi][1], rows_tok[gi][2], rows_tok[gi][3]);
-          }
-        }
         ++issued;
         if (++stage == S::kStages) {
           stage = 0;
@@ -214,13 +195,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
-    if (*abort_flag) {
+    if (*abort_flag && lane == 0) {
       // Let our own copies land before the CTA can exit.
       const long first = issued > S::kStages ? issued - S::kStages : 0;
       for (long i = first; i < issued; ++i)
         mbar_wait(bar_full + 8 * static_cast<int>(i % S::kStages),
                   static_cast<uint32_t>((i / S::kStages) & 1));
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -254,6 +236,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
+          // token rows written by cp.async (generic proxy) are read by the MMA
+          // through the async proxy
+          if (BSRC == kGather) fence_proxy_async_smem();
           const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
           const uint64_t adesc = smem_desc_sw128(sA + stage * kABytes);
           const uint64_t bdesc = smem_desc_sw128(sB + stage * S::kBBytes);
@@ -288,7 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < kRoleThreads / 32) {
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3;          // TMEM lane quadrant this warp may read
     const int r = qd * 32 + lane;     // row of the 128-row weight tile
@@ -387,6 +372,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = acc[n];
       }
     }
+  } else if (BSRC == kGather) {
+    // ------------------------------------------------------------ token gather
+    // Thread t copies 16-byte chunk c = t % 8 of rows n = t/8 + 4*NG*i; a
+    // warp instruction covers four whole 128-byte rows.  Padding rows are not
+    // copied: their MMA columns are never stored.
+    constexpr int kR = S::kRowsPerGatherThread;
+    constexpr int kRowStep = 4 * (S::kGatherWarps > 0 ? S::kGatherWarps : 1);
+    const int t = threadIdx.x - kRoleThreads;
+    const int c = t & 7;
+    const int r0 = t >> 3;
+    const uint8_t* rows = static_cast<const uint8_t*>(p.b_rows) + c * 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      if (*abort_flag) break;
+      const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
+      int tok[kR];
+#pragma unroll
+      for (int i = 0; i < kR; ++i) {
+        const int n = r0 + kRowStep * i;
+        tok[i] = n < w.rows ? __ldg(p.sorted_ids + w.row0 + n) / p.topk : -1;
+      }
+      for (int kt = w.kt0; kt < w.kt1; ++kt) {
+        if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u)) {
+          report_timeout(p, abort_flag);
+          ok = false;
+          break;
+        }
+        const uint32_t b_dst = sB + stage * S::kBBytes;
+        const uint8_t* src = rows + static_cast<size_t>(kt) * kKBytes;
+#pragma unroll
+        for (int i = 0; i < kR; ++i) {
+          const int n = r0 + kRowStep * i;
+          if (tok[i] >= 0)
+            cp_async_16(b_dst + n * kKBytes + ((c ^ (n & 7)) << 4),
+                        src + static_cast<size_t>(tok[i]) * p.b_row_bytes);
+        }
+        cp_async_arrive_noinc(bar_full + 8 * stage);
+        if (++stage == S::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
   }
 
   tc_fence_before();
@@ -400,7 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int FP8, int BN, int BSRC>
 cudaError_t launch_gemm_inst(int grid, cudaStream_t st, bool pdl, const CUtensorMap& a,
                              const CUtensorMap& b, const GemmParams& p) {
-  using S = GemmShape<FP8, BN>;
+  using S = GemmShape<FP8, BN, BSRC>;
   auto kern = moe_gemm_kernel<FP8, BN, BSRC>;
   static int configured[64] = {0};
   int dev = 0;
@@ -412,7 +443,7 @@ cudaError_t launch_gemm_inst(int grid, cudaStream_t st, bool pdl, const CUtensor
     if (err != cudaSuccess) return err;
     configured[dev] = 1;
   }
-  return launch_kernel(kern, dim3(grid), dim3(kGemmThreads), S::kSmemBytes, st, pdl, a, b, p);
+  return launch_kernel(kern, dim3(grid), dim3(S::kThreads), S::kSmemBytes, st, pdl, a, b, p);
 }
 
 template <int FP8, int BSRC>

@@ -394,6 +394,8 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g1.tiles = ip.tiles;
   g1.num_tiles = ip.num_tiles;
   g1.sorted_ids = ip.sorted_ids;
+  g1.b_rows = p.fp8 ? static_cast<const void*>(xq) : x;
+  g1.b_row_bytes = p.H * esize;
   g1.topk = p.k;
   g1.sentinel = tk;
   g1.w_scale = p.fp8 ? scales->w13_scale : nullptr;

@@ -1,5 +1,5 @@
-// ptx.cuh — inline-PTX wrappers for sm_103a: mbarrier, TMA (tiled and
-// gather4), tcgen05 (TMEM alloc, MMA, commit, loads), PDL and e4m3 packing.
+// ptx.cuh — inline-PTX wrappers for sm_103a: mbarrier, TMA, cp.async,
+// tcgen05 (TMEM alloc, MMA, commit, loads), PDL and e4m3 packing.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -78,15 +78,21 @@ MOE_DEV void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
-// Four rows r0..r3 of a 2-D tensor (box one row high) at column c0, written
-// to consecutive 128-byte rows of shared memory.
-MOE_DEV void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int r0,
-                         int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
+
+// ------------------------------------------------------------------ cp.async
+// 16-byte global -> shared copy through L2 (bypassing L1).
+MOE_DEV void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this arrival).
+MOE_DEV void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Order shared-memory writes made through the generic proxy (cp.async, st)
+// before later async-proxy reads (tcgen05.mma operands, TMA).
+MOE_DEV void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
