@@ -1,8 +1,10 @@
 """Benchmark of the fused MoE layer on GB300.
 
-One step = one moe_forward (align, Gate-Up, SiLU-and-mul, Down, combine) over
-one batch of the Mixtral-8x7B-shaped bf16 layer (H=4096, I=14336, E=8, k=2)
-at T tokens (default 64, the top of the decode range), inputs resident in HBM.
+One step = one pass of the layer (align, [x-quant], Gate-Up, SiLU-and-mul,
+Down, combine; the router first where it is in the path) over one batch of a
+workload of moe_expert_layer_align_gb300.workloads, inputs resident in HBM.
+Default: the Mixtral-8x7B-shaped bf16 layer (H=4096, I=14336, E=8, k=2) at
+T=64, the top of the decode range; --config/--T pick another.
 L2 is flushed (a write of 2x the L2 size) before every timed step and every
 step is timed with CUDA events on the launching stream, as the SGLang MoE
 tuning guide (section 2.5) does.  Steps replay a CUDA graph of one
@@ -14,7 +16,8 @@ over the workload's other token counts, an end-to-end number through host
 buffers, the oracle timed on the host cores, and the SM clocks sampled during
 the timed region.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--T 64] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--T 64]
+                  [--impl reference] [--no-sweep] [--no-cpu] [--ncu]
 """
 from __future__ import annotations
 
@@ -33,9 +36,9 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "MoE layer µs & HBM GB/s vs 8 TB/s at T=1–64; TFLOP/s vs peak at T≥1024"
-CFG = 2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_SOURCES = ("k_gemm.cuh", "k_gemm_bf16.cu", "k_gemm_bf16_direct.cu", "ptx.cuh")
+GEMM_SOURCES = ("k_gemm.cuh", "k_gemm_bf16.cu", "k_gemm_bf16_direct.cu", "k_gemm_fp8.cu",
+                "ptx.cuh")
 
 
 def peaks():
@@ -131,43 +134,60 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload
 
-def layer_numbers(wl):
-    """Algorithmic bytes and FLOPs of one layer invocation (routed work only)."""
-    ids = wl.topk_ids.cpu().numpy()
+def layer_numbers(wl, topk_ids):
+    """Algorithmic bytes and FLOPs of one layer invocation (routed work only;
+    the method's own intermediates are overhead, not credited)."""
+    ids = topk_ids.cpu().numpy()
     U = len(np.unique(ids))
-    T, H, I, k = wl.T, wl.H, wl.I, wl.k
-    wbytes = 3 * H * I * 2 * U
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    bw = 2 if wl.mode == "bf16" else 1
+    scales13 = 0 if wl.mode == "bf16" else 4 * (2 * I // 128) * (H // 128)
+    scales2 = 0 if wl.mode == "bf16" else 4 * (H // 128) * (I // 128)
+    w13_bytes = U * (2 * I * H * bw + scales13)
+    w2_bytes = U * (H * I * bw + scales2)
+    router_bytes = 2 * E * H * 2 if wl.wr is not None else 0
     io = T * H * 2 + T * k * 8 + T * H * 2
-    return dict(U=U, weight_bytes=wbytes, bytes=wbytes + io, flops=6 * T * k * H * I,
-                gateup_bytes=2 * I * H * 2 * U + T * H * 2,
-                down_bytes=H * I * 2 * U + T * H * 2)
+    flops = 6 * T * k * H * I + (2 * T * H * 2 * E if wl.wr is not None else 0)
+    return dict(U=U, weight_bytes=w13_bytes + w2_bytes,
+                bytes=w13_bytes + w2_bytes + router_bytes + io, flops=flops,
+                gateup_bytes=w13_bytes + T * H * bw, down_bytes=w2_bytes)
 
 
-def make_workload(T, device, weights=None):
+def make_workload(cfg, T, device, base=None):
     from moe_expert_layer_align_gb300 import workloads
-    if weights is None:
-        return workloads.make(CFG, T, device)
-    c = workloads.CONFIGS[CFG]
-    g = torch.Generator(device=device)
-    g.manual_seed(1000 * CFG + T)
-    x = torch.randn((T, c["H"]), generator=g, device=device).bfloat16()
-    ids, w = workloads.synth_routing(T, c["E"], c["k"], c["routing"], c["scale"], g, device)
-    return workloads.Workload(name=c["name"], T=T, H=c["H"], I=c["I"], E=c["E"], k=c["k"],
-                              mode="bf16", out="bf16", x=x, w13=weights[0], w2=weights[1],
-                              topk_ids=ids, topk_w=w, meta=dict(config=CFG))
+    return workloads.make(cfg, T, device, base=base)
 
 
 class Layer:
-    """One moe_forward on fixed buffers, captured in a CUDA graph."""
+    """One step on fixed buffers — moe_router_topk (in-path router only) then
+    moe_forward — captured in a CUDA graph.  Router weights are split into
+    their two bf16 parts once, before any timing."""
 
     def __init__(self, wl, stream, opts=None, graph=True):
         import moe_expert_layer_align_gb300 as moe
         self.moe, self.wl, self.stream, self.opts = moe, wl, stream, opts
-        shape = moe.layer_shape(wl.x, wl.w13, wl.topk_ids, 0, torch.bfloat16)
-        self.ws = torch.empty(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
-        self.out = torch.empty(wl.x.shape, dtype=torch.bfloat16, device="cuda")
-        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        dev = wl.x.device
+        self.fp8 = wl.mode == "fp8"
+        self.w13 = wl.w13q if self.fp8 else wl.w13
+        self.w2 = wl.w2q if self.fp8 else wl.w2
+        self.scales = (wl.w13s, wl.w2s) if self.fp8 else None
+        if wl.wr is not None:
+            self.hi_lo = moe.moe_router_prepare(wl.wr, stream=stream)
+            self.ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device=dev)
+            self.w = torch.empty((wl.T, wl.k), dtype=torch.float32, device=dev)
+            self.scores = torch.empty((wl.T, wl.E), dtype=torch.float32, device=dev)
+            self.rws = torch.empty(max(16, moe.moe_router_workspace_bytes(wl.T, wl.H, wl.E)),
+                                   dtype=torch.uint8, device=dev)
+        else:
+            self.hi_lo = None
+            self.ids, self.w = wl.topk_ids, wl.topk_w
+        shape = moe.layer_shape(wl.x, self.w13, self.ids, 0, torch.bfloat16)
+        self.shape = shape
+        self.ws = torch.empty(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device=dev)
+        self.out = torch.empty(wl.x.shape, dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
+        self.kernels_per_step = 5 + (1 if self.fp8 else 0) + (2 if self.hi_lo is not None else 0)
         if graph:
             with torch.cuda.stream(stream):
                 self.call()                       # warm the launch path before capture
@@ -177,11 +197,19 @@ class Layer:
                 self.call()
             stream.synchronize()
 
+    def route(self):
+        wl = self.wl
+        self.moe.moe_router_topk(wl.x, self.hi_lo, wl.k, wl.router_fn, wl.router_scale,
+                                 scores=self.scores, topk_ids=self.ids, topk_w=self.w,
+                                 workspace=self.rws, stream=self.stream)
+
     def call(self):
         wl = self.wl
-        self.moe.moe_forward(wl.x, wl.w13, wl.w2, wl.topk_ids, wl.topk_w, out=self.out,
-                             workspace=self.ws, dev_status=self.status, stream=self.stream,
-                             opts=self.opts)
+        if self.hi_lo is not None:
+            self.route()
+        self.moe.moe_forward(wl.x, self.w13, self.w2, self.ids, self.w, scales=self.scales,
+                             out=self.out, workspace=self.ws, dev_status=self.status,
+                             stream=self.stream, opts=self.opts)
 
     def run(self):
         # replay() launches on the current stream: make it ours
@@ -215,7 +243,8 @@ def time_layer(layer, stream, flush, steps, warmup):
 def stage_times(wl, stream, flush, steps):
     """Per-stage device time (us) from events recorded between the stages,
     captured with the layer in a CUDA graph (recording events between stages
-    serialises them: PDL overlap is lost in this pass)."""
+    serialises them: PDL overlap is lost in this pass).  The in-path router is
+    timed as its own graph."""
     import moe_expert_layer_align_gb300 as moe
     n = len(moe.STAGES) + 1
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -223,6 +252,13 @@ def stage_times(wl, stream, flush, steps):
         ev.record(stream)
     layer = Layer(wl, stream, opts=moe.make_opts(stage_events=evs), graph=True)
     acc = np.zeros(n - 1)
+    router = 0.0
+    rgraph = None
+    if layer.hi_lo is not None:
+        rgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rgraph, stream=stream):
+            layer.route()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(steps):
         with torch.cuda.stream(stream):
             flush.zero_()
@@ -230,29 +266,40 @@ def stage_times(wl, stream, flush, steps):
         stream.synchronize()
         for i in range(n - 1):
             acc[i] += evs[i].elapsed_time(evs[i + 1]) * 1e3
-    return dict(zip(moe.STAGES, (acc / steps).tolist()))
+        if rgraph is not None:
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                s0.record(stream)
+                rgraph.replay()
+                s1.record(stream)
+            stream.synchronize()
+            router += s0.elapsed_time(s1) * 1e3
+    out = dict(zip(moe.STAGES, (acc / steps).tolist()))
+    if rgraph is not None:
+        out = {"router": router / steps, **out}
+    return out
 
 
 def e2e_time(wl, stream, steps, warmup):
-    """moe_forward through the public API with host (pinned) inputs and result:
-    H2D of x / topk ids / topk weights, the layer, D2H of the output."""
-    import moe_expert_layer_align_gb300 as moe
+    """The public API with host (pinned) inputs and result: H2D of x (and of
+    the top-k ids and weights when the router is outside the path), the step,
+    D2H of the output."""
+    dev_layer = Layer(wl, stream, graph=False)
     hx = wl.x.cpu().pin_memory()
-    hid = wl.topk_ids.cpu().pin_memory()
-    hw = wl.topk_w.cpu().pin_memory()
+    hid = None if dev_layer.hi_lo is not None else wl.topk_ids.cpu().pin_memory()
+    hw = None if dev_layer.hi_lo is not None else wl.topk_w.cpu().pin_memory()
     hout = torch.empty(wl.x.shape, dtype=torch.bfloat16).pin_memory()
-    dx, did, dw = torch.empty_like(wl.x), torch.empty_like(wl.topk_ids), torch.empty_like(wl.topk_w)
-    shape = moe.layer_shape(wl.x, wl.w13, wl.topk_ids, 0, torch.bfloat16)
-    ws = torch.empty(moe.moe_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
-    out = torch.empty(wl.x.shape, dtype=torch.bfloat16, device="cuda")
+    dx = wl.x                        # the layer reads these buffers
+    did, dw = dev_layer.ids, dev_layer.w
 
     def step():
         with torch.cuda.stream(stream):
             dx.copy_(hx, non_blocking=True)
-            did.copy_(hid, non_blocking=True)
-            dw.copy_(hw, non_blocking=True)
-            moe.moe_forward(dx, wl.w13, wl.w2, did, dw, out=out, workspace=ws, stream=stream)
-            hout.copy_(out, non_blocking=True)
+            if hid is not None:
+                did.copy_(hid, non_blocking=True)
+                dw.copy_(hw, non_blocking=True)
+            dev_layer.call()
+            hout.copy_(dev_layer.out, non_blocking=True)
 
     for _ in range(warmup):
         step()
@@ -264,69 +311,114 @@ def e2e_time(wl, stream, steps, warmup):
     e.record(stream)
     stream.synchronize()
     us = s.elapsed_time(e) * 1e3 / steps
-    return {"value": us, "unit": "us",
-            "h2d_bytes_per_step": hx.numel() * 2 + hid.numel() * 4 + hw.numel() * 4,
+    h2d = hx.numel() * 2 + (0 if hid is None else hid.numel() * 4 + hw.numel() * 4)
+    return {"value": us, "unit": "us", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": hout.numel() * 2}
 
 
-def oracle_baseline(wl, budget_s=15.0, max_tokens=None):
+def oracle_baseline(wl, topk_ids, topk_w, budget_s=15.0, max_tokens=None):
     """The oracle on the host cores over a bounded sample of the batch's
-    tokens; latency scaled to the whole batch."""
+    tokens; latency scaled to the whole batch.  (In-path router: its fp64
+    scores over the whole batch are timed and added.)"""
     import oracle
-    from tests.helpers import bits16
-    x = bits16(wl.x)
-    w13 = bits16(wl.w13)
-    w2 = bits16(wl.w2)
-    ids = wl.topk_ids.cpu().numpy()
-    w = wl.topk_w.cpu().numpy()
+    from tests.helpers import bits16, u8
+    ids = topk_ids.cpu().numpy()
+    w = topk_w.cpu().numpy()
+    if wl.mode == "bf16":
+        args = (bits16(wl.x), bits16(wl.w13), bits16(wl.w2), ids, w)
+        fn = oracle.moe_bf16
+    else:
+        xq, xs = oracle.quant_x(bits16(wl.x))
+        args = (xq, xs, u8(wl.w13q), wl.w13s.cpu().numpy(), u8(wl.w2q), wl.w2s.cpu().numpy(),
+                ids, w)
+        fn = oracle.moe_fp8
     t0 = time.perf_counter()
-    oracle.moe_bf16(x, w13, w2, ids, w, np.array([0], np.int32))
+    fn(*args, np.array([0], np.int32))
     one = time.perf_counter() - t0
     n = int(max(1, min(wl.T, budget_s // max(one, 1e-6))))
     if max_tokens:
         n = min(n, max_tokens)
     sel = np.linspace(0, wl.T - 1, n).astype(np.int32)
     t0 = time.perf_counter()
-    oracle.moe_bf16(x, w13, w2, ids, w, sel)
+    fn(*args, sel)
     dt = time.perf_counter() - t0
-    return {"value": dt / n * wl.T * 1e6, "unit": "us", "cores": oracle.num_threads(),
-            "kind": "oracle",
+    us = dt / n * wl.T * 1e6
+    extra = ""
+    if wl.wr is not None:
+        t0 = time.perf_counter()
+        oracle.router_scores(bits16(wl.x), wl.wr.cpu().numpy())
+        r = time.perf_counter() - t0
+        us += r * 1e6
+        extra = f"; fp64 router scores of all {wl.T} tokens {r:.3f} s added"
+    return {"value": us, "unit": "us", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{n} of {wl.T} tokens of the T={wl.T} batch (fp64 C oracle, OpenMP); "
-                      f"measured {dt:.2f} s, scaled x{wl.T}/{n}"}
+                      f"measured {dt:.2f} s, scaled x{wl.T}/{n}{extra}"}
 
 
 # ---------------------------------------------------------------- arms
+
+def workload_config(cfg, T, wl, nums, extra=None):
+    from moe_expert_layer_align_gb300 import workloads
+    c = workloads.CONFIGS[cfg]
+    d = {"workload": f"{c['name']} MoE layer T={T}", "T": T, "H": wl.H, "I": wl.I, "E": wl.E,
+         "k": wl.k, "weights": "e4m3 + fp32 128x128 block scales" if wl.mode == "fp8" else "bf16",
+         "routing": "in-path router (two-bf16 split), Zipf(1.2) bias" if wl.wr is not None
+         else f"{c['routing']} top-{wl.k}" + (f" x{c['scale']}" if c["scale"] != 1.0 else ""),
+         "active_experts": nums["U"]}
+    d.update(extra or {})
+    return d
+
+
+def oracle_routing(wl):
+    """Top-k ids and weights of the in-path router computed by the oracle."""
+    import oracle
+    from tests.helpers import bits16
+    s = oracle.router_scores(bits16(wl.x), wl.wr.cpu().numpy())
+    ids, w = oracle.router_topk(s, wl.k, wl.router_fn, wl.router_scale)
+    return torch.from_numpy(ids), torch.from_numpy(w.astype(np.float32))
+
 
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    wl = make_workload(args.T, "cpu")
+    wl = make_workload(args.config, args.T, "cpu")
+    if wl.wr is not None:
+        ids, w = oracle_routing(wl)
+    else:
+        ids, w = wl.topk_ids, wl.topk_w
+    nums = layer_numbers(wl, ids)
     for _ in range(args.warmup):
-        oracle_baseline(wl, budget_s=0, max_tokens=1)
+        oracle_baseline(wl, ids, w, budget_s=0, max_tokens=1)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(oracle_baseline(wl, budget_s=5.0)["value"])
+        vals.append(oracle_baseline(wl, ids, w, budget_s=5.0)["value"])
     wall = time.perf_counter() - t0
-    cb = oracle_baseline(wl, budget_s=5.0)
+    cb = oracle_baseline(wl, ids, w, budget_s=5.0)
     v = float(np.mean(vals))
-    import oracle
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"mixtral-8x7b-bf16 MoE layer T={args.T}", "T": args.T,
-                       "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "l2": "n/a (host)"},
-            "cpu_baseline": {"value": v, "unit": "us", "cores": oracle.num_threads(),
-                             "kind": "oracle", "sample": cb["sample"]},
+            "config": workload_config(args.config, args.T, wl, nums, {"l2": "n/a (host)"}),
+            "cpu_baseline": {"value": v, "unit": "us", "cores": cb["cores"], "kind": "oracle",
+                             "sample": cb["sample"]},
             "e2e": {"value": v, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": wall}
     print(json.dumps(line), flush=True)
 
 
+def roofline_times(nums, pk, fp8):
+    t_bytes = nums["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e6
+    peak = pk["bf16_tflops"] * (2.0 if fp8 else 1.0)   # e4m3 dense = 2x bf16 (nominal ratio)
+    t_flops = nums["flops"] / (peak * 1e12) * 1e6
+    return t_bytes, t_flops
+
+
 def run_cuda(args):
     import moe_expert_layer_align_gb300 as moe  # noqa: F401  (loads the CUDA library)
+    from moe_expert_layer_align_gb300 import workloads
     ws_, rank, local = dist_env()
     torch.cuda.set_device(local)
     if ws_ > 1:
@@ -337,10 +429,12 @@ def run_cuda(args):
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
 
-    wl = make_workload(args.T, "cuda")
-    weights = (wl.w13, wl.w2)
-    nums = layer_numbers(wl)
+    cfg = args.config
+    wl = make_workload(cfg, args.T, "cuda")
+    fp8 = wl.mode == "fp8"
     layer = Layer(wl, stream)
+    stream.synchronize()
+    nums = layer_numbers(wl, layer.ids)
 
     def barrier():
         if ws_ > 1:
@@ -361,27 +455,27 @@ def run_cuda(args):
     result = None
     if rank == 0:
         stg = stage_times(wl, stream, flush, max(3, min(args.steps, 10)))
-        t_bytes = nums["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e6
-        t_flops = nums["flops"] / (pk["bf16_tflops"] * 1e12) * 1e6
+        t_bytes, t_flops = roofline_times(nums, pk, fp8)
         gu_us = stg["gateup"]
         achieved = nums["gateup_bytes"] / (gu_us * 1e-6) / 1e9
-        roof = {"bound": "hbm", "kernel": "moe_gemm_kernel<bf16, gather> (Gate-Up)",
-                "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "peak_kind": f"{pk_kind} burst copy",
-                "traffic": ncu_traffic("gateup", args.T),
-                "algorithmic_bytes_per_launch": nums["gateup_bytes"],
-                "launch_us": gu_us}
+        kname = f"moe_gemm_kernel<{'e4m3' if fp8 else 'bf16'}, gather> (Gate-Up)"
+        roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                "peak_kind": f"{pk_kind} burst copy (MEASURED_PEAKS.json hbm_gbs)",
+                "traffic": ncu_traffic(f"c{cfg}:gateup", args.T),
+                "algorithmic_bytes_per_launch": nums["gateup_bytes"], "launch_us": gu_us}
         sweep = []
         if not args.no_sweep:
-            for T in (1, 2, 4, 8, 16, 32, 64, 128, 512, 2048):
-                w2l = make_workload(T, "cuda", weights)
-                n2 = layer_numbers(w2l)
+            for T in workloads.CONFIGS[cfg]["sweep"]:
+                w2l = make_workload(cfg, T, "cuda", base=wl)
                 L2 = Layer(w2l, stream)
+                stream.synchronize()
+                n2 = layer_numbers(w2l, L2.ids)
                 tt, _ = time_layer(L2, stream, flush, 20, 3)
                 u = float(np.median(tt))
-                tb = n2["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e6
-                tf = n2["flops"] / (pk["bf16_tflops"] * 1e12) * 1e6
+                tb, tf = roofline_times(n2, pk, fp8)
                 sweep.append({"T": T, "us": u, "active_experts": n2["U"],
+                              "block_m": int(moe.moe_plan(L2.shape).block_m),
                               "hbm_gbs": n2["bytes"] / (u * 1e-6) / 1e9,
                               "tflops": n2["flops"] / (u * 1e-6) / 1e12,
                               "bound": "hbm" if tb >= tf else "tensor",
@@ -391,17 +485,18 @@ def run_cuda(args):
         clk.__exit__()
         clocks = clk.summary()
         clocks["window"] = "timed region, stage pass, sweep and e2e pass"
-        cpu = None if args.no_cpu else oracle_baseline(wl.to("cpu"))
+        cpu = None if args.no_cpu else oracle_baseline(wl.to("cpu"), layer.ids, layer.w)
+        plan = moe.moe_plan(layer.shape)
         result = {
             "metric": METRIC, "value": us, "unit": "us", "n_gpus": ws_, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded; random-init Mixtral-8x7B-shaped experts)",
-            "config": {"workload": f"mixtral-8x7b-bf16 MoE layer T={args.T}", "T": args.T,
-                       "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                       "active_experts": nums["U"], "replicas": ws_,
-                       "l2": f"flushed before every step ({flush.numel() >> 20} MiB write)",
-                       "timing": "CUDA graph of one moe_forward, CUDA events per step"},
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+            "data": "synthetic (seeded; random-init experts of the named shape)",
+            "config": workload_config(cfg, args.T, wl, nums, {
+                "replicas": ws_, "block_m": plan.block_m,
+                "split_k": [plan.split_gateup, plan.split_down],
+                "l2": f"flushed before every step ({flush.numel() >> 20} MiB write)",
+                "timing": "CUDA graph of one step, CUDA events per step"}),
             "layer": {"us_median": float(np.median(times)), "us_p10": float(np.percentile(times, 10)),
                       "us_p90": float(np.percentile(times, 90)),
                       "hbm_gbs": nums["bytes"] / (us * 1e-6) / 1e9,
@@ -416,7 +511,7 @@ def run_cuda(args):
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,
-            "gpu_launches": 5 * args.steps,
+            "gpu_launches": layer.kernels_per_step * args.steps,
             "wall_s_timed_region": wall,
         }
         print(json.dumps(result), flush=True)
@@ -429,18 +524,18 @@ def run_cuda(args):
 
 
 def run_ncu(args):
-    """Profiler mode: W + K plain moe_forward calls on the workload, nothing
-    else on the GPU (no graphs, flush, sweep or oracle).  Not a bench line."""
+    """Profiler mode: W + K plain steps on the workload, nothing else on the
+    GPU (no graphs, flush, sweep or oracle).  Not a bench line."""
     import moe_expert_layer_align_gb300 as moe  # noqa: F401
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
-    wl = make_workload(args.T, "cuda")
+    wl = make_workload(args.config, args.T, "cuda")
     layer = Layer(wl, stream, graph=False)
     for _ in range(args.warmup + args.steps):
         layer.run()
     stream.synchronize()
-    print(json.dumps({"ncu_mode": True, "T": args.T, "calls": args.warmup + args.steps,
-                      "dev_status": int(layer.status.item())}))
+    print(json.dumps({"ncu_mode": True, "config": args.config, "T": args.T,
+                      "calls": args.warmup + args.steps, "dev_status": int(layer.status.item())}))
 
 
 def main():
@@ -448,6 +543,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5],
+                    help="workload (moe_expert_layer_align_gb300.workloads.CONFIGS)")
     ap.add_argument("--T", type=int, default=64)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-sweep", action="store_true")

@@ -144,30 +144,50 @@ def zipf_router_weights(H, E, s, seed, device="cpu"):
     return wr
 
 
+def make_tokens(cfg: int, T: int, H: int, E: int, k: int, device="cpu", token_seed=None):
+    """Hidden states and (for layers whose router is outside the path) top-k
+    routing of workload `cfg` at T tokens: x first, then the routing, both
+    from one generator seeded 1000*cfg + T."""
+    c = CONFIGS[cfg]
+    gt = _gen(1000 * cfg + T if token_seed is None else token_seed, device)
+    x = torch.randn((T, H), generator=gt, device=device).bfloat16()
+    if c["routing"] == "router":
+        x[:, 0] = 1.0            # carries the Zipf bias of the router weights
+        return x, None, None
+    ids, w = synth_routing(T, E, k, c["routing"], c["scale"], gt, device)
+    return x, ids, w
+
+
 def make(cfg: int, T: int | None = None, device="cpu", *, H=None, I=None, E=None, k=None,
-         weight_seed: int | None = None, token_seed: int | None = None) -> Workload:
+         weight_seed: int | None = None, token_seed: int | None = None,
+         base: "Workload | None" = None) -> Workload:
     """Workload `cfg` (1..5) at T tokens.  Shape fields may be overridden to
-    draw smaller cases of the same recipe (tests)."""
+    draw smaller cases of the same recipe (tests).  With `base`, its weights
+    are reused and only the tokens are drawn (a sweep over T)."""
     c = dict(CONFIGS[cfg])
     T = c["sweep"][0] if T is None else T
+    if base is not None:
+        H, I, E, k = base.H, base.I, base.E, base.k
     H = c["H"] if H is None else H
     I = c["I"] if I is None else I
     E = c["E"] if E is None else E
     k = c["k"] if k is None else k
     wseed = 1000 * cfg if weight_seed is None else weight_seed
-    tseed = 1000 * cfg + T if token_seed is None else token_seed
-    gt = _gen(tseed, device)
-    x = torch.randn((T, H), generator=gt, device=device).bfloat16()
+    x, ids, w = make_tokens(cfg, T, H, E, k, device, token_seed)
     wl = Workload(name=c["name"], T=T, H=H, I=I, E=E, k=k, mode=c["mode"], out=c["out"], x=x,
-                  meta=dict(config=cfg, weight_seed=wseed, token_seed=tseed))
-    for key, v in expert_weights(H, I, E, c["mode"], wseed, device).items():
-        setattr(wl, key, v)
-    if c["routing"] == "router":
-        x[:, 0] = 1.0
-        wl.wr = zipf_router_weights(H, E, c["zipf_s"], wseed + 1, device)
-        wl.router_fn, wl.router_scale = 0, 1.0
+                  topk_ids=ids, topk_w=w,
+                  meta=dict(config=cfg, weight_seed=wseed,
+                            token_seed=1000 * cfg + T if token_seed is None else token_seed))
+    if base is not None:
+        for key in ("w13", "w2", "w13q", "w13s", "w2q", "w2s", "wr"):
+            setattr(wl, key, getattr(base, key))
     else:
-        wl.topk_ids, wl.topk_w = synth_routing(T, E, k, c["routing"], c["scale"], gt, device)
+        for key, v in expert_weights(H, I, E, c["mode"], wseed, device).items():
+            setattr(wl, key, v)
+        if c["routing"] == "router":
+            wl.wr = zipf_router_weights(H, E, c["zipf_s"], wseed + 1, device)
+    if c["routing"] == "router":
+        wl.router_fn, wl.router_scale = 0, 1.0
     return wl
 
 
