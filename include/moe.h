@@ -115,6 +115,9 @@ typedef struct {
    * last one (index 6).  NULL entries are skipped.  Recording events between
    * stages serialises them (PDL overlap is lost); use for profiling only. */
   void* stage_events[8];
+  /* 1: run SiLU-and-mul as its own stage even where the plan fuses it into
+   * the Gate-Up epilogue (BF16 layer with an unsplit Gate-Up). */
+  int32_t separate_act;
 } moe_forward_opts;
 
 /* Where moe_forward keeps its intermediates inside the caller's workspace
@@ -123,12 +126,12 @@ typedef struct {
   int32_t block_m, tiles_cap, rows_cap;
   int32_t split_gateup, split_down;    /* split-K counts S1, S2 */
   int32_t grid_gateup, grid_down;      /* persistent CTAs per GEMM */
-  int32_t reserved;
+  int32_t fused_act;   /* 1: SiLU-and-mul runs in the Gate-Up epilogue (no G) */
   size_t off_counts, off_offsets, off_sorted_ids, off_tile_expert, off_tiles,
       off_inv_pos, off_num_tiles;
   size_t off_xq;   /* FP8: e4m3 x            [T][H]                         */
   size_t off_xs;   /* FP8: fp32 x scales     [T][H/128]                     */
-  size_t off_g;    /* fp32 Gate-Up partials  [S1][rows_cap][2I]             */
+  size_t off_g;    /* fp32 Gate-Up partials  [S1][rows_cap][2I] (0 bytes when fused_act) */
   size_t off_a;    /* activation: bf16 [rows_cap][I] or e4m3 [rows_cap][I]  */
   size_t off_as;   /* FP8: fp32 act scales   [rows_cap][I/128]              */
   size_t off_y;    /* fp32 Down partials     [S2][rows_cap][H] (sorted rows)*/

@@ -44,13 +44,13 @@ class moe_scales(ctypes.Structure):
 
 class moe_forward_opts(ctypes.Structure):
     _fields_ = [("disable_pdl", _i32), ("split_gateup", _i32), ("split_down", _i32),
-                ("grid_ctas", _i32), ("stage_events", _vp * 8)]
+                ("grid_ctas", _i32), ("stage_events", _vp * 8), ("separate_act", _i32)]
 
 
 class moe_workspace_layout(ctypes.Structure):
     _fields_ = [("block_m", _i32), ("tiles_cap", _i32), ("rows_cap", _i32),
                 ("split_gateup", _i32), ("split_down", _i32), ("grid_gateup", _i32),
-                ("grid_down", _i32), ("reserved", _i32)] + [
+                ("grid_down", _i32), ("fused_act", _i32)] + [
         (n, _sz) for n in ("off_counts", "off_offsets", "off_sorted_ids", "off_tile_expert",
                            "off_tiles", "off_inv_pos", "off_num_tiles", "off_xq", "off_xs",
                            "off_g", "off_a", "off_as", "off_y", "total_bytes")]
@@ -138,9 +138,10 @@ def moe_index_tiles_cap(T, k, E, block_m) -> int:
 
 
 def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
-              stage_events=None) -> moe_forward_opts:
+              stage_events=None, separate_act=False) -> moe_forward_opts:
     o = moe_forward_opts()
     o.disable_pdl = int(disable_pdl)
+    o.separate_act = int(separate_act)
     o.split_gateup = split_gateup
     o.split_down = split_down
     o.grid_ctas = grid_ctas
@@ -290,9 +291,11 @@ def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None) -> dic
         tiles=v(L.off_tiles, 4 * tc, torch.int32, (tc, 4)),
         inv_pos=v(L.off_inv_pos, T * k, torch.int32, (T * k,)),
         num_tiles=v(L.off_num_tiles, 1, torch.int32, (1,)),
-        G=v(L.off_g, L.split_gateup * rc * 2 * I, torch.float32, (L.split_gateup, rc, 2 * I)),
         Y=v(L.off_y, L.split_down * rc * H, torch.float32, (L.split_down, rc, H)),
     )
+    if not L.fused_act:
+        out["G"] = v(L.off_g, L.split_gateup * rc * 2 * I, torch.float32,
+                     (L.split_gateup, rc, 2 * I))
     if fp8:
         out["xq"] = v(L.off_xq, T * H, torch.uint8, (T, H))
         out["xs"] = v(L.off_xs, T * (H // 128), torch.float32, (T, H // 128))

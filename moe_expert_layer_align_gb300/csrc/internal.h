@@ -33,6 +33,8 @@ struct GemmParams {
   const float* w_scale;      // FP8: [E][M/128][K/128]
   const float* b_scale;      // FP8: gather [T][K/128]; direct [rows_cap][K/128]
   float* out;                // [splits][rows_cap][M] fp32 partial sums
+  void* act_out;             // Gate-Up, bf16, one split: SiLU(g)*u as bf16 [rows_cap][I]
+                             // instead of the partial sums
   int rows_cap;              // rows of one split slice of `out`
   int32_t* dev_status;
 };

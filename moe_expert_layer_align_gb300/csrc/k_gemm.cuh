@@ -4,7 +4,10 @@
 // Role in the layer (HPC-Ops × SGLang, section "MoE", fused pipeline): the
 // "Gate-Up GEMM reads the original token rows through the routing index" and
 // the Down GEMM is "the same persistent task-map expert GEMM".  The same
-// kernel also runs the router's two-bf16 GEMM (section "Router GEMM").
+// kernel also runs the router's two-bf16 GEMM (section "Router GEMM").  For
+// the bf16 layer with an unsplit Gate-Up, the epilogue also applies the
+// SiLU-and-mul of section "MoE", "Gate-Up and activation" and writes the
+// activation Down reads, so no separate activation stage runs.
 //
 // Orientation ("swap-AB"): the MMA's M side is always 128 weight rows, the N
 // side (BN = block_m) is the token tile.  A decode-sized expert group of a
@@ -14,10 +17,10 @@
 // tile's expert:
 //   out[ks][row0 + n][col(m)] = sum_{k in split ks} W[e][row(m)][k] * B[n][k]
 // where B[n] is x[sorted_ids[row0+n] / topk] (gather), row row0+n of the
-// activation (direct) or row q*BN+n of x (dense).  Gate-Up pairs the tile:
-// TMEM lanes 0..63 hold gate rows mt*64.., lanes 64..127 the matching up rows
-// I + mt*64.., so a later fused SiLU-and-mul epilogue finds both halves in one
-// tile.  Split-K partial sums are written in fp32 and reduced, in a fixed
+// activation (direct) or row q*BN+n of x (dense).  Gate-Up pairs the tile per
+// 32-lane TMEM quadrant q: lanes 32q..32q+15 hold gate rows mt*64+16q.. and
+// lanes 32q+16..32q+31 the matching up rows I+mt*64+16q.., so each gate/up
+// pair meets inside one warp (a shuffle apart).  Split-K partial sums are written in fp32 and reduced, in a fixed
 // order, by the next stage (act or combine): nothing is accumulated with
 // atomics.
 //
@@ -39,6 +42,8 @@
 // the kernel ORs kStatusTimeout into dev_status, drains its own copies and
 // MMAs, frees TMEM and returns.
 #pragma once
+#include <cuda_bf16.h>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -180,8 +185,9 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           const int kc = kt * S::kElemsPerStage;
           mbar_arrive_expect_tx(full, bytes);
           if (BSRC == kGather) {
-            tma_load_3d(a_dst, &tmA, full, kc, w.mt * 64, w.e);
-            tma_load_3d(a_dst + 64 * kKBytes, &tmA, full, kc, p.I + w.mt * 64, w.e);
+            // one box of the 5-D view (K, 16 rows, gate|up, 16-row group,
+            // expert): smem rows 32q..32q+15 gate rows, 32q+16.. up rows
+            tma_load_5d(a_dst, &tmA, full, kc, 0, 0, w.mt * 4, w.e);
           } else {
             tma_load_3d(a_dst, &tmA, full, kc, w.mt * kTileM, w.e);
             tma_load_2d(sB + stage * S::kBBytes, &tmB, full, kc, w.row0);
@@ -284,8 +290,9 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
       const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
       int col;
       bool col_ok = true;
+      const int feat = w.mt * 64 + qd * 16 + (lane & 15);  // Gate-Up: this lane's channel
       if (BSRC == kGather) {
-        col = (r < 64) ? (w.mt * 64 + r) : (p.I + w.mt * 64 + (r - 64));
+        col = lane < 16 ? feat : p.I + feat;
       } else {
         col = w.mt * kTileM + r;
         col_ok = col < p.M;
@@ -297,16 +304,37 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           break;
         }
         tc_fence_after();
+        const bool fuse = BSRC == kGather && p.act_out != nullptr;
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c) {
           if (c * 16 < w.rows) {
             uint32_t v[16];
             tmem_ld16(t_lane + static_cast<uint32_t>(ab * BN + c * 16), v);
             tmem_ld_wait();
+            if (fuse) {
+              // lanes 0..15 hold gate, 16..31 the matching up: swap halves, then
+              // lanes 0..15 finish columns 0..7 of the chunk, lanes 16..31 8..15.
+              const bool lo = lane < 16;
+              __nv_bfloat16* arow = static_cast<__nv_bfloat16*>(p.act_out) +
+                                    static_cast<size_t>(w.row0) * p.I + feat;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int n = c * 16 + j;
-              if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = __uint_as_float(v[j]);
+              for (int jj = 0; jj < 8; ++jj) {
+                const float mine_a = __uint_as_float(v[jj]);
+                const float mine_b = __uint_as_float(v[8 + jj]);
+                const float peer_a = __shfl_xor_sync(0xffffffffu, mine_a, 16);
+                const float peer_b = __shfl_xor_sync(0xffffffffu, mine_b, 16);
+                const float g = lo ? mine_a : peer_b;
+                const float u = lo ? peer_a : mine_b;
+                const int n = c * 16 + (lo ? jj : 8 + jj);
+                if (n < w.rows)
+                  arow[static_cast<size_t>(n) * p.I] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int n = c * 16 + j;
+                if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = __uint_as_float(v[j]);
+              }
             }
           }
         }
@@ -328,7 +356,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
             row = (BSRC == kGather) ? __ldg(p.sorted_ids + w.row0 + n) / p.topk : w.row0 + n;
           srow[i] = row;
         }
-        const int blk = (BSRC == kGather) ? ((r < 64 ? w.mt * 64 : p.I + w.mt * 64) >> 7) : w.mt;
+        const int blk = (BSRC == kGather) ? ((lane < 16 ? w.mt * 64 : p.I + w.mt * 64) >> 7) : w.mt;
         const float* wsp = p.w_scale + (static_cast<size_t>(w.e) * (p.M >> 7) + blk) * KB;
         float acc[BN];
 #pragma unroll

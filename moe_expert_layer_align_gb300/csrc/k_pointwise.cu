@@ -61,64 +61,67 @@ cudaError_t launch_quant_x(const void* x, int T, int H, uint8_t* xq, float* xs, 
 // BF16: A[p][i] = bf16(a).  FP8: per 128 channels s = amax/448, codes e4m3.
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+constexpr int kActThreads = 256;
+
 template <int FP8>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kActThreads)
     moe_act_kernel(const float* __restrict__ G, int splits, int rows_cap, int I,
                    const int32_t* __restrict__ sorted_ids, int sentinel, void* __restrict__ A,
                    float* __restrict__ As) {
   pdl_wait();
   pdl_launch_dependents();
-  const int p = blockIdx.x;
-  if (__ldg(sorted_ids + p) >= sentinel) return;  // padding row
-  const int i = (blockIdx.y * 128 + threadIdx.x) * 4;
-  // FP8: a warp covers one whole 128-channel group, so this exit is
-  // warp-uniform and the group's shuffles stay complete.
-  if (i >= I) return;
   const size_t two_i = 2 * static_cast<size_t>(I);
   const size_t slice = static_cast<size_t>(rows_cap) * two_i;
-  float v[4];
-  {
-    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+  // Block-strided over index rows, thread-strided over 4-channel groups.  In
+  // FP8 mode a warp covers one whole 128-channel group per iteration (the
+  // loop bound is warp-uniform because I % 128 == 0).
+  for (int p = blockIdx.x; p < rows_cap; p += gridDim.x) {
+    if (__ldg(sorted_ids + p) >= sentinel) continue;  // padding row (block-uniform)
     const float* row = G + static_cast<size_t>(p) * two_i;
-    for (int s = 0; s < splits; ++s) {
-      const float4 gs = __ldg(reinterpret_cast<const float4*>(row + s * slice + i));
-      const float4 us = __ldg(reinterpret_cast<const float4*>(row + s * slice + I + i));
-      g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
-      u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
+    for (int i = threadIdx.x * 4; i < I; i += kActThreads * 4) {
+      float4 g = __ldg(reinterpret_cast<const float4*>(row + i));
+      float4 u = __ldg(reinterpret_cast<const float4*>(row + I + i));
+      for (int s = 1; s < splits; ++s) {
+        const float4 gs = __ldg(reinterpret_cast<const float4*>(row + s * slice + i));
+        const float4 us = __ldg(reinterpret_cast<const float4*>(row + s * slice + I + i));
+        g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
+        u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
+      }
+      float v[4] = {silu_mul(g.x, u.x), silu_mul(g.y, u.y), silu_mul(g.z, u.z),
+                    silu_mul(g.w, u.w)};
+      if (FP8) {
+        float sc;
+        const uint32_t q = quant_group4(v, &sc);
+        uint8_t* Aq = static_cast<uint8_t*>(A);
+        *reinterpret_cast<uint32_t*>(Aq + static_cast<size_t>(p) * I + i) = q;
+        if ((threadIdx.x & 31) == 0) As[static_cast<size_t>(p) * (I / 128) + i / 128] = sc;
+      } else {
+        __nv_bfloat16* Ab = static_cast<__nv_bfloat16*>(A) + static_cast<size_t>(p) * I + i;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(Ab) = packed;
+      }
     }
-    v[0] = silu_mul(g.x, u.x);
-    v[1] = silu_mul(g.y, u.y);
-    v[2] = silu_mul(g.z, u.z);
-    v[3] = silu_mul(g.w, u.w);
-  }
-  if (FP8) {
-    float s;
-    const uint32_t q = quant_group4(v, &s);
-    uint8_t* Aq = static_cast<uint8_t*>(A);
-    *reinterpret_cast<uint32_t*>(Aq + static_cast<size_t>(p) * I + i) = q;
-    if ((threadIdx.x & 31) == 0) As[static_cast<size_t>(p) * (I / 128) + i / 128] = s;
-  } else {
-    __nv_bfloat16* Ab = static_cast<__nv_bfloat16*>(A) + static_cast<size_t>(p) * I + i;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(Ab) = packed;
   }
 }
 
 cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
                        const int32_t* sorted_ids, int sentinel, void* A, float* As,
                        cudaStream_t st, bool pdl) {
-  // 128 threads x 4 channels per block column; FP8 needs I % 128 == 0 so that
-  // every warp holds one whole 128-channel group.
-  const dim3 grid(rows_cap, (I + 511) / 512);
+  // A few resident blocks per SM walk all rows: launching one block per
+  // (row, column chunk) spent most of the stage scheduling blocks of padding.
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = rows_cap < 4 * sms ? rows_cap : 4 * sms;
   if (fp8)
-    return launch_kernel(moe_act_kernel<1>, grid, dim3(128), 0, st, pdl, G, splits, rows_cap, I,
-                         sorted_ids, sentinel, A, As);
-  return launch_kernel(moe_act_kernel<0>, grid, dim3(128), 0, st, pdl, G, splits, rows_cap, I,
-                       sorted_ids, sentinel, A, As);
+    return launch_kernel(moe_act_kernel<1>, dim3(grid), dim3(kActThreads), 0, st, pdl, G, splits,
+                         rows_cap, I, sorted_ids, sentinel, A, As);
+  return launch_kernel(moe_act_kernel<0>, dim3(grid), dim3(kActThreads), 0, st, pdl, G, splits,
+                       rows_cap, I, sorted_ids, sentinel, A, As);
 }
 
 // ---------------------------------------------------------------- combine
@@ -126,6 +129,8 @@ cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
 // weighted reduction restores expert outputs to token order.
 //   out[t][h] = sum_{j ascending} w[t][j] * sum_{s ascending} Y[s][inv_pos[t*k+j]][h]
 // fp32, fixed order, no atomics.
+constexpr int kCombineBatch = 8;   // assignments whose rows are loaded together
+
 __global__ void __launch_bounds__(128)
     moe_combine_kernel(const float* __restrict__ Y, int splits, int rows_cap, int H,
                        const int32_t* __restrict__ inv_pos, const float* __restrict__ topk_w,
@@ -137,20 +142,39 @@ __global__ void __launch_bounds__(128)
   if (h >= H) return;
   const size_t slice = static_cast<size_t>(rows_cap) * H;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const int pos = __ldg(inv_pos + static_cast<size_t>(t) * k + j);
-    if (pos < 0) continue;
-    const float w = __ldg(topk_w + static_cast<size_t>(t) * k + j);
-    const float* row = Y + static_cast<size_t>(pos) * H + h;
-    float4 y = __ldg(reinterpret_cast<const float4*>(row));
-    for (int s = 1; s < splits; ++s) {
-      const float4 ys = __ldg(reinterpret_cast<const float4*>(row + s * slice));
-      y.x += ys.x; y.y += ys.y; y.z += ys.z; y.w += ys.w;
+  for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+    // Issue every row load of the batch before reducing: the reduction order
+    // (splits ascending, then j ascending) is unchanged.
+    int pos[kCombineBatch];
+    float w[kCombineBatch];
+    float4 y[kCombineBatch];
+#pragma unroll
+    for (int b = 0; b < kCombineBatch; ++b) {
+      const int j = j0 + b;
+      pos[b] = j < k ? __ldg(inv_pos + static_cast<size_t>(t) * k + j) : -1;
+      w[b] = j < k ? __ldg(topk_w + static_cast<size_t>(t) * k + j) : 0.f;
     }
-    acc.x = fmaf(w, y.x, acc.x);
-    acc.y = fmaf(w, y.y, acc.y);
-    acc.z = fmaf(w, y.z, acc.z);
-    acc.w = fmaf(w, y.w, acc.w);
+#pragma unroll
+    for (int b = 0; b < kCombineBatch; ++b)
+      y[b] = pos[b] >= 0 ? __ldg(reinterpret_cast<const float4*>(Y + static_cast<size_t>(pos[b]) * H + h))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 1; s < splits; ++s) {
+#pragma unroll
+      for (int b = 0; b < kCombineBatch; ++b) {
+        if (pos[b] < 0) continue;
+        const float4 ys = __ldg(reinterpret_cast<const float4*>(
+            Y + s * slice + static_cast<size_t>(pos[b]) * H + h));
+        y[b].x += ys.x; y[b].y += ys.y; y[b].z += ys.z; y[b].w += ys.w;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kCombineBatch; ++b) {
+      if (pos[b] < 0) continue;   // dropped assignment contributes 0
+      acc.x = fmaf(w[b], y[b].x, acc.x);
+      acc.y = fmaf(w[b], y[b].y, acc.y);
+      acc.z = fmaf(w[b], y[b].z, acc.z);
+      acc.w = fmaf(w[b], y[b].w, acc.w);
+    }
   }
   const size_t o = static_cast<size_t>(t) * H + h;
   if (out_bf16) {

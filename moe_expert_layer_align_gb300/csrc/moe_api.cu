@@ -27,6 +27,7 @@ struct Plan {
   int tiles_cap, rows_cap;
   int s1, kts1, kt1, mt1;  // Gate-Up: splits, k-tiles per split, k-tiles, weight tiles
   int s2, kts2, kt2, mt2;  // Down
+  int fused_act;           // SiLU-and-mul in the Gate-Up epilogue
   size_t off[13];
   size_t total;
 };
@@ -137,6 +138,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
     p->kts2 = (p->kt2 + o->split_down - 1) / o->split_down;
     p->s2 = (p->kt2 + p->kts2 - 1) / p->kts2;
   }
+  p->fused_act = !p->fp8 && p->s1 == 1 && !(o && o->separate_act);
   // workspace layout
   const size_t tk = static_cast<size_t>(s->T) * s->k;
   const size_t rc = p->rows_cap;
@@ -150,7 +152,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
       4,
       p->fp8 ? static_cast<size_t>(s->T) * s->H : 0,
       p->fp8 ? 4 * static_cast<size_t>(s->T) * (s->H / 128) : 0,
-      4 * static_cast<size_t>(p->s1) * rc * 2 * s->I,
+      p->fused_act ? 0 : 4 * static_cast<size_t>(p->s1) * rc * 2 * s->I,
       rc * s->I * (p->fp8 ? 1 : 2),
       p->fp8 ? 4 * rc * (s->I / 128) : 0,
       4 * static_cast<size_t>(p->s2) * rc * s->H,
@@ -173,6 +175,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->split_down = p.s2;
   L->grid_gateup = kPlanCtas;
   L->grid_down = kPlanCtas;
+  L->fused_act = p.fused_act;
   L->off_counts = p.off[kOffCounts];
   L->off_offsets = p.off[kOffOffsets];
   L->off_sorted_ids = p.off[kOffSorted];
@@ -244,6 +247,25 @@ bool make_map_3d(CUtensorMap* m, const void* base, int esize, uint64_t cols, uin
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Gate-Up weights W13 [experts][2I][cols] as the 5-D view
+// (cols, 16 rows, gate|up, I/16 row groups, experts): one box of
+// {128 bytes, 16, 2, 4, 1} brings 64 gate rows and their 64 up rows,
+// interleaved 16 by 16, in a single copy.
+bool make_map_gateup(CUtensorMap* m, const void* base, int esize, uint64_t cols, uint64_t I,
+                     uint64_t experts) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t row = cols * esize;
+  const cuuint64_t dims[5] = {cols, 16, 2, I / 16, experts};
+  const cuuint64_t strides[4] = {row, I * row, 16 * row, 2 * I * row};
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(128 / esize), 16, 2, 4, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -364,7 +386,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   const int tk = p.T * p.k;
 
   CUtensorMap tmW13, tmX, tmW2, tmA;
-  if (!make_map_3d(&tmW13, w13, esize, p.H, 2ull * p.I, p.E, 64) ||
+  if (!make_map_gateup(&tmW13, w13, esize, p.H, p.I, p.E) ||
       !make_map_2d(&tmX, p.fp8 ? static_cast<const void*>(xq) : x, esize, p.H, p.T, 1) ||
       !make_map_3d(&tmW2, w2, esize, p.I, p.H, p.E, 128) ||
       !make_map_2d(&tmA, A, esize, p.I, p.rows_cap, p.bm))
@@ -403,6 +425,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g1.w_scale = p.fp8 ? scales->w13_scale : nullptr;
   g1.b_scale = p.fp8 ? xs : nullptr;
   g1.out = G;
+  g1.act_out = p.fused_act ? A : nullptr;
   g1.rows_cap = p.rows_cap;
   g1.dev_status = dev_status;
   const int units1 = p.mt1 * p.s1 * p.tiles_cap;
@@ -410,8 +433,10 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   record(opts, 3, s);
-  e = launch_act(p.fp8, G, p.s1, p.rows_cap, p.I, ip.sorted_ids, tk, A, As, s, pdl);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (!p.fused_act) {
+    e = launch_act(p.fp8, G, p.s1, p.rows_cap, p.I, ip.sorted_ids, tk, A, As, s, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
 
   record(opts, 4, s);
   GemmParams g2 = {};

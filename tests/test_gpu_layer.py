@@ -50,39 +50,52 @@ def test_every_block_m(bm, mode_cfg):
     assert_layer_close(got, oracle_layer(wl), wl.mode, f"bm={bm}")
 
 
-@pytest.mark.parametrize("s1,s2", [(1, 1), (2, 3), (4, 8), (3, 1)])
+@pytest.mark.parametrize("s1,s2,sep", [(1, 1, False), (1, 2, True), (2, 3, False),
+                                        (4, 8, False), (3, 1, False)])
 @pytest.mark.parametrize("mode_cfg", [2, 4])
-def test_forced_splits_and_no_pdl(s1, s2, mode_cfg):
+def test_forced_splits_and_no_pdl(s1, s2, sep, mode_cfg):
     import moe_expert_layer_align_gb300 as moe
     kw = dict(H=1024, I=512, E=8) if mode_cfg == 4 else dict(H=1024, I=512, E=8)
     wl = small(mode_cfg, 24, **kw)
-    opts = moe.make_opts(disable_pdl=(s1 == 3), split_gateup=s1, split_down=s2)
+    opts = moe.make_opts(disable_pdl=(s1 == 3), split_gateup=s1, split_down=s2,
+                         separate_act=sep)
     got = run_layer(wl, opts=opts).float().cpu().numpy()
     assert_layer_close(got, oracle_layer(wl), wl.mode, f"splits {s1},{s2}")
 
 
-def test_intermediates_bf16():
+@pytest.mark.parametrize("fused", [True, False])
+def test_intermediates_bf16(fused):
     import moe_expert_layer_align_gb300 as moe
     wl = small(2, 33, H=256, I=128, E=4)
+    # unsplit Gate-Up fuses SiLU-and-mul into its epilogue; a split one
+    # leaves fp32 partials for the separate stage
+    opts = moe.make_opts(split_gateup=1 if fused else 2)
     shape = moe.layer_shape(wl.x, wl.w13, wl.topk_ids, 0, torch.bfloat16)
-    ws = torch.zeros(moe.moe_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
-    run_layer(wl, workspace=ws)
+    ws = torch.zeros(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
+    run_layer(wl, workspace=ws, opts=opts)
     torch.cuda.synchronize()
-    v = moe.workspace_views(ws, shape)
+    v = moe.workspace_views(ws, shape, opts)
+    assert v["layout"].fused_act == int(fused)
     ref = oracle.align(wl.topk_ids.cpu().numpy(), wl.E, v["layout"].block_m)
     for n in ("counts", "offsets", "sorted_ids", "tile_expert", "tiles", "inv_pos", "num_tiles"):
         np.testing.assert_array_equal(v[n].cpu().numpy().reshape(-1), ref[n].reshape(-1), n)
-    # Gate-Up partial sums of every valid row against fp64 products
+    # Gate-Up sums (split case) and the bf16 activation of every valid row
+    # against fp64 products
     sid = ref["sorted_ids"]
     X = wl.x.double().cpu().numpy()
     W13 = wl.w13.double().cpu().numpy()
-    G = v["G"].sum(0).double().cpu().numpy()
+    A = v["A"].double().cpu().numpy()
+    G = None if fused else v["G"].sum(0).double().cpu().numpy()
     rows = np.flatnonzero(sid < wl.T * wl.k)
+    I = wl.I
     for p in rows:
         a = sid[p]
         e = wl.topk_ids.reshape(-1)[a].item()
         g_ref = W13[e] @ X[a // wl.k]
-        np.testing.assert_allclose(G[p], g_ref, rtol=1e-4, atol=1e-4 * np.abs(g_ref).max())
+        if G is not None:
+            np.testing.assert_allclose(G[p], g_ref, rtol=1e-4, atol=1e-4 * np.abs(g_ref).max())
+        act = g_ref[:I] / (1 + np.exp(-g_ref[:I])) * g_ref[I:]
+        np.testing.assert_allclose(A[p], act, rtol=1e-2, atol=1e-2 * np.abs(act).max())
 
 
 def test_intermediates_fp8_codes():
