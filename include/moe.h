@@ -104,7 +104,9 @@ typedef struct {
   const float* w2_scale;   /* [E][H/128][I/128]  */
 } moe_scales;
 
-/* Options of moe_forward_ex (zero-initialised = defaults of moe_forward). */
+/* Options of moe_forward_ex (zero-initialised = defaults of moe_forward).
+ * Stage events: with the shared-memory index there is no align stage (its
+ * two events are recorded back to back). */
 typedef struct {
   int32_t disable_pdl;      /* 1: plain stream order instead of PDL chaining */
   int32_t split_gateup;     /* 0: planner; else forced split-K count, Gate-Up */
@@ -118,6 +120,10 @@ typedef struct {
   /* 1: run SiLU-and-mul as its own stage even where the plan fuses it into
    * the Gate-Up epilogue (BF16 layer with an unsplit Gate-Up). */
   int32_t separate_act;
+  /* 1: every GEMM CTA rebuilds the routing index from the top-k ids in its
+   * shared memory (T*k <= 4096 and room next to the pipeline), instead of
+   * the separate index kernel; the Gate-Up writes the index out. */
+  int32_t smem_index;
 } moe_forward_opts;
 
 /* Where moe_forward keeps its intermediates inside the caller's workspace
@@ -127,10 +133,14 @@ typedef struct {
   int32_t split_gateup, split_down;    /* split-K counts S1, S2 */
   int32_t grid_gateup, grid_down;      /* persistent CTAs per GEMM */
   int32_t fused_act;   /* 1: SiLU-and-mul runs in the Gate-Up epilogue (no G) */
+  int32_t smem_index;  /* 1: GEMM CTAs rebuild the index in shared memory; the
+                          Gate-Up writes it out (no separate index kernel) */
+  int32_t reserved;
   size_t off_counts, off_offsets, off_sorted_ids, off_tile_expert, off_tiles,
       off_inv_pos, off_num_tiles;
   size_t off_xq;   /* FP8: e4m3 x            [T][H]                         */
   size_t off_xs;   /* FP8: fp32 x scales     [T][H/128]                     */
+  size_t off_xs_rows; /* FP8: the same scales in index-row order [rows_cap][H/128] */
   size_t off_g;    /* fp32 Gate-Up partials  [S1][rows_cap][2I] (0 bytes when fused_act) */
   size_t off_a;    /* activation: bf16 [rows_cap][I] or e4m3 [rows_cap][I]  */
   size_t off_as;   /* FP8: fp32 act scales   [rows_cap][I/128]              */

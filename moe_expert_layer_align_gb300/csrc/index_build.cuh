@@ -1,0 +1,158 @@
+// index_build.cuh — the routing and index build as block-level device code.
+//
+// HPC-Ops × SGLang, section "MoE", fused pipeline, "routing and index build":
+// a shared-memory counting pass arranges token-expert assignments into
+// contiguous per-expert intervals without global atomics and emits the tile
+// task map the persistent expert GEMM consumes.
+//
+// One thread block builds the whole index.  Warp w of the block owns the
+// contiguous slice [w*seg, (w+1)*seg) of the flat assignments a = t*k + j and
+// walks it in rounds of 32 (one assignment per lane):
+//   1. count: __match_any_sync groups a round's lanes by expert and the
+//      group's lowest lane adds the group size to cnt[w][e] (one writer per
+//      address, no atomics);
+//   2. scan: per expert an exclusive prefix of cnt[.][e] over the warps gives
+//      each warp's base inside the expert; a warp scan of the counts rounded
+//      up to block_m gives offsets[];
+//   3. scatter: the same rounds again; an assignment's row is
+//      offsets[e] + base[w][e] + (lanes of its group below it).
+// Slices ascend in a, rounds run in order and ranks inside a round follow the
+// lane, so each interval lists its assignments in ascending a: the result is
+// unique and deterministic.  The caller chooses where rows and tiles go (the
+// align kernel writes global memory; the GEMM's prologue, shared memory).
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ int lanemask_lt() {
+  int m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Shared-memory scratch of one index build.
+struct IndexScratch {
+  int32_t* cnt;    // [nwarps][E]: per-warp counts, then per-warp bases
+  int32_t* offs;   // [E + 1]: padded offsets
+  int32_t* tot;    // [E]: per-expert counts
+  int32_t* flag;   // [1]: an invalid id was seen
+  static __host__ __device__ constexpr size_t words(int nwarps, int E) {
+    return static_cast<size_t>(nwarps) * E + (E + 1) + E + 1;
+  }
+  __device__ void carve(int32_t* base, int nwarps, int E) {
+    cnt = base;
+    offs = cnt + nwarps * E;
+    tot = offs + E + 1;
+    flag = tot + E;
+  }
+};
+
+// Steps 1-2: counts, per-warp bases and padded offsets, all in `sc`.  `src`
+// holds the T*k ids (shared or global memory).  Ends with a block barrier.
+__device__ __forceinline__ void index_count_and_scan(const int32_t* src, int tk, int E, int bm,
+                                                     const IndexScratch& sc) {
+  const int tid = threadIdx.x, nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < nwarps * E; i += nthreads) sc.cnt[i] = 0;
+  if (tid == 0) *sc.flag = 0;
+  __syncthreads();
+  const int seg = (tk + nwarps - 1) / nwarps;
+  const int beg = min(tk, warp * seg);
+  const int end = min(tk, beg + seg);
+  for (int base = beg; base < end; base += 32) {
+    const int a = base + lane;
+    const bool in = a < end;
+    const int e = in ? src[a] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    if (in && !valid) *sc.flag = 1;
+    const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1);
+    if (valid && lane == __ffs(grp) - 1) sc.cnt[warp * E + e] += __popc(grp);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += nthreads) {
+    int run = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = sc.cnt[w * E + e];
+      sc.cnt[w * E + e] = run;
+      run += c;
+    }
+    sc.tot[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of the padded counts: warp 0, each lane a run of experts
+  if (warp == 0) {
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int sum = 0;
+    for (int e = e0; e < e1; ++e) sum += (sc.tot[e] + bm - 1) / bm * bm;
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int run = incl - sum;
+    for (int e = e0; e < e1; ++e) {
+      sc.offs[e] = run;
+      run += (sc.tot[e] + bm - 1) / bm * bm;
+    }
+    if (lane == 31) sc.offs[E] = incl;
+  }
+  __syncthreads();
+}
+
+// Step 3: every valid assignment a goes to row(pos, a); an invalid one to
+// invalid(a).  Uses and advances the per-warp bases in sc.cnt.  No barrier.
+template <class RowFn, class InvalidFn>
+__device__ __forceinline__ void index_scatter(const int32_t* src, int tk, int E,
+                                              const IndexScratch& sc, RowFn row,
+                                              InvalidFn invalid) {
+  const int tid = threadIdx.x, nwarps = blockDim.x >> 5;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int seg = (tk + nwarps - 1) / nwarps;
+  const int beg = min(tk, warp * seg);
+  const int end = min(tk, beg + seg);
+  for (int base = beg; base < end; base += 32) {
+    const int a = base + lane;
+    const bool in = a < end;
+    const int e = in ? src[a] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1);
+    if (valid)
+      row(sc.offs[e] + sc.cnt[warp * E + e] + __popc(grp & lanemask_lt()), a);
+    else if (in)
+      invalid(a);
+    __syncwarp();
+    if (valid && lane == __ffs(grp) - 1) sc.cnt[warp * E + e] += __popc(grp);
+    __syncwarp();
+  }
+}
+
+// Padding rows of every expert interval, then the tail [offs[E], rows_end).
+template <class PadFn>
+__device__ __forceinline__ void index_pads(int E, int rows_end, const IndexScratch& sc, PadFn pad) {
+  const int tid = threadIdx.x, nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int e = warp; e < E; e += nwarps)
+    for (int pos = sc.offs[e] + sc.tot[e] + lane; pos < sc.offs[e + 1]; pos += 32) pad(pos);
+  for (int pos = sc.offs[E] + tid; pos < rows_end; pos += nthreads) pad(pos);
+}
+
+// Task-map entry of row tile q: {expert, row_start, rows_valid, 0}, or
+// {-1, q*bm, 0, 0} past the last tile.
+__device__ __forceinline__ int4 index_tile(int q, int E, int bm, const IndexScratch& sc) {
+  const int row0 = q * bm;
+  if (row0 >= sc.offs[E]) return make_int4(-1, row0, 0, 0);
+  int lo = 0, hi = E - 1;   // largest e with offs[e] <= row0 (a non-empty expert)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sc.offs[mid] <= row0) lo = mid; else hi = mid - 1;
+  }
+  return make_int4(lo, row0, min(bm, sc.offs[lo] + sc.tot[lo] - row0), 0);
+}
+
+}  // namespace moe

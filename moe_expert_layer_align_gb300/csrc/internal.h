@@ -31,17 +31,32 @@ struct GemmParams {
   int sentinel;              // gather: T*k marks padding rows
   int dense_rows;            // dense: number of rows
   const float* w_scale;      // FP8: [E][M/128][K/128]
-  const float* b_scale;      // FP8: gather [T][K/128]; direct [rows_cap][K/128]
+  const float* b_scale;      // FP8: token-operand scales by index row [rows_cap][K/128]
   float* out;                // [splits][rows_cap][M] fp32 partial sums
   void* act_out;             // Gate-Up, bf16, one split: SiLU(g)*u as bf16 [rows_cap][I]
                              // instead of the partial sums
-  int rows_cap;              // rows of one split slice of `out`
+  int rows_cap;              // rows of one split slice of `out` (and of the index)
   int32_t* dev_status;
+  // Shared-memory index mode: every CTA rebuilds the routing index from the
+  // top-k ids in its prologue instead of reading tiles / sorted_ids.
+  int smem_index;
+  const int32_t* topk_ids;   // [T][topk], an input of the layer call
+  int T, E, tiles_cap;
+  int write_index;           // CTA 0 also writes the index to `index_out` and the
+  struct {                   // expert-id status bit to dev_status
+    int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
+  } index_out;
+  int early_weights;         // contiguous token operand: stream weights before the wait
+  int scale_by_token;        // FP8 gathered operand: b_scale rows are tokens
 };
 
-// Shared memory bytes and pipeline depth of one GEMM instantiation.
-int gemm_stages(int fp8, int bn);
-size_t gemm_smem_bytes(int fp8, int bn, int kt_per_split);
+// Bytes of the shared-memory index of one GEMM CTA (shared-memory index mode).
+size_t gemm_index_smem_bytes(int nwarps, int E, int tk, int rows_cap, int tiles_cap);
+
+// Shared memory of one GEMM instantiation without the index, and its warps.
+size_t gemm_smem_bytes(int fp8, int bn, int bsrc);
+int gemm_warps(int bn, int bsrc);
+constexpr size_t kMaxGemmSmem = 227 * 1024;
 
 // Launch the persistent GEMM (defined per mode in k_gemm_{bf16,fp8}.cu).
 cudaError_t launch_gemm_bf16(int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
@@ -58,8 +73,9 @@ struct IndexPtrs {
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                          const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st,
                          bool pdl);
-cudaError_t launch_quant_x(const void* x, int T, int H, uint8_t* xq, float* xs,
-                           cudaStream_t st, bool pdl);
+cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* inv_pos,
+                           uint8_t* xq, float* xs, float* xs_rows, cudaStream_t st, bool pdl);
+// (inv_pos / xs_rows may be null: then only the per-token scales are written)
 cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
                        const int32_t* sorted_ids, int sentinel, void* A, float* As,
                        cudaStream_t st, bool pdl);

@@ -1,5 +1,5 @@
 // k_gemm.cuh — persistent grouped expert GEMM on the 5th-generation tensor
-// cores (tcgen05, accumulators in TMEM, operands staged by TMA).
+// cores (tcgen05, accumulators in TMEM, operands staged by TMA / cp.async).
 //
 // Role in the layer (HPC-Ops × SGLang, section "MoE", fused pipeline): the
 // "Gate-Up GEMM reads the original token rows through the routing index" and
@@ -20,14 +20,24 @@
 // activation (direct) or row q*BN+n of x (dense).  Gate-Up pairs the tile per
 // 32-lane TMEM quadrant q: lanes 32q..32q+15 hold gate rows mt*64+16q.. and
 // lanes 32q+16..32q+31 the matching up rows I+mt*64+16q.., so each gate/up
-// pair meets inside one warp (a shuffle apart).  Split-K partial sums are written in fp32 and reduced, in a fixed
-// order, by the next stage (act or combine): nothing is accumulated with
-// atomics.
+// pair meets inside one warp (a shuffle apart).  Split-K partial sums are
+// written in fp32 and reduced, in a fixed order, by the next stage (act or
+// combine): nothing is accumulated with atomics.
 //
 // FP8 (e4m3, kind::f8f6f4): every 128-wide K block is its own MMA group into
-// one of two TMEM buffers; the epilogue warps read it and add
-// partial * w_scale[e][row/128][kb] * b_scale[token][kb] into fp32 registers
-// (block scales are fp32, so the product cannot be folded into the MMA).
+// one of up to 8 TMEM buffers; the epilogue warps read it and add
+// partial * w_scale[e][row/128][kb] * b_scale[row or token][kb] into fp32
+// registers (block scales are fp32, so the product cannot be folded into the
+// MMA).
+//
+// Index modes.  With few assignments every CTA rebuilds the routing index in
+// its own shared memory from the top-k ids (index_build.cuh) — an input of
+// the layer call, so this needs no wait on the previous stage; CTA 0 of the
+// Gate-Up also writes the index out for the later stages.  No separate index
+// kernel runs, the Gate-Up streams weights as soon as it starts, and the Down
+// GEMM streams its first weight stages before the previous stage has
+// finished.  With many assignments an index kernel runs first and CTAs read
+// the task map from global memory.
 //
 // Warp roles: warp 0 issues the TMA loads (weights; the token tile too when
 // its rows are contiguous), warp 1 (one thread) issues MMAs, warps 2..5 drain
@@ -38,12 +48,13 @@
 // rate of a dense load of the same bytes.)  With the accumulator in TMEM
 // instead of registers this split costs no registers, so the Hopper argument
 // for one warp group doing everything ("occupancy first, no warp
-// specialisation") does not carry over.  Every wait is bounded (kWaitLimitNs); on a timeout
-// the kernel ORs kStatusTimeout into dev_status, drains its own copies and
-// MMAs, frees TMEM and returns.
+// specialisation") does not carry over.  Every wait is bounded
+// (kWaitLimitNs); on a timeout the kernel ORs kStatusTimeout into dev_status,
+// drains its own copies and MMAs, frees TMEM and returns.
 #pragma once
 #include <cuda_bf16.h>
 
+#include "index_build.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -65,44 +76,95 @@ struct GemmShape {
   static constexpr int kGatherWarps = BSRC == kGather ? (BN >= 128 ? 2 : 1) : 0;
   static constexpr int kGatherThreads = 32 * kGatherWarps;
   static constexpr int kThreads = kRoleThreads + kGatherThreads;
+  static constexpr int kWarps = kThreads / 32;
   static constexpr int kRowsPerGatherThread = kGatherWarps ? BN / (4 * kGatherWarps) : 1;
   static constexpr int kBBytes = BN * kKBytes;
-  static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+  // TMEM accumulator buffers: two per-unit buffers for bf16; for FP8 every
+  // 128-wide K block is its own buffer, so keep up to 8 in flight (the MMA
+  // would otherwise wait on the epilogue's promotion every other K block).
+  static constexpr int kAccBufs = FP8 ? (512 / BN < 8 ? 512 / BN : 8) : 2;
+  static constexpr int kTmemCols = (kAccBufs * BN < 32) ? 32 : kAccBufs * BN;
   static constexpr int kElemsPerStage = FP8 ? 128 : 64;
   static constexpr uint32_t kIdesc = mma_idesc(FP8 ? 0u : 1u, kTileM, BN);
   static constexpr int kOffB = kStages * kABytes;
   static constexpr int kOffBar = kOffB + kStages * kBBytes;
-  static constexpr int kNumBars = 2 * kStages + 5;  // full, empty, acc_full[2], acc_empty[2], drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;  // + drain
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr size_t kSmemBytes = 1024 + kOffMisc + 16;
+  static constexpr int kOffIdx = (kOffMisc + 16 + 15) & ~15;       // shared-memory index
+  static constexpr size_t kSmemBytes = 1024 + kOffIdx;             // without the index
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0");
+};
+
+// Shared-memory index: build scratch, staged ids, sorted rows, task map.
+struct SmemIndex {
+  IndexScratch sc;
+  int32_t* ids;    // [T*k]
+  int32_t* rows;   // [rows_cap]: assignment per sorted row, T*k on padding
+  int4* tiles;     // [tiles_cap]
+  __host__ __device__ static size_t words_before_tiles(int nwarps, int E, int tk, int rows_cap) {
+    return (IndexScratch::words(nwarps, E) + tk + rows_cap + 3) & ~static_cast<size_t>(3);
+  }
+  __host__ __device__ static size_t bytes(int nwarps, int E, int tk, int rows_cap, int tiles_cap) {
+    return 4 * words_before_tiles(nwarps, E, tk, rows_cap) + 16 * static_cast<size_t>(tiles_cap);
+  }
+  __device__ void carve(int32_t* base, int nwarps, int E, int tk, int rows_cap) {
+    sc.carve(base, nwarps, E);
+    ids = base + IndexScratch::words(nwarps, E);
+    rows = ids + tk;
+    tiles = reinterpret_cast<int4*>(base + words_before_tiles(nwarps, E, tk, rows_cap));
+  }
 };
 
 struct WorkUnit {
   int mt, ks, e, row0, rows, kt0, kt1;
 };
 
+// Unit u = ((mt * splits + ks) * num_tiles + q): consecutive units share a
+// weight tile.  The task-map entry is the only memory read, so roles load
+// the next unit's entry while they work on the current one.
 template <int BN, int BSRC>
-__device__ __forceinline__ WorkUnit decode_unit(int u, int num_tiles, const GemmParams& p) {
+__device__ __forceinline__ int4 load_tile(int q, const GemmParams& p, const int4* smem_tiles) {
+  if (BSRC == kDense) return make_int4(0, q * BN, min(BN, p.dense_rows - q * BN), 0);
+  if (smem_tiles) return smem_tiles[q];
+  // L2-coherent load: the Down GEMM may read the task map before its PDL wait
+  return __ldcg(reinterpret_cast<const int4*>(p.tiles) + q);
+}
+
+__device__ __forceinline__ WorkUnit make_unit(int u, int num_tiles, int4 t, const GemmParams& p) {
   WorkUnit w;
-  const int q = u % num_tiles;
   const int r = u / num_tiles;
   w.ks = r % p.splits;
   w.mt = r / p.splits;
-  if (BSRC == kDense) {
-    w.e = 0;
-    w.row0 = q * BN;
-    w.rows = min(BN, p.dense_rows - w.row0);
-  } else {
-    const int4 t = __ldg(reinterpret_cast<const int4*>(p.tiles) + q);
-    w.e = t.x;
-    w.row0 = t.y;
-    w.rows = t.z;
-  }
+  w.e = t.x;
+  w.row0 = t.y;
+  w.rows = t.z;
   w.kt0 = w.ks * p.kt_per_split;
   w.kt1 = min(p.kt_total, w.kt0 + p.kt_per_split);
   return w;
 }
+
+// Iterates a CTA's units with the next task-map entry prefetched.
+template <int BN, int BSRC>
+struct UnitIter {
+  int u, units, num_tiles;
+  const int4* smem_tiles;
+  int4 next;
+  __device__ __forceinline__ UnitIter(int units_, int num_tiles_, const GemmParams& p,
+                                      const int4* st)
+      : u(blockIdx.x), units(units_), num_tiles(num_tiles_), smem_tiles(st) {
+    if (u < units) next = load_tile<BN, BSRC>(u % num_tiles, p, smem_tiles);
+  }
+  __device__ __forceinline__ bool valid() const { return u < units; }
+  // The current unit; starts the load of the one after it.
+  __device__ __forceinline__ WorkUnit take(const GemmParams& p) {
+    const int4 t = next;
+    const int un = u + gridDim.x;
+    if (un < units) next = load_tile<BN, BSRC>(un % num_tiles, p, smem_tiles);
+    return make_unit(u, num_tiles, t, p);
+  }
+  __device__ __forceinline__ void advance() { u += gridDim.x; }
+  __device__ __forceinline__ bool has_next() const { return u + static_cast<int>(gridDim.x) < units; }
+};
 
 __device__ __forceinline__ void report_timeout(const GemmParams& p, volatile int* abort_flag) {
   *abort_flag = 1;
@@ -122,13 +184,14 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
   const uint32_t bar_full = sA + S::kOffBar;
   const uint32_t bar_empty = bar_full + 8 * S::kStages;
   const uint32_t bar_accf = bar_empty + 8 * S::kStages;
-  const uint32_t bar_acce = bar_accf + 16;
-  const uint32_t bar_drain = bar_acce + 16;
+  const uint32_t bar_acce = bar_accf + 8 * S::kAccBufs;
+  const uint32_t bar_drain = bar_acce + 8 * S::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int tk = p.T * p.topk;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
@@ -136,7 +199,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
       mbar_init(bar_full + 8 * s, 1 + S::kGatherThreads);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < S::kAccBufs; ++b) {
       mbar_init(bar_accf + 8 * b, 1);
       mbar_init(bar_acce + 8 * b, 4);  // one arrival per epilogue warp
     }
@@ -150,29 +213,76 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), S::kTmemCols);
     tmem_relinquish();
   }
+
+  SmemIndex si;
+  const bool smem_idx = BSRC != kDense && p.smem_index;
+  if (smem_idx) {
+    // The top-k ids are an input of the call: complete before its first
+    // kernel started, so they are read without waiting on the predecessor.
+    si.carve(reinterpret_cast<int32_t*>(smem + S::kOffIdx), S::kWarps, p.E, tk, p.rows_cap);
+    for (int i = threadIdx.x; i < tk; i += S::kThreads) si.ids[i] = __ldg(p.topk_ids + i);
+    index_count_and_scan(si.ids, tk, p.E, BN, si.sc);
+    index_scatter(si.ids, tk, p.E, si.sc, [&](int pos, int a) { si.rows[pos] = a; },
+                  [](int) {});
+    index_pads(p.E, p.rows_cap, si.sc, [&](int pos) { si.rows[pos] = tk; });
+    for (int q = threadIdx.x; q < p.tiles_cap; q += S::kThreads)
+      si.tiles[q] = index_tile(q, p.E, BN, si.sc);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Everything above overlapped the previous stage; from here on we read
-  // what it wrote.
-  pdl_wait();
-  pdl_launch_dependents();
-
-  const int num_tiles = (BSRC == kDense) ? (p.dense_rows + BN - 1) / BN : __ldg(p.num_tiles);
+  int num_tiles;
+  const int4* smem_tiles = nullptr;
+  // Early start: the roles wait on the previous stage only where they read
+  // its output.  Gate-Up with the shared-memory index; Down whenever its
+  // index was written at least two stages back (the Gate-Up waited for it
+  // before letting this grid launch).
+  const bool early = smem_idx || (BSRC == kDirect && p.early_weights);
+  if (smem_idx) {
+    num_tiles = si.sc.offs[p.E] / BN;
+    smem_tiles = si.tiles;
+  } else {
+    if (!early) pdl_wait();
+    num_tiles = (BSRC == kDense) ? (p.dense_rows + BN - 1) / BN : __ldcg(p.num_tiles);
+  }
+  pdl_launch_dependents();   // dependents read nothing of ours before their own wait
   const int units = num_tiles * p.m_tiles * p.splits;
+  // assignment held by sorted row `pos`
+  auto row_assign = [&](int pos) -> int {
+    return smem_idx ? si.rows[pos] : __ldcg(p.sorted_ids + pos);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // With the shared-memory index and a contiguous token operand (Down), the
+    // first kStages weight tiles are requested before waiting on the stage
+    // that writes the token rows; their token loads follow the wait.
     int stage = 0;
     uint32_t phase = 0;
     long issued = 0;
     bool ok = true;
-    const uint32_t bytes = kABytes + (BSRC == kGather ? 0u : static_cast<uint32_t>(S::kBBytes));
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    constexpr uint32_t bytes = kABytes + (BSRC == kGather ? 0u : static_cast<uint32_t>(S::kBBytes));
+    bool b_now = !(early && BSRC == kDirect);
+    int deferred = 0;
+    auto flush_deferred = [&]() {
+      pdl_wait();
+      int i = 0;
+      for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); i < deferred && it.valid();
+           it.advance()) {
+        const WorkUnit w = it.take(p);
+        for (int kt = w.kt0; kt < w.kt1 && i < deferred; ++kt, ++i)
+          if (lane == 0)
+            tma_load_2d(sB + i * S::kBBytes, &tmB, bar_full + 8 * i, kt * S::kElemsPerStage,
+                        w.row0);
+      }
+      __syncwarp();
+      b_now = true;
+    };
+    for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); ok && it.valid(); it.advance()) {
       if (*abort_flag) break;
-      const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
+      const WorkUnit w = it.take(p);
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u)) {
           report_timeout(p, abort_flag);
@@ -190,7 +300,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
             tma_load_5d(a_dst, &tmA, full, kc, 0, 0, w.mt * 4, w.e);
           } else {
             tma_load_3d(a_dst, &tmA, full, kc, w.mt * kTileM, w.e);
-            tma_load_2d(sB + stage * S::kBBytes, &tmB, full, kc, w.row0);
+            if (b_now) tma_load_2d(sB + stage * S::kBBytes, &tmB, full, kc, w.row0);
           }
         }
         __syncwarp();
@@ -199,8 +309,10 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           stage = 0;
           phase ^= 1u;
         }
+        if (!b_now && ++deferred == S::kStages) flush_deferred();
       }
     }
+    if (!b_now) flush_deferred();   // fewer stages than the ring holds
     if (*abort_flag && lane == 0) {
       // Let our own copies land before the CTA can exit.
       const long first = issued > S::kStages ? issued - S::kStages : 0;
@@ -219,7 +331,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         if (*abort_flag) break;
-        const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
+        const WorkUnit w = make_unit(u, num_tiles, make_int4(0, 0, 0, 0), p);  // K range only
         if (!FP8) {
           if (!mbar_wait(bar_acce + 8 * ab, aph ^ 1u)) {
             report_timeout(p, abort_flag);
@@ -263,14 +375,18 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           }
           if (FP8) {
             tc_commit(bar_accf + 8 * ab);
-            ab ^= 1;
-            if (ab == 0) aph ^= 1u;
+            if (++ab == S::kAccBufs) {
+              ab = 0;
+              aph ^= 1u;
+            }
           }
         }
         if (!FP8 && ok) {
           tc_commit(bar_accf + 8 * ab);
-          ab ^= 1;
-          if (ab == 0) aph ^= 1u;
+          if (++ab == S::kAccBufs) {
+            ab = 0;
+            aph ^= 1u;
+          }
         }
       }
       if (*abort_flag) {
@@ -281,13 +397,38 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
     __syncwarp();
   } else if (warp < kRoleThreads / 32) {
     // ------------------------------------------------------------ epilogue
+    if (early) pdl_wait();   // reads scales, writes outputs the chain reads
+    if (smem_idx && p.write_index && blockIdx.x == 0) {
+      // The later stages read the index from global memory.
+      const int et = threadIdx.x - 64;
+      for (int e = et; e < p.E; e += 128) p.index_out.counts[e] = si.sc.tot[e];
+      for (int e = et; e <= p.E; e += 128) p.index_out.offsets[e] = si.sc.offs[e];
+      for (int pos = et; pos < p.rows_cap; pos += 128) {
+        const int a = si.rows[pos];
+        p.index_out.sorted_ids[pos] = a;
+        if (a < tk) p.index_out.inv_pos[a] = pos;
+      }
+      for (int a = et; a < tk; a += 128) {
+        const int e = si.ids[a];
+        if (e < 0 || e >= p.E) p.index_out.inv_pos[a] = -1;
+      }
+      for (int q = et; q < p.tiles_cap; q += 128) {
+        const int4 t = si.tiles[q];
+        p.index_out.tile_expert[q] = t.x;
+        reinterpret_cast<int4*>(p.index_out.tiles)[q] = t;
+      }
+      if (et == 0) {
+        *p.index_out.num_tiles = num_tiles;
+        if (p.dev_status) *p.dev_status = *si.sc.flag ? kStatusExpertId : 0;
+      }
+    }
     const int qd = warp & 3;          // TMEM lane quadrant this warp may read
     const int r = qd * 32 + lane;     // row of the 128-row weight tile
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
     int ab = 0;
     uint32_t aph = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
+    for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); it.valid(); it.advance()) {
+      const WorkUnit w = it.take(p);
       int col;
       bool col_ok = true;
       const int feat = w.mt * 64 + qd * 16 + (lane & 15);  // Gate-Up: this lane's channel
@@ -341,8 +482,10 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
-        ab ^= 1;
-        if (ab == 0) aph ^= 1u;
+        if (++ab == S::kAccBufs) {
+          ab = 0;
+          aph ^= 1u;
+        }
       } else {
         // Per-column scale rows: lane l serves columns l, l+32, ...
         constexpr int kCPerLane = BN / 32 > 0 ? BN / 32 : 1;
@@ -353,7 +496,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           const int n = lane + 32 * i;
           int row = -1;
           if (n < w.rows && n < BN)
-            row = (BSRC == kGather) ? __ldg(p.sorted_ids + w.row0 + n) / p.topk : w.row0 + n;
+            row = p.scale_by_token ? row_assign(w.row0 + n) / p.topk : w.row0 + n;
           srow[i] = row;
         }
         const int blk = (BSRC == kGather) ? ((lane < 16 ? w.mt * 64 : p.I + w.mt * 64) >> 7) : w.mt;
@@ -391,8 +534,10 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
-          ab ^= 1;
-          if (ab == 0) aph ^= 1u;
+          if (++ab == S::kAccBufs) {
+            ab = 0;
+            aph ^= 1u;
+          }
         }
         if (!ok) break;
 #pragma unroll
@@ -411,18 +556,24 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
     const int c = t & 7;
     const int r0 = t >> 3;
     const uint8_t* rows = static_cast<const uint8_t*>(p.b_rows) + c * 16;
+    if (early) pdl_wait();   // the token rows may come from the previous stage
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    int tok[kR];
+    bool tok_ready = false;       // tok[] already holds the current unit's rows
+    for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); ok && it.valid(); it.advance()) {
       if (*abort_flag) break;
-      const WorkUnit w = decode_unit<BN, BSRC>(u, num_tiles, p);
-      int tok[kR];
+      const WorkUnit w = it.take(p);
+      if (!tok_ready) {
 #pragma unroll
-      for (int i = 0; i < kR; ++i) {
-        const int n = r0 + kRowStep * i;
-        tok[i] = n < w.rows ? __ldg(p.sorted_ids + w.row0 + n) / p.topk : -1;
+        for (int i = 0; i < kR; ++i) {
+          const int n = r0 + kRowStep * i;
+          tok[i] = n < w.rows ? row_assign(w.row0 + n) / p.topk : -1;
+        }
       }
+      int tok_next[kR];
+      tok_ready = false;
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u)) {
           report_timeout(p, abort_flag);
@@ -443,6 +594,20 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           stage = 0;
           phase ^= 1u;
         }
+        if (kt == w.kt0 && it.has_next()) {
+          // the next unit's task-map entry has landed by now: fetch its rows
+          const int4 tn = it.next;
+#pragma unroll
+          for (int i = 0; i < kR; ++i) {
+            const int n = r0 + kRowStep * i;
+            tok_next[i] = n < tn.z ? row_assign(tn.y + n) / p.topk : -1;
+          }
+          tok_ready = true;
+        }
+      }
+      if (tok_ready) {
+#pragma unroll
+        for (int i = 0; i < kR; ++i) tok[i] = tok_next[i];
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
@@ -467,11 +632,15 @@ cudaError_t launch_gemm_inst(int grid, cudaStream_t st, bool pdl, const CUtensor
   if (err != cudaSuccess) return err;
   if (dev < 64 && !configured[dev]) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(S::kSmemBytes));
+                               static_cast<int>(kMaxGemmSmem));
     if (err != cudaSuccess) return err;
     configured[dev] = 1;
   }
-  return launch_kernel(kern, dim3(grid), dim3(S::kThreads), S::kSmemBytes, st, pdl, a, b, p);
+  size_t smem = S::kSmemBytes;
+  if (BSRC != kDense && p.smem_index)
+    smem += SmemIndex::bytes(S::kWarps, p.E, p.T * p.topk, p.rows_cap, p.tiles_cap);
+  if (smem > kMaxGemmSmem) return cudaErrorInvalidValue;
+  return launch_kernel(kern, dim3(grid), dim3(S::kThreads), smem, st, pdl, a, b, p);
 }
 
 template <int FP8, int BSRC>

@@ -14,17 +14,31 @@ cudaError_t launch_gemm_bf16(int bn, int bsrc, int grid, cudaStream_t st, bool p
   return launch_gemm_bf16_gather_dense(bn, bsrc, grid, st, pdl, a, b, p);
 }
 
-int gemm_stages(int fp8, int bn) { return stages_for(fp8, bn); }
-
-size_t gemm_smem_bytes(int fp8, int bn, int) {
+template <int FP8, int BSRC>
+size_t smem_bytes_bn(int bn) {
   switch (bn) {
-    case 16: return fp8 ? GemmShape<1, 16>::kSmemBytes : GemmShape<0, 16>::kSmemBytes;
-    case 32: return fp8 ? GemmShape<1, 32>::kSmemBytes : GemmShape<0, 32>::kSmemBytes;
-    case 64: return fp8 ? GemmShape<1, 64>::kSmemBytes : GemmShape<0, 64>::kSmemBytes;
-    case 128: return fp8 ? GemmShape<1, 128>::kSmemBytes : GemmShape<0, 128>::kSmemBytes;
-    case 256: return GemmShape<0, 256>::kSmemBytes;
+    case 16: return GemmShape<FP8, 16, BSRC>::kSmemBytes;
+    case 32: return GemmShape<FP8, 32, BSRC>::kSmemBytes;
+    case 64: return GemmShape<FP8, 64, BSRC>::kSmemBytes;
+    case 128: return GemmShape<FP8, 128, BSRC>::kSmemBytes;
+    case 256: return FP8 ? 0 : GemmShape<0, 256, BSRC>::kSmemBytes;
     default: return 0;
   }
+}
+
+size_t gemm_smem_bytes(int fp8, int bn, int bsrc) {
+  if (bsrc == kGather) return fp8 ? smem_bytes_bn<1, kGather>(bn) : smem_bytes_bn<0, kGather>(bn);
+  return fp8 ? smem_bytes_bn<1, kDirect>(bn) : smem_bytes_bn<0, kDirect>(bn);
+}
+
+int gemm_warps(int bn, int bsrc) {
+  return bsrc == kGather ? (bn >= 128 ? GemmShape<0, 128, kGather>::kWarps
+                                      : GemmShape<0, 16, kGather>::kWarps)
+                         : GemmShape<0, 16, kDirect>::kWarps;
+}
+
+size_t gemm_index_smem_bytes(int nwarps, int E, int tk, int rows_cap, int tiles_cap) {
+  return SmemIndex::bytes(nwarps, E, tk, rows_cap, tiles_cap);
 }
 
 }  // namespace moe

@@ -24,16 +24,23 @@ __device__ __forceinline__ uint32_t quant_group4(const float (&v)[4], float* sca
 }
 
 // ---------------------------------------------------------------- x quant
-// x bf16 [T][H] -> xq e4m3 [T][H], xs [T][H/128]; one warp per group.
+// x bf16 [T][H] -> xq e4m3 [T][H], xs [T][H/128]; one warp per group.  The
+// scales are also written to the index rows that hold the token's
+// assignments (xs_rows[inv_pos[t*k+j]]), so the Gate-Up epilogue reads them
+// by row without going through the index.
 __global__ void __launch_bounds__(128) moe_quant_x_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          int T, int H, uint8_t* __restrict__ xq,
-                                                          float* __restrict__ xs) {
+                                                          int T, int H, int k,
+                                                          const int32_t* __restrict__ inv_pos,
+                                                          uint8_t* __restrict__ xq,
+                                                          float* __restrict__ xs,
+                                                          float* __restrict__ xs_rows) {
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
   const int g = blockIdx.y * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (g >= H / 128) return;
+  const int G = H / 128;
+  if (g >= G) return;
   const size_t base = static_cast<size_t>(t) * H + g * 128 + lane * 4;
   const uint2 raw = *reinterpret_cast<const uint2*>(x + base);
   const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
@@ -42,14 +49,19 @@ __global__ void __launch_bounds__(128) moe_quant_x_kernel(const __nv_bfloat16* _
   float s;
   const uint32_t q = quant_group4(v, &s);
   *reinterpret_cast<uint32_t*>(xq + base) = q;
-  if (lane == 0) xs[static_cast<size_t>(t) * (H / 128) + g] = s;
+  if (lane == 0) xs[static_cast<size_t>(t) * G + g] = s;
+  if (inv_pos != nullptr)
+    for (int j = lane; j < k; j += 32) {
+      const int pos = __ldg(inv_pos + static_cast<size_t>(t) * k + j);
+      if (pos >= 0) xs_rows[static_cast<size_t>(pos) * G + g] = s;
+    }
 }
 
-cudaError_t launch_quant_x(const void* x, int T, int H, uint8_t* xq, float* xs, cudaStream_t st,
-                           bool pdl) {
+cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* inv_pos,
+                           uint8_t* xq, float* xs, float* xs_rows, cudaStream_t st, bool pdl) {
   const dim3 grid(T, (H / 128 + 3) / 4);
   return launch_kernel(moe_quant_x_kernel, grid, dim3(128), 0, st, pdl,
-                       static_cast<const __nv_bfloat16*>(x), T, H, xq, xs);
+                       static_cast<const __nv_bfloat16*>(x), T, H, k, inv_pos, xq, xs, xs_rows);
 }
 
 // ---------------------------------------------------------------- act
@@ -81,6 +93,7 @@ __global__ void __launch_bounds__(kActThreads)
     for (int i = threadIdx.x * 4; i < I; i += kActThreads * 4) {
       float4 g = __ldg(reinterpret_cast<const float4*>(row + i));
       float4 u = __ldg(reinterpret_cast<const float4*>(row + I + i));
+#pragma unroll 4
       for (int s = 1; s < splits; ++s) {
         const float4 gs = __ldg(reinterpret_cast<const float4*>(row + s * slice + i));
         const float4 us = __ldg(reinterpret_cast<const float4*>(row + s * slice + I + i));
@@ -158,6 +171,7 @@ __global__ void __launch_bounds__(128)
     for (int b = 0; b < kCombineBatch; ++b)
       y[b] = pos[b] >= 0 ? __ldg(reinterpret_cast<const float4*>(Y + static_cast<size_t>(pos[b]) * H + h))
                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
     for (int s = 1; s < splits; ++s) {
 #pragma unroll
       for (int b = 0; b < kCombineBatch; ++b) {
@@ -240,17 +254,19 @@ __global__ void __launch_bounds__(128)
   constexpr int kPer = kRouterMaxE / 32;
   float s[kPer];
   const size_t slice = static_cast<size_t>(rows_cap) * 2 * E;
+  const int per = (E + 31) / 32;   // slots this warp really uses
   float mx = -INFINITY;
+  const float* row = P + static_cast<size_t>(t) * 2 * E;
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = lane + 32 * i;
     float v = -INFINITY;
-    if (e < E) {
-      float hi = 0.f, lo = 0.f;
-      const float* row = P + static_cast<size_t>(t) * 2 * E;
-      for (int sp = 0; sp < splits; ++sp) {
-        hi += row[sp * slice + e];
-        lo += row[sp * slice + E + e];
+    if (i < per && e < E) {
+      float hi = __ldg(row + e), lo = __ldg(row + E + e);
+#pragma unroll 4
+      for (int sp = 1; sp < splits; ++sp) {
+        hi += __ldg(row + sp * slice + e);
+        lo += __ldg(row + sp * slice + E + e);
       }
       v = hi + lo * (1.0f / 256.0f);
       scores[static_cast<size_t>(t) * E + e] = v;

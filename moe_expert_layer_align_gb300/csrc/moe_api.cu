@@ -21,6 +21,8 @@ namespace {
 // plan, and with it the workspace size, is a function of the shape alone.
 constexpr int kPlanCtas = 152;
 constexpr int kMaxSplits = 32;
+// Largest T*k for which GEMM CTAs rebuild the routing index themselves.
+constexpr int kSmemIndexMaxAssignments = 4096;
 
 struct Plan {
   int T, H, I, E, k, bm, fp8, out_bf16;
@@ -28,13 +30,14 @@ struct Plan {
   int s1, kts1, kt1, mt1;  // Gate-Up: splits, k-tiles per split, k-tiles, weight tiles
   int s2, kts2, kt2, mt2;  // Down
   int fused_act;           // SiLU-and-mul in the Gate-Up epilogue
-  size_t off[13];
+  int smem_index;          // GEMM CTAs rebuild the index in shared memory
+  size_t off[14];
   size_t total;
 };
 
 enum {
   kOffCounts, kOffOffsets, kOffSorted, kOffTileExpert, kOffTiles, kOffInvPos, kOffNumTiles,
-  kOffXq, kOffXs, kOffG, kOffA, kOffAs, kOffY
+  kOffXq, kOffXs, kOffXsRows, kOffG, kOffA, kOffAs, kOffY, kNumOff
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -74,10 +77,11 @@ int est_tiles(int T, int k, int E, int bm, int tiles_cap) {
 
 // Split-K count minimising (waves of units) x (k-tiles per unit) plus the
 // cost of writing and re-reading fp32 partial rows, in k-tile units.
-void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int* kts_out) {
+void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int* kts_out,
+                  int max_splits = kMaxSplits) {
   double best = 1e300;
   int bs = 1, bk = kt_total;
-  for (int s = 1; s <= std::min(kMaxSplits, kt_total); ++s) {
+  for (int s = 1; s <= std::min(max_splits, kt_total); ++s) {
     const int kts = (kt_total + s - 1) / s;
     const int se = (kt_total + kts - 1) / kts;
     if (se != s) continue;            // same as a smaller count
@@ -139,10 +143,24 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
     p->s2 = (p->kt2 + p->kts2 - 1) / p->kts2;
   }
   p->fused_act = !p->fp8 && p->s1 == 1 && !(o && o->separate_act);
+  // On request (small batches): every GEMM CTA rebuilds the index from the
+  // top-k ids in shared memory when it fits next to the pipeline (no index
+  // kernel).  Measured no faster than the index kernel, so not the default.
+  {
+    const int tk = s->T * s->k;
+    bool fits = tk <= kSmemIndexMaxAssignments && o && o->smem_index;
+    for (int bsrc : {static_cast<int>(kGather), static_cast<int>(kDirect)}) {
+      const size_t need = gemm_smem_bytes(p->fp8, p->bm, bsrc) +
+                          gemm_index_smem_bytes(gemm_warps(p->bm, bsrc), s->E, tk, p->rows_cap,
+                                                p->tiles_cap);
+      if (need > kMaxGemmSmem) fits = false;
+    }
+    p->smem_index = fits;
+  }
   // workspace layout
   const size_t tk = static_cast<size_t>(s->T) * s->k;
   const size_t rc = p->rows_cap;
-  const size_t sizes[13] = {
+  const size_t sizes[kNumOff] = {
       4u * s->E,
       4u * (s->E + 1),
       4 * rc,
@@ -152,13 +170,14 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
       4,
       p->fp8 ? static_cast<size_t>(s->T) * s->H : 0,
       p->fp8 ? 4 * static_cast<size_t>(s->T) * (s->H / 128) : 0,
+      p->fp8 ? 4 * rc * (s->H / 128) : 0,
       p->fused_act ? 0 : 4 * static_cast<size_t>(p->s1) * rc * 2 * s->I,
       rc * s->I * (p->fp8 ? 1 : 2),
       p->fp8 ? 4 * rc * (s->I / 128) : 0,
       4 * static_cast<size_t>(p->s2) * rc * s->H,
   };
   size_t cur = 0;
-  for (int i = 0; i < 13; ++i) {
+  for (int i = 0; i < kNumOff; ++i) {
     p->off[i] = cur;
     cur = align_up(cur + sizes[i], 256);
   }
@@ -176,6 +195,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->grid_gateup = kPlanCtas;
   L->grid_down = kPlanCtas;
   L->fused_act = p.fused_act;
+  L->smem_index = p.smem_index;
   L->off_counts = p.off[kOffCounts];
   L->off_offsets = p.off[kOffOffsets];
   L->off_sorted_ids = p.off[kOffSorted];
@@ -185,6 +205,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->off_num_tiles = p.off[kOffNumTiles];
   L->off_xq = p.off[kOffXq];
   L->off_xs = p.off[kOffXs];
+  L->off_xs_rows = p.off[kOffXsRows];
   L->off_g = p.off[kOffG];
   L->off_a = p.off[kOffA];
   L->off_as = p.off[kOffAs];
@@ -304,7 +325,8 @@ bool router_plan(int T, int H, int E, RouterPlan* r) {
   r->rows_cap = (T + r->bn - 1) / r->bn * r->bn;
   r->kt = H / 64;
   r->mt = 2 * E / 128;
-  choose_split(r->mt, r->kt, r->rows_cap / r->bn, r->bn, &r->splits, &r->kts);
+  // few splits: every score sums its partials in the top-k kernel
+  choose_split(r->mt, r->kt, r->rows_cap / r->bn, r->bn, &r->splits, &r->kts, 4);
   r->bytes = 4ull * r->splits * r->rows_cap * 2 * E;
   return true;
 }
@@ -378,6 +400,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
                reinterpret_cast<int32_t*>(at(kOffNumTiles))};
   uint8_t* xq = at(kOffXq);
   float* xs = reinterpret_cast<float*>(at(kOffXs));
+  float* xs_rows = reinterpret_cast<float*>(at(kOffXsRows));
   float* G = reinterpret_cast<float*>(at(kOffG));
   void* A = at(kOffA);
   float* As = reinterpret_cast<float*>(at(kOffAs));
@@ -396,13 +419,27 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   const int grid_cap = opts && opts->grid_ctas > 0 ? opts->grid_ctas : sms;
   cudaError_t e;
 
+  // The first launch of the call waits for all earlier work on the stream
+  // (no PDL attribute); later launches overlap their predecessor's tail.
+  bool first = true;
+  auto chain = [&]() {
+    const bool r = first ? false : pdl;
+    first = false;
+    return r;
+  };
+
   record(opts, 0, s);
-  e = launch_align(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s, false);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (!p.smem_index) {
+    e = launch_align(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s, chain());
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
 
   record(opts, 1, s);
   if (p.fp8) {
-    e = launch_quant_x(x, p.T, p.H, xq, xs, s, pdl);
+    // with the shared-memory index the scales stay per token (the Gate-Up
+    // epilogue looks tokens up in its own index)
+    e = launch_quant_x(x, p.T, p.H, p.k, p.smem_index ? nullptr : ip.inv_pos, xq, xs,
+                       p.smem_index ? nullptr : xs_rows, s, chain());
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
 
@@ -423,13 +460,22 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g1.topk = p.k;
   g1.sentinel = tk;
   g1.w_scale = p.fp8 ? scales->w13_scale : nullptr;
-  g1.b_scale = p.fp8 ? xs : nullptr;
+  g1.b_scale = p.fp8 ? (p.smem_index ? xs : xs_rows) : nullptr;
+  g1.scale_by_token = p.smem_index;
+  g1.smem_index = p.smem_index;
+  g1.topk_ids = topk_ids;
+  g1.T = p.T;
+  g1.E = p.E;
+  g1.tiles_cap = p.tiles_cap;
+  g1.write_index = p.smem_index;
+  g1.index_out = {ip.counts, ip.offsets, ip.sorted_ids, ip.tile_expert, ip.tiles, ip.inv_pos,
+                  ip.num_tiles};
   g1.out = G;
   g1.act_out = p.fused_act ? A : nullptr;
   g1.rows_cap = p.rows_cap;
   g1.dev_status = dev_status;
   const int units1 = p.mt1 * p.s1 * p.tiles_cap;
-  e = launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, pdl, tmW13, tmX, g1);
+  e = launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13, tmX, g1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   record(opts, 3, s);
@@ -454,6 +500,12 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g2.sentinel = tk;
   g2.w_scale = p.fp8 ? scales->w2_scale : nullptr;
   g2.b_scale = p.fp8 ? As : nullptr;
+  g2.smem_index = p.smem_index;
+  g2.topk_ids = topk_ids;
+  g2.T = p.T;
+  g2.E = p.E;
+  g2.tiles_cap = p.tiles_cap;
+  g2.early_weights = 1;   // the index is complete before this grid launches
   g2.out = Y;
   g2.rows_cap = p.rows_cap;
   g2.dev_status = dev_status;

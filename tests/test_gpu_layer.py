@@ -31,10 +31,14 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("smem_index", [False, True])
 @pytest.mark.parametrize("cfg,T,kw", CASES)
-def test_layer_matches_oracle(cfg, T, kw):
+def test_layer_matches_oracle(cfg, T, kw, smem_index):
+    import moe_expert_layer_align_gb300 as moe
     wl = small(cfg, T, **kw)
-    got = run_layer(wl).float().cpu().numpy()
+    # the index kernel (default) or every GEMM CTA rebuilding the index
+    opts = moe.make_opts(smem_index=True) if smem_index else None
+    got = run_layer(wl, opts=opts).float().cpu().numpy()
     ref = oracle_layer(wl)
     assert_layer_close(got, ref, wl.mode, f"cfg{cfg} T={T}")
 
@@ -58,24 +62,26 @@ def test_forced_splits_and_no_pdl(s1, s2, sep, mode_cfg):
     kw = dict(H=1024, I=512, E=8) if mode_cfg == 4 else dict(H=1024, I=512, E=8)
     wl = small(mode_cfg, 24, **kw)
     opts = moe.make_opts(disable_pdl=(s1 == 3), split_gateup=s1, split_down=s2,
-                         separate_act=sep)
+                         separate_act=sep, smem_index=(s2 == 3))
     got = run_layer(wl, opts=opts).float().cpu().numpy()
     assert_layer_close(got, oracle_layer(wl), wl.mode, f"splits {s1},{s2}")
 
 
-@pytest.mark.parametrize("fused", [True, False])
-def test_intermediates_bf16(fused):
+@pytest.mark.parametrize("fused,smem_index", [(True, False), (False, False), (True, True)])
+def test_intermediates_bf16(fused, smem_index):
     import moe_expert_layer_align_gb300 as moe
     wl = small(2, 33, H=256, I=128, E=4)
     # unsplit Gate-Up fuses SiLU-and-mul into its epilogue; a split one
-    # leaves fp32 partials for the separate stage
-    opts = moe.make_opts(split_gateup=1 if fused else 2)
+    # leaves fp32 partials for the separate stage.  The index comes from the
+    # Gate-Up's CTA 0 (shared-memory mode) or from the index kernel.
+    opts = moe.make_opts(split_gateup=1 if fused else 2, smem_index=smem_index)
     shape = moe.layer_shape(wl.x, wl.w13, wl.topk_ids, 0, torch.bfloat16)
     ws = torch.zeros(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
     run_layer(wl, workspace=ws, opts=opts)
     torch.cuda.synchronize()
     v = moe.workspace_views(ws, shape, opts)
     assert v["layout"].fused_act == int(fused)
+    assert v["layout"].smem_index == int(smem_index)
     ref = oracle.align(wl.topk_ids.cpu().numpy(), wl.E, v["layout"].block_m)
     for n in ("counts", "offsets", "sorted_ids", "tile_expert", "tiles", "inv_pos", "num_tiles"):
         np.testing.assert_array_equal(v[n].cpu().numpy().reshape(-1), ref[n].reshape(-1), n)
@@ -98,17 +104,27 @@ def test_intermediates_bf16(fused):
         np.testing.assert_allclose(A[p], act, rtol=1e-2, atol=1e-2 * np.abs(act).max())
 
 
-def test_intermediates_fp8_codes():
+@pytest.mark.parametrize("smem_index", [False, True])
+def test_intermediates_fp8_codes(smem_index):
     import moe_expert_layer_align_gb300 as moe
     wl = small(4, 20, H=512, I=256, E=6, k=3)
+    opts = moe.make_opts(smem_index=smem_index)
     shape = moe.layer_shape(wl.x, wl.w13q, wl.topk_ids, 0, torch.bfloat16)
-    ws = torch.zeros(moe.moe_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
-    got = run_layer(wl, workspace=ws).float().cpu().numpy()
+    ws = torch.zeros(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
+    got = run_layer(wl, workspace=ws, opts=opts).float().cpu().numpy()
     torch.cuda.synchronize()
-    v = moe.workspace_views(ws, shape)
+    v = moe.workspace_views(ws, shape, opts)
+    ref_idx = oracle.align(wl.topk_ids.cpu().numpy(), wl.E, v["layout"].block_m)
+    for n in ("counts", "offsets", "sorted_ids", "tile_expert", "tiles", "inv_pos", "num_tiles"):
+        np.testing.assert_array_equal(v[n].cpu().numpy().reshape(-1), ref_idx[n].reshape(-1), n)
     xq, xs = oracle.quant_x(bits16(wl.x))
     np.testing.assert_array_equal(v["xq"].cpu().numpy(), xq)          # bit-exact
     np.testing.assert_array_equal(v["xs"].cpu().numpy(), xs)
+    if not smem_index:
+        # the same scales scattered to the index rows that hold each token
+        sid = v["sorted_ids"].cpu().numpy()
+        rows = np.flatnonzero(sid < wl.T * wl.k)
+        np.testing.assert_array_equal(v["xs_rows"].cpu().numpy()[rows], xs[sid[rows] // wl.k])
     ref, aq, as_ = oracle_layer(wl, return_act=True)
     assert_layer_close(got, ref, "fp8", "fp8 layer")
     inv = v["inv_pos"].cpu().numpy()
@@ -125,13 +141,16 @@ def test_intermediates_fp8_codes():
     assert n_diff <= max(2, wl.T * wl.k * wl.I // 2000), n_diff
 
 
-def test_invalid_ids_contribute_zero_and_are_flagged():
+@pytest.mark.parametrize("smem_index", [False, True])
+def test_invalid_ids_contribute_zero_and_are_flagged(smem_index):
+    import moe_expert_layer_align_gb300 as moe
     wl = small(3, 30, H=256, I=128, E=16)
     ids = wl.topk_ids.clone()
     ids[2, 1] = -3
     ids[7, 0] = 99
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    got = run_layer(wl, topk_ids=ids, dev_status=st).float().cpu().numpy()
+    st = torch.full((1,), 12345, dtype=torch.int32, device="cuda")   # cleared by the call
+    got = run_layer(wl, topk_ids=ids, dev_status=st,
+                    opts=moe.make_opts(smem_index=smem_index)).float().cpu().numpy()
     torch.cuda.synchronize()
     assert st.item() == (1 << 6)
     ref = oracle_layer(wl, topk_ids=ids.cpu())
