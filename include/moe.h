@@ -124,6 +124,9 @@ typedef struct {
    * shared memory (T*k <= 4096 and room next to the pipeline), instead of
    * the separate index kernel; the Gate-Up writes the index out. */
   int32_t smem_index;
+  /* 1: one 128-row weight tile per GEMM work unit even for large token tiles
+   * (where the plan pairs two to halve the token-tile traffic per MMA). */
+  int32_t single_weight_tile;
 } moe_forward_opts;
 
 /* Where moe_forward keeps its intermediates inside the caller's workspace
@@ -135,7 +138,7 @@ typedef struct {
   int32_t fused_act;   /* 1: SiLU-and-mul runs in the Gate-Up epilogue (no G) */
   int32_t smem_index;  /* 1: GEMM CTAs rebuild the index in shared memory; the
                           Gate-Up writes it out (no separate index kernel) */
-  int32_t reserved;
+  int32_t weight_tiles_per_unit;  /* Gate-Up | Down << 8 (1 or 2 each) */
   size_t off_counts, off_offsets, off_sorted_ids, off_tile_expert, off_tiles,
       off_inv_pos, off_num_tiles;
   size_t off_xq;   /* FP8: e4m3 x            [T][H]                         */

@@ -45,14 +45,14 @@ class moe_scales(ctypes.Structure):
 class moe_forward_opts(ctypes.Structure):
     _fields_ = [("disable_pdl", _i32), ("split_gateup", _i32), ("split_down", _i32),
                 ("grid_ctas", _i32), ("stage_events", _vp * 8), ("separate_act", _i32),
-                ("smem_index", _i32)]
+                ("smem_index", _i32), ("single_weight_tile", _i32)]
 
 
 class moe_workspace_layout(ctypes.Structure):
     _fields_ = [("block_m", _i32), ("tiles_cap", _i32), ("rows_cap", _i32),
                 ("split_gateup", _i32), ("split_down", _i32), ("grid_gateup", _i32),
                 ("grid_down", _i32), ("fused_act", _i32), ("smem_index", _i32),
-                ("reserved", _i32)] + [
+                ("weight_tiles_per_unit", _i32)] + [
         (n, _sz) for n in ("off_counts", "off_offsets", "off_sorted_ids", "off_tile_expert",
                            "off_tiles", "off_inv_pos", "off_num_tiles", "off_xq", "off_xs",
                            "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "total_bytes")]
@@ -140,11 +140,13 @@ def moe_index_tiles_cap(T, k, E, block_m) -> int:
 
 
 def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
-              stage_events=None, separate_act=False, smem_index=False) -> moe_forward_opts:
+              stage_events=None, separate_act=False, smem_index=False,
+              single_weight_tile=False) -> moe_forward_opts:
     o = moe_forward_opts()
     o.disable_pdl = int(disable_pdl)
     o.separate_act = int(separate_act)
     o.smem_index = int(smem_index)
+    o.single_weight_tile = int(single_weight_tile)
     o.split_gateup = split_gateup
     o.split_down = split_down
     o.grid_ctas = grid_ctas

@@ -59,9 +59,11 @@ int gemm_warps(int bn, int bsrc);
 constexpr size_t kMaxGemmSmem = 227 * 1024;
 
 // Launch the persistent GEMM (defined per mode in k_gemm_{bf16,fp8}.cu).
+// `me` weight tiles per work unit (1, or 2 for bf16 with bn 128 / 256);
+// p.m_tiles then counts groups of `me` tiles.
 cudaError_t launch_gemm_bf16(int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
                              const CUtensorMap& tmA, const CUtensorMap& tmB,
-                             const GemmParams& p);
+                             const GemmParams& p, int me = 1);
 cudaError_t launch_gemm_fp8(int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
                             const CUtensorMap& tmA, const CUtensorMap& tmB,
                             const GemmParams& p);

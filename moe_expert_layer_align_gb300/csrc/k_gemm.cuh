@@ -65,13 +65,18 @@ constexpr int kTileM = 128;                 // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // K bytes per pipeline stage
 constexpr int kABytes = kTileM * kKBytes;   // 16 KB weight tile per stage
 
-__host__ __device__ constexpr int stages_for(int fp8, int bn) {
-  return bn <= 32 ? 8 : bn == 64 ? (fp8 ? 7 : 8) : bn == 128 ? (fp8 ? 5 : 6) : 4;
+__host__ __device__ constexpr int stages_for(int fp8, int bn, int me) {
+  return me == 1 ? (bn <= 32 ? 8 : bn == 64 ? (fp8 ? 7 : 8) : bn == 128 ? (fp8 ? 5 : 6) : 4)
+                 : (196608 / (me * kABytes + bn * kKBytes) < 8 ? 196608 / (me * kABytes + bn * kKBytes)
+                                                               : 8);
 }
 
-template <int FP8, int BN, int BSRC = kDirect>
+// ME weight tiles per work unit: ME = 2 halves the token-tile traffic per
+// MMA for large (prefill) tiles, where L2 bandwidth, not HBM, is the limit.
+template <int FP8, int BN, int BSRC = kDirect, int ME = 1>
 struct GemmShape {
-  static constexpr int kStages = stages_for(FP8, BN);
+  static constexpr int kStages = stages_for(FP8, BN, ME);
+  static constexpr int kAStage = ME * kABytes;
   // token-row gather warps (gathered operand only) and block size
   static constexpr int kGatherWarps = BSRC == kGather ? (BN >= 128 ? 2 : 1) : 0;
   static constexpr int kGatherThreads = 32 * kGatherWarps;
@@ -79,20 +84,24 @@ struct GemmShape {
   static constexpr int kWarps = kThreads / 32;
   static constexpr int kRowsPerGatherThread = kGatherWarps ? BN / (4 * kGatherWarps) : 1;
   static constexpr int kBBytes = BN * kKBytes;
-  // TMEM accumulator buffers: two per-unit buffers for bf16; for FP8 every
-  // 128-wide K block is its own buffer, so keep up to 8 in flight (the MMA
-  // would otherwise wait on the epilogue's promotion every other K block).
-  static constexpr int kAccBufs = FP8 ? (512 / BN < 8 ? 512 / BN : 8) : 2;
-  static constexpr int kTmemCols = (kAccBufs * BN < 32) ? 32 : kAccBufs * BN;
+  // TMEM accumulator buffers (each ME x BN columns): two per-unit buffers
+  // for bf16 where they fit; for FP8 every 128-wide K block is its own
+  // buffer, so keep up to 8 in flight (the MMA would otherwise wait on the
+  // epilogue's promotion every other K block).
+  static constexpr int kAccBufs =
+      FP8 ? (512 / BN < 8 ? 512 / BN : 8) : (512 / (ME * BN) < 2 ? 1 : 2);
+  static constexpr int kTmemCols = (kAccBufs * ME * BN < 32) ? 32 : kAccBufs * ME * BN;
   static constexpr int kElemsPerStage = FP8 ? 128 : 64;
   static constexpr uint32_t kIdesc = mma_idesc(FP8 ? 0u : 1u, kTileM, BN);
-  static constexpr int kOffB = kStages * kABytes;
+  static constexpr int kOffB = kStages * kAStage;
   static constexpr int kOffBar = kOffB + kStages * kBBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;  // + drain
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffIdx = (kOffMisc + 16 + 15) & ~15;       // shared-memory index
   static constexpr size_t kSmemBytes = 1024 + kOffIdx;             // without the index
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0");
+  static_assert(ME == 1 || !FP8, "FP8 promotion keeps one weight tile per unit");
+  static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
 };
 
 // Shared-memory index: build scratch, staged ids, sorted rows, task map.
@@ -171,11 +180,11 @@ __device__ __forceinline__ void report_timeout(const GemmParams& p, volatile int
   if (p.dev_status) atomicOr(p.dev_status, kStatusTimeout);
 }
 
-template <int FP8, int BN, int BSRC>
-__global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
+template <int FP8, int BN, int BSRC, int ME>
+__global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-  using S = GemmShape<FP8, BN, BSRC>;
+  using S = GemmShape<FP8, BN, BSRC, ME>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -263,7 +272,8 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
     uint32_t phase = 0;
     long issued = 0;
     bool ok = true;
-    constexpr uint32_t bytes = kABytes + (BSRC == kGather ? 0u : static_cast<uint32_t>(S::kBBytes));
+    constexpr uint32_t bytes =
+        S::kAStage + (BSRC == kGather ? 0u : static_cast<uint32_t>(S::kBBytes));
     bool b_now = !(early && BSRC == kDirect);
     int deferred = 0;
     auto flush_deferred = [&]() {
@@ -291,17 +301,21 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
         }
         if (lane == 0) {
           const uint32_t full = bar_full + 8 * stage;
-          const uint32_t a_dst = sA + stage * kABytes;
+          const uint32_t a_dst = sA + stage * S::kAStage;
           const int kc = kt * S::kElemsPerStage;
           mbar_arrive_expect_tx(full, bytes);
-          if (BSRC == kGather) {
-            // one box of the 5-D view (K, 16 rows, gate|up, 16-row group,
-            // expert): smem rows 32q..32q+15 gate rows, 32q+16.. up rows
-            tma_load_5d(a_dst, &tmA, full, kc, 0, 0, w.mt * 4, w.e);
-          } else {
-            tma_load_3d(a_dst, &tmA, full, kc, w.mt * kTileM, w.e);
-            if (b_now) tma_load_2d(sB + stage * S::kBBytes, &tmB, full, kc, w.row0);
+#pragma unroll
+          for (int me = 0; me < ME; ++me) {
+            const int mt = w.mt * ME + me;
+            if (BSRC == kGather)
+              // one box of the 5-D view (K, 16 rows, gate|up, 16-row group,
+              // expert): smem rows 32q..32q+15 gate rows, 32q+16.. up rows
+              tma_load_5d(a_dst + me * kABytes, &tmA, full, kc, 0, 0, mt * 4, w.e);
+            else
+              tma_load_3d(a_dst + me * kABytes, &tmA, full, kc, mt * kTileM, w.e);
           }
+          if (BSRC != kGather && b_now)
+            tma_load_2d(sB + stage * S::kBBytes, &tmB, full, kc, w.row0);
         }
         __syncwarp();
         ++issued;
@@ -357,16 +371,19 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           // token rows written by cp.async (generic proxy) are read by the MMA
           // through the async proxy
           if (BSRC == kGather) fence_proxy_async_smem();
-          const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
-          const uint64_t adesc = smem_desc_sw128(sA + stage * kABytes);
           const uint64_t bdesc = smem_desc_sw128(sB + stage * S::kBBytes);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
-            const uint32_t acc = FP8 ? (k > 0) : (kt > w.kt0 || k > 0);
-            if (FP8)
-              mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, S::kIdesc, acc);
-            else
-              mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, S::kIdesc, acc);
+          for (int me = 0; me < ME; ++me) {
+            const uint32_t d = tmem_base + static_cast<uint32_t>((ab * ME + me) * BN);
+            const uint64_t adesc = smem_desc_sw128(sA + stage * S::kAStage + me * kABytes);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
+              const uint32_t acc = FP8 ? (k > 0) : (kt > w.kt0 || k > 0);
+              if (FP8)
+                mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, S::kIdesc, acc);
+              else
+                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, S::kIdesc, acc);
+            }
           }
           tc_commit(bar_empty + 8 * stage);
           if (++stage == S::kStages) {
@@ -429,16 +446,6 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
     uint32_t aph = 0;
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); it.valid(); it.advance()) {
       const WorkUnit w = it.take(p);
-      int col;
-      bool col_ok = true;
-      const int feat = w.mt * 64 + qd * 16 + (lane & 15);  // Gate-Up: this lane's channel
-      if (BSRC == kGather) {
-        col = lane < 16 ? feat : p.I + feat;
-      } else {
-        col = w.mt * kTileM + r;
-        col_ok = col < p.M;
-      }
-      float* outp = p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0) * p.M + col;
       if (!FP8) {
         if (!mbar_wait(bar_accf + 8 * ab, aph)) {
           report_timeout(p, abort_flag);
@@ -446,11 +453,24 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
         }
         tc_fence_after();
         const bool fuse = BSRC == kGather && p.act_out != nullptr;
+#pragma unroll 1
+        for (int me = 0; me < ME; ++me) {
+        const int mt = w.mt * ME + me;
+        int col;
+        bool col_ok = true;
+        const int feat = mt * 64 + qd * 16 + (lane & 15);  // Gate-Up: this lane's channel
+        if (BSRC == kGather) {
+          col = lane < 16 ? feat : p.I + feat;
+        } else {
+          col = mt * kTileM + r;
+          col_ok = col < p.M;
+        }
+        float* outp = p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0) * p.M + col;
 #pragma unroll
         for (int c = 0; c < BN / 16; ++c) {
           if (c * 16 < w.rows) {
             uint32_t v[16];
-            tmem_ld16(t_lane + static_cast<uint32_t>(ab * BN + c * 16), v);
+            tmem_ld16(t_lane + static_cast<uint32_t>((ab * ME + me) * BN + c * 16), v);
             tmem_ld_wait();
             if (fuse) {
               // lanes 0..15 hold gate, 16..31 the matching up: swap halves, then
@@ -479,6 +499,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
             }
           }
         }
+        }  // me
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
@@ -487,6 +508,16 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
           aph ^= 1u;
         }
       } else {
+        const int feat = w.mt * 64 + qd * 16 + (lane & 15);  // Gate-Up: this lane's channel
+        int col;
+        bool col_ok = true;
+        if (BSRC == kGather) {
+          col = lane < 16 ? feat : p.I + feat;
+        } else {
+          col = w.mt * kTileM + r;
+          col_ok = col < p.M;
+        }
+        float* outp = p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0) * p.M + col;
         // Per-column scale rows: lane l serves columns l, l+32, ...
         constexpr int kCPerLane = BN / 32 > 0 ? BN / 32 : 1;
         const int KB = p.kt_total;
@@ -621,11 +652,11 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC>::kThreads, 1)
   }
 }
 
-template <int FP8, int BN, int BSRC>
+template <int FP8, int BN, int BSRC, int ME = 1>
 cudaError_t launch_gemm_inst(int grid, cudaStream_t st, bool pdl, const CUtensorMap& a,
                              const CUtensorMap& b, const GemmParams& p) {
-  using S = GemmShape<FP8, BN, BSRC>;
-  auto kern = moe_gemm_kernel<FP8, BN, BSRC>;
+  using S = GemmShape<FP8, BN, BSRC, ME>;
+  auto kern = moe_gemm_kernel<FP8, BN, BSRC, ME>;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -645,7 +676,14 @@ cudaError_t launch_gemm_inst(int grid, cudaStream_t st, bool pdl, const CUtensor
 
 template <int FP8, int BSRC>
 cudaError_t launch_gemm_bn(int bn, int grid, cudaStream_t st, bool pdl, const CUtensorMap& a,
-                           const CUtensorMap& b, const GemmParams& p) {
+                           const CUtensorMap& b, const GemmParams& p, int me = 1) {
+  if (me == 2) {
+    if constexpr (!FP8) {
+      if (bn == 128) return launch_gemm_inst<FP8, 128, BSRC, 2>(grid, st, pdl, a, b, p);
+      if (bn == 256) return launch_gemm_inst<FP8, 256, BSRC, 2>(grid, st, pdl, a, b, p);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (bn) {
     case 16: return launch_gemm_inst<FP8, 16, BSRC>(grid, st, pdl, a, b, p);
     case 32: return launch_gemm_inst<FP8, 32, BSRC>(grid, st, pdl, a, b, p);

@@ -6,12 +6,13 @@ namespace moe {
 
 cudaError_t launch_gemm_bf16_gather_dense(int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
                                           const CUtensorMap& a, const CUtensorMap& b,
-                                          const GemmParams& p);
+                                          const GemmParams& p, int me);
 
 cudaError_t launch_gemm_bf16(int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
-                             const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p) {
-  if (bsrc == kDirect) return launch_gemm_bn<0, kDirect>(bn, grid, st, pdl, a, b, p);
-  return launch_gemm_bf16_gather_dense(bn, bsrc, grid, st, pdl, a, b, p);
+                             const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                             int me) {
+  if (bsrc == kDirect) return launch_gemm_bn<0, kDirect>(bn, grid, st, pdl, a, b, p, me);
+  return launch_gemm_bf16_gather_dense(bn, bsrc, grid, st, pdl, a, b, p, me);
 }
 
 template <int FP8, int BSRC>

@@ -29,6 +29,7 @@ struct Plan {
   int tiles_cap, rows_cap;
   int s1, kts1, kt1, mt1;  // Gate-Up: splits, k-tiles per split, k-tiles, weight tiles
   int s2, kts2, kt2, mt2;  // Down
+  int me1, me2;            // weight tiles per work unit (2: large token tiles, bf16)
   int fused_act;           // SiLU-and-mul in the Gate-Up epilogue
   int smem_index;          // GEMM CTAs rebuild the index in shared memory
   size_t off[14];
@@ -131,9 +132,13 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
   p->mt1 = s->I / 64;
   p->kt2 = s->I / kstage;
   p->mt2 = s->H / 128;
+  // Large token tiles (prefill) are L2-bandwidth bound with one 128-row
+  // weight tile per unit: pair two weight tiles per unit there.
+  p->me1 = (!p->fp8 && p->bm >= 128 && p->mt1 % 2 == 0 && !(o && o->single_weight_tile)) ? 2 : 1;
+  p->me2 = (!p->fp8 && p->bm >= 128 && p->mt2 % 2 == 0 && !(o && o->single_weight_tile)) ? 2 : 1;
   const int est = est_tiles(s->T, s->k, s->E, p->bm, p->tiles_cap);
-  choose_split(p->mt1, p->kt1, est, p->bm, &p->s1, &p->kts1);
-  choose_split(p->mt2, p->kt2, est, p->bm, &p->s2, &p->kts2);
+  choose_split(p->mt1 / p->me1, p->kt1, est, p->bm, &p->s1, &p->kts1);
+  choose_split(p->mt2 / p->me2, p->kt2, est, p->bm, &p->s2, &p->kts2);
   if (o && o->split_gateup > 0) {
     p->kts1 = (p->kt1 + o->split_gateup - 1) / o->split_gateup;
     p->s1 = (p->kt1 + p->kts1 - 1) / p->kts1;
@@ -196,6 +201,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->grid_down = kPlanCtas;
   L->fused_act = p.fused_act;
   L->smem_index = p.smem_index;
+  L->weight_tiles_per_unit = p.me1 | (p.me2 << 8);
   L->off_counts = p.off[kOffCounts];
   L->off_offsets = p.off[kOffOffsets];
   L->off_sorted_ids = p.off[kOffSorted];
@@ -308,9 +314,10 @@ void record(const moe_forward_opts* o, int i, cudaStream_t st) {
 }
 
 cudaError_t launch_gemm(int fp8, int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
-                        const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p) {
+                        const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                        int me = 1) {
   return fp8 ? launch_gemm_fp8(bn, bsrc, grid, st, pdl, a, b, p)
-             : launch_gemm_bf16(bn, bsrc, grid, st, pdl, a, b, p);
+             : launch_gemm_bf16(bn, bsrc, grid, st, pdl, a, b, p, me);
 }
 
 // Router plan: row tile, split-K count and workspace for the partial sums.
@@ -448,7 +455,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g1.M = 2 * p.I;
   g1.K = p.H;
   g1.I = p.I;
-  g1.m_tiles = p.mt1;
+  g1.m_tiles = p.mt1 / p.me1;
   g1.splits = p.s1;
   g1.kt_per_split = p.kts1;
   g1.kt_total = p.kt1;
@@ -474,8 +481,9 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g1.act_out = p.fused_act ? A : nullptr;
   g1.rows_cap = p.rows_cap;
   g1.dev_status = dev_status;
-  const int units1 = p.mt1 * p.s1 * p.tiles_cap;
-  e = launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13, tmX, g1);
+  const int units1 = g1.m_tiles * p.s1 * p.tiles_cap;
+  e = launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13, tmX, g1,
+                  p.me1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   record(opts, 3, s);
@@ -489,7 +497,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g2.M = p.H;
   g2.K = p.I;
   g2.I = 0;
-  g2.m_tiles = p.mt2;
+  g2.m_tiles = p.mt2 / p.me2;
   g2.splits = p.s2;
   g2.kt_per_split = p.kts2;
   g2.kt_total = p.kt2;
@@ -509,8 +517,9 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g2.out = Y;
   g2.rows_cap = p.rows_cap;
   g2.dev_status = dev_status;
-  const int units2 = p.mt2 * p.s2 * p.tiles_cap;
-  e = launch_gemm(p.fp8, p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2);
+  const int units2 = g2.m_tiles * p.s2 * p.tiles_cap;
+  e = launch_gemm(p.fp8, p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2,
+                  p.me2);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   record(opts, 5, s);

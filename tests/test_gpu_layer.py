@@ -186,3 +186,17 @@ def test_combine_alone():
             if p >= 0:
                 ref[t] += w[t, j].item() * Ys[p]
     np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("single", [False, True])
+def test_two_weight_tiles_per_unit(bm, single):
+    # large token tiles pair two 128-row weight tiles per GEMM unit (bf16)
+    import moe_expert_layer_align_gb300 as moe
+    wl = small(2, 300, H=512, I=256, E=4)
+    opts = moe.make_opts(single_weight_tile=single)
+    shape = moe.layer_shape(wl.x, wl.w13, wl.topk_ids, bm, torch.bfloat16)
+    L = moe.moe_plan(shape, opts)
+    assert L.weight_tiles_per_unit == (0x101 if single else 0x202)
+    got = run_layer(wl, block_m=bm, opts=opts).float().cpu().numpy()
+    assert_layer_close(got, oracle_layer(wl), "bf16", f"bm={bm} single={single}")
