@@ -141,6 +141,7 @@ typedef struct {
   int32_t weight_tiles_per_unit;  /* Gate-Up | Down << 8 (1 or 2 each) */
   size_t off_counts, off_offsets, off_sorted_ids, off_tile_expert, off_tiles,
       off_inv_pos, off_num_tiles;
+  size_t off_index_scratch; /* per-chunk histograms of the split index build */
   size_t off_xq;   /* FP8: e4m3 x            [T][H]                         */
   size_t off_xs;   /* FP8: fp32 x scales     [T][H/128]                     */
   size_t off_xs_rows; /* FP8: the same scales in index-row order [rows_cap][H/128] */

@@ -54,7 +54,7 @@ class moe_workspace_layout(ctypes.Structure):
                 ("grid_down", _i32), ("fused_act", _i32), ("smem_index", _i32),
                 ("weight_tiles_per_unit", _i32)] + [
         (n, _sz) for n in ("off_counts", "off_offsets", "off_sorted_ids", "off_tile_expert",
-                           "off_tiles", "off_inv_pos", "off_num_tiles", "off_xq", "off_xs",
+                           "off_tiles", "off_inv_pos", "off_num_tiles", "off_index_scratch", "off_xq", "off_xs",
                            "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "total_bytes")]
 
 

@@ -8,7 +8,7 @@
 // One thread block builds the whole index.  Warp w of the block owns the
 // contiguous slice [w*seg, (w+1)*seg) of the flat assignments a = t*k + j and
 // walks it in rounds of 32 (one assignment per lane):
-//   1. count: __match_any_sync groups a round's lanes by expert and the
+//   1. count: a ballot per key bit groups a round's lanes by expert and the
 //      group's lowest lane adds the group size to cnt[w][e] (one writer per
 //      address, no atomics);
 //   2. scan: per expert an exclusive prefix of cnt[.][e] over the warps gives
@@ -33,6 +33,27 @@ __device__ __forceinline__ int lanemask_lt() {
   return m;
 }
 
+// Lanes of the warp whose key equals this lane's, from one ballot per key
+// bit (ANDing each bit's agreement mask).  Keys are in [0, 2^bits); a lane
+// with an invalid id passes key = 2^bits, so `bits + 1` bits are compared.
+// (One vote per bit instead of __match_any_sync, whose cost grows with the
+// number of distinct keys in the warp.)
+__device__ __forceinline__ unsigned peer_mask(int key, int bits) {
+  unsigned mask = 0xffffffffu;
+  for (int b = 0; b <= bits; ++b) {
+    const bool set = (key >> b) & 1;
+    const unsigned v = __ballot_sync(0xffffffffu, set);
+    mask &= set ? v : ~v;
+  }
+  return mask;
+}
+
+__device__ __forceinline__ int key_bits(int E) {
+  int b = 0;
+  while ((1 << b) < E) ++b;
+  return b;
+}
+
 // Shared-memory scratch of one index build.
 struct IndexScratch {
   int32_t* cnt;    // [nwarps][E]: per-warp counts, then per-warp bases
@@ -50,40 +71,10 @@ struct IndexScratch {
   }
 };
 
-// Steps 1-2: counts, per-warp bases and padded offsets, all in `sc`.  `src`
-// holds the T*k ids (shared or global memory).  Ends with a block barrier.
-__device__ __forceinline__ void index_count_and_scan(const int32_t* src, int tk, int E, int bm,
-                                                     const IndexScratch& sc) {
-  const int tid = threadIdx.x, nthreads = blockDim.x, nwarps = nthreads >> 5;
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < nwarps * E; i += nthreads) sc.cnt[i] = 0;
-  if (tid == 0) *sc.flag = 0;
-  __syncthreads();
-  const int seg = (tk + nwarps - 1) / nwarps;
-  const int beg = min(tk, warp * seg);
-  const int end = min(tk, beg + seg);
-  for (int base = beg; base < end; base += 32) {
-    const int a = base + lane;
-    const bool in = a < end;
-    const int e = in ? src[a] : -1;
-    const bool valid = in && e >= 0 && e < E;
-    if (in && !valid) *sc.flag = 1;
-    const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1);
-    if (valid && lane == __ffs(grp) - 1) sc.cnt[warp * E + e] += __popc(grp);
-    __syncwarp();
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += nthreads) {
-    int run = 0;
-    for (int w = 0; w < nwarps; ++w) {
-      const int c = sc.cnt[w * E + e];
-      sc.cnt[w * E + e] = run;
-      run += c;
-    }
-    sc.tot[e] = run;
-  }
-  __syncthreads();
-  // exclusive scan of the padded counts: warp 0, each lane a run of experts
+// offs[0..E] = exclusive prefix of tot[] rounded up to multiples of bm (warp
+// 0; each lane a run of experts).  Ends with a block barrier.
+__device__ __forceinline__ void index_scan_offsets(int E, int bm, const IndexScratch& sc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
@@ -105,6 +96,43 @@ __device__ __forceinline__ void index_count_and_scan(const int32_t* src, int tk,
   __syncthreads();
 }
 
+// Steps 1-2: counts, per-warp bases and padded offsets, all in `sc`.  `src`
+// holds the T*k ids (shared or global memory).  Ends with a block barrier.
+__device__ __forceinline__ void index_count_and_scan(const int32_t* src, int tk, int E, int bm,
+                                                     const IndexScratch& sc) {
+  const int tid = threadIdx.x, nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < nwarps * E; i += nthreads) sc.cnt[i] = 0;
+  if (tid == 0) *sc.flag = 0;
+  __syncthreads();
+  const int seg = (tk + nwarps - 1) / nwarps;
+  const int beg = min(tk, warp * seg);
+  const int end = min(tk, beg + seg);
+  const int bits = key_bits(E);
+  for (int base = beg; base < end; base += 32) {
+    const int a = base + lane;
+    const bool in = a < end;
+    const int e = in ? src[a] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    if (in && !valid) *sc.flag = 1;
+    const unsigned grp = peer_mask(valid ? e : (1 << bits), bits);
+    if (valid && lane == __ffs(grp) - 1) sc.cnt[warp * E + e] += __popc(grp);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += nthreads) {
+    int run = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = sc.cnt[w * E + e];
+      sc.cnt[w * E + e] = run;
+      run += c;
+    }
+    sc.tot[e] = run;
+  }
+  __syncthreads();
+  index_scan_offsets(E, bm, sc);
+}
+
 // Step 3: every valid assignment a goes to row(pos, a); an invalid one to
 // invalid(a).  Uses and advances the per-warp bases in sc.cnt.  No barrier.
 template <class RowFn, class InvalidFn>
@@ -116,12 +144,13 @@ __device__ __forceinline__ void index_scatter(const int32_t* src, int tk, int E,
   const int seg = (tk + nwarps - 1) / nwarps;
   const int beg = min(tk, warp * seg);
   const int end = min(tk, beg + seg);
+  const int bits = key_bits(E);
   for (int base = beg; base < end; base += 32) {
     const int a = base + lane;
     const bool in = a < end;
     const int e = in ? src[a] : -1;
     const bool valid = in && e >= 0 && e < E;
-    const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1);
+    const unsigned grp = peer_mask(valid ? e : (1 << bits), bits);
     if (valid)
       row(sc.offs[e] + sc.cnt[warp * E + e] + __popc(grp & lanemask_lt()), a);
     else if (in)

@@ -75,6 +75,12 @@ struct IndexPtrs {
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                          const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st,
                          bool pdl);
+// The same index built by three kernels over chunks of assignments (count,
+// scan, scatter); `scratch` holds align_split_scratch_words(T, k, E) ints.
+size_t align_split_scratch_words(int T, int k, int E);
+cudaError_t launch_align_split(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
+                               const IndexPtrs& idx, int32_t* scratch, int32_t* dev_status,
+                               cudaStream_t st, bool pdl);
 cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* inv_pos,
                            uint8_t* xq, float* xs, float* xs_rows, cudaStream_t st, bool pdl);
 // (inv_pos / xs_rows may be null: then only the per-token scales are written)

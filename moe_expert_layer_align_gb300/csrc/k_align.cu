@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(kAlignThreads)
   extern __shared__ int32_t sm[];
   IndexScratch sc;
   sc.carve(sm, kAlignWarps, E);
-  int32_t* sids = sm + IndexScratch::words(kAlignWarps, E);   // [T*k] staged ids (optional)
+  // [T*k] staged ids (optional), 16-byte aligned for vector stores
+  int32_t* sids = sm + ((IndexScratch::words(kAlignWarps, E) + 3) & ~static_cast<size_t>(3));
 
   const int tid = threadIdx.x;
   const int tk = T * k;
@@ -30,8 +31,16 @@ __global__ void __launch_bounds__(kAlignThreads)
   pdl_launch_dependents();
 
   if (tid == 0 && dev_status) *dev_status = 0;
-  if (stage_ids)
-    for (int i = tid; i < tk; i += kAlignThreads) sids[i] = __ldg(ids + i);
+  if (stage_ids) {
+    // 16-byte loads, several in flight per thread (one dependent load per
+    // iteration made this loop the kernel's cost at 32K assignments)
+    const int n4 = (reinterpret_cast<uintptr_t>(ids) & 15) ? 0 : tk / 4;
+    const int4* ids4 = reinterpret_cast<const int4*>(ids);
+    int4* s4 = reinterpret_cast<int4*>(sids);
+#pragma unroll 8
+    for (int i = tid; i < n4; i += kAlignThreads) s4[i] = __ldg(ids4 + i);
+    for (int i = 4 * n4 + tid; i < tk; i += kAlignThreads) sids[i] = __ldg(ids + i);
+  }
   const int32_t* src = stage_ids ? sids : ids;
 
   index_count_and_scan(src, tk, E, bm, sc);
@@ -60,7 +69,8 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int ti
   const int tk = T * k;
   const int stage_ids = tk <= kAlignMaxStagedIds ? 1 : 0;
   const size_t smem =
-      sizeof(int32_t) * (IndexScratch::words(kAlignWarps, E) + (stage_ids ? tk : 0));
+      sizeof(int32_t) * (((IndexScratch::words(kAlignWarps, E) + 3) & ~static_cast<size_t>(3)) +
+                         (stage_ids ? tk : 0));
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -73,6 +83,132 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int ti
   }
   return launch_kernel(moe_align_kernel, dim3(1), dim3(kAlignThreads), smem, st, pdl, ids, T, k, E,
                        bm, tiles_cap, idx, dev_status, stage_ids);
+}
+
+// ---------------------------------------------------------------- split build
+// For many assignments the same algorithm runs over chunks of kChunk
+// assignments, one CTA each, so that no single SM walks them all:
+//   count:   per-CTA expert histogram of its chunk (hist[b][e]);
+//   scan:    one CTA turns hist into per-CTA bases (exclusive prefix over b,
+//            in place), totals, padded offsets, padding and the task map;
+//   scatter: each CTA re-ranks its chunk and writes its assignments at
+//            offsets[e] + base[b][e] + (rank inside the chunk).
+// Chunks ascend in a and the in-chunk ranks are the block algorithm's, so
+// the result equals the single-CTA build's.
+constexpr int kChunk = 1024;
+constexpr int kSplitThreads = 256;
+constexpr int kSplitWarps = kSplitThreads / 32;
+
+__host__ __device__ inline size_t chunk_smem_words(int E) {
+  return ((IndexScratch::words(kSplitWarps, E) + 3) & ~static_cast<size_t>(3)) + kChunk;
+}
+
+__device__ __forceinline__ int stage_chunk(const int32_t* ids, int tk, int32_t* chunk) {
+  const int a0 = blockIdx.x * kChunk;
+  const int n = min(kChunk, tk - a0);
+  for (int i = threadIdx.x; i < n; i += kSplitThreads) chunk[i] = __ldg(ids + a0 + i);
+  return n;
+}
+
+__global__ void __launch_bounds__(kSplitThreads)
+    moe_align_count_kernel(const int32_t* __restrict__ ids, int tk, int E, int bm,
+                           int32_t* __restrict__ hist, int32_t* __restrict__ flags) {
+  extern __shared__ int32_t sm[];
+  IndexScratch sc;
+  sc.carve(sm, kSplitWarps, E);
+  int32_t* chunk = sm + (chunk_smem_words(E) - kChunk);
+  pdl_wait();
+  pdl_launch_dependents();
+  const int n = stage_chunk(ids, tk, chunk);
+  index_count_and_scan(chunk, n, E, bm, sc);
+  for (int e = threadIdx.x; e < E; e += kSplitThreads)
+    hist[static_cast<size_t>(blockIdx.x) * E + e] = sc.tot[e];
+  if (threadIdx.x == 0) flags[blockIdx.x] = *sc.flag;
+}
+
+__global__ void __launch_bounds__(kAlignThreads)
+    moe_align_scan_kernel(int32_t* __restrict__ hist, const int32_t* __restrict__ flags, int nb,
+                          int tk, int E, int bm, int tiles_cap, IndexPtrs idx,
+                          int32_t* dev_status) {
+  extern __shared__ int32_t sm[];
+  IndexScratch sc;
+  sc.carve(sm, 1, E);   // tot and offs only
+  const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int e = tid; e < E; e += kAlignThreads) {
+    int run = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int c = hist[static_cast<size_t>(b) * E + e];
+      hist[static_cast<size_t>(b) * E + e] = run;
+      run += c;
+    }
+    sc.tot[e] = run;
+    idx.counts[e] = run;
+  }
+  __syncthreads();
+  index_scan_offsets(E, bm, sc);
+  for (int e = tid; e <= E; e += kAlignThreads) idx.offsets[e] = sc.offs[e];
+  index_pads(E, tiles_cap * bm, sc, [&](int pos) { idx.sorted_ids[pos] = tk; });
+  if (tid == 0) *idx.num_tiles = sc.offs[E] / bm;
+  for (int q = tid; q < tiles_cap; q += kAlignThreads) {
+    const int4 t = index_tile(q, E, bm, sc);
+    idx.tile_expert[q] = t.x;
+    reinterpret_cast<int4*>(idx.tiles)[q] = t;
+  }
+  if (tid == 0 && dev_status) {
+    int any = 0;
+    for (int b = 0; b < nb; ++b) any |= flags[b];
+    *dev_status = any ? kStatusExpertId : 0;
+  }
+}
+
+__global__ void __launch_bounds__(kSplitThreads)
+    moe_align_scatter_kernel(const int32_t* __restrict__ ids, int tk, int E, int bm,
+                             const int32_t* __restrict__ base, IndexPtrs idx) {
+  extern __shared__ int32_t sm[];
+  IndexScratch sc;
+  sc.carve(sm, kSplitWarps, E);
+  int32_t* chunk = sm + (chunk_smem_words(E) - kChunk);
+  pdl_wait();
+  pdl_launch_dependents();
+  const int n = stage_chunk(ids, tk, chunk);
+  index_count_and_scan(chunk, n, E, bm, sc);   // in-chunk per-warp bases
+  for (int e = threadIdx.x; e < E; e += kSplitThreads)
+    sc.offs[e] = idx.offsets[e] + base[static_cast<size_t>(blockIdx.x) * E + e];
+  __syncthreads();
+  const int a0 = blockIdx.x * kChunk;
+  index_scatter(
+      chunk, n, E, sc,
+      [&](int pos, int a) {
+        idx.sorted_ids[pos] = a0 + a;
+        idx.inv_pos[a0 + a] = pos;
+      },
+      [&](int a) { idx.inv_pos[a0 + a] = -1; });
+}
+
+size_t align_split_scratch_words(int T, int k, int E) {
+  const int nb = (T * k + kChunk - 1) / kChunk;
+  return static_cast<size_t>(nb) * E + nb;
+}
+
+cudaError_t launch_align_split(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
+                               const IndexPtrs& idx, int32_t* scratch, int32_t* dev_status,
+                               cudaStream_t st, bool pdl) {
+  const int tk = T * k;
+  const int nb = (tk + kChunk - 1) / kChunk;
+  int32_t* hist = scratch;
+  int32_t* flags = scratch + static_cast<size_t>(nb) * E;
+  const size_t chunk_smem = 4 * chunk_smem_words(E);
+  cudaError_t e = launch_kernel(moe_align_count_kernel, dim3(nb), dim3(kSplitThreads), chunk_smem,
+                                st, pdl, ids, tk, E, bm, hist, flags);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(moe_align_scan_kernel, dim3(1), dim3(kAlignThreads),
+                    4 * IndexScratch::words(1, E), st, true, hist,
+                    static_cast<const int32_t*>(flags), nb, tk, E, bm, tiles_cap, idx, dev_status);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(moe_align_scatter_kernel, dim3(nb), dim3(kSplitThreads), chunk_smem, st,
+                       true, ids, tk, E, bm, static_cast<const int32_t*>(hist), idx);
 }
 
 }  // namespace moe

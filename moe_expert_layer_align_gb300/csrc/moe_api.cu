@@ -23,6 +23,8 @@ constexpr int kPlanCtas = 152;
 constexpr int kMaxSplits = 32;
 // Largest T*k for which GEMM CTAs rebuild the routing index themselves.
 constexpr int kSmemIndexMaxAssignments = 4096;
+// Above this many assignments the index is built over chunks by several CTAs.
+constexpr int kSplitIndexMinAssignments = 2048;
 
 struct Plan {
   int T, H, I, E, k, bm, fp8, out_bf16;
@@ -32,13 +34,14 @@ struct Plan {
   int me1, me2;            // weight tiles per work unit (2: large token tiles, bf16)
   int fused_act;           // SiLU-and-mul in the Gate-Up epilogue
   int smem_index;          // GEMM CTAs rebuild the index in shared memory
-  size_t off[14];
+  size_t off[15];
+  int split_index;         // index built by the count / scan / scatter kernels
   size_t total;
 };
 
 enum {
   kOffCounts, kOffOffsets, kOffSorted, kOffTileExpert, kOffTiles, kOffInvPos, kOffNumTiles,
-  kOffXq, kOffXs, kOffXsRows, kOffG, kOffA, kOffAs, kOffY, kNumOff
+  kOffIdxScratch, kOffXq, kOffXs, kOffXsRows, kOffG, kOffA, kOffAs, kOffY, kNumOff
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -82,6 +85,9 @@ void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int*
                   int max_splits = kMaxSplits) {
   double best = 1e300;
   int bs = 1, bk = kt_total;
+  // Large token tiles: the GEMM is tensor-bound and the fp32 partial rows
+  // would cost more than the balance a split buys back (measured).
+  if (bn >= 128 && static_cast<double>(m_tiles) * tiles >= kPlanCtas) max_splits = 1;
   for (int s = 1; s <= std::min(max_splits, kt_total); ++s) {
     const int kts = (kt_total + s - 1) / s;
     const int se = (kt_total + kts - 1) / kts;
@@ -162,6 +168,8 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
     }
     p->smem_index = fits;
   }
+  // many assignments: build the index over chunks, one CTA each
+  p->split_index = !p->smem_index && static_cast<int64_t>(s->T) * s->k > kSplitIndexMinAssignments;
   // workspace layout
   const size_t tk = static_cast<size_t>(s->T) * s->k;
   const size_t rc = p->rows_cap;
@@ -173,6 +181,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
       16u * p->tiles_cap,
       4 * tk,
       4,
+      p->split_index ? 4 * align_split_scratch_words(s->T, s->k, s->E) : 0,
       p->fp8 ? static_cast<size_t>(s->T) * s->H : 0,
       p->fp8 ? 4 * static_cast<size_t>(s->T) * (s->H / 128) : 0,
       p->fp8 ? 4 * rc * (s->H / 128) : 0,
@@ -209,6 +218,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->off_tiles = p.off[kOffTiles];
   L->off_inv_pos = p.off[kOffInvPos];
   L->off_num_tiles = p.off[kOffNumTiles];
+  L->off_index_scratch = p.off[kOffIdxScratch];
   L->off_xq = p.off[kOffXq];
   L->off_xs = p.off[kOffXs];
   L->off_xs_rows = p.off[kOffXsRows];
@@ -436,7 +446,11 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   };
 
   record(opts, 0, s);
-  if (!p.smem_index) {
+  if (p.split_index) {
+    e = launch_align_split(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip,
+                           reinterpret_cast<int32_t*>(at(kOffIdxScratch)), dev_status, s, chain());
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (!p.smem_index) {
     e = launch_align(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s, chain());
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }

@@ -45,7 +45,7 @@ def test_plan_is_consistent(T, H, I, E, k, fp8):
     assert L.rows_cap == L.tiles_cap * L.block_m
     assert L.split_gateup >= 1 and L.split_down >= 1
     offs = [L.off_counts, L.off_offsets, L.off_sorted_ids, L.off_tile_expert, L.off_tiles,
-            L.off_inv_pos, L.off_num_tiles, L.off_xq, L.off_xs, L.off_g, L.off_a, L.off_as,
+            L.off_inv_pos, L.off_num_tiles, L.off_index_scratch, L.off_xq, L.off_xs, L.off_g, L.off_a, L.off_as,
             L.off_y]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert L.off_y + 4 * L.split_down * L.rows_cap * H <= L.total_bytes

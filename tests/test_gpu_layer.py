@@ -200,3 +200,34 @@ def test_two_weight_tiles_per_unit(bm, single):
     assert L.weight_tiles_per_unit == (0x101 if single else 0x202)
     got = run_layer(wl, block_m=bm, opts=opts).float().cpu().numpy()
     assert_layer_close(got, oracle_layer(wl), "bf16", f"bm={bm} single={single}")
+
+
+@pytest.mark.parametrize("zipf", [None, 1.2])
+def test_index_over_chunks_is_bitwise_the_single_block_index(zipf):
+    # Above a few thousand assignments the index is built by several CTAs over
+    # chunks of the flat assignment list (the last one ragged); the rows must
+    # still list each expert's assignments in ascending order, exactly as the
+    # oracle's counting sort does, and invalid ids must still be flagged.
+    import moe_expert_layer_align_gb300 as moe
+    wl = small(3, 700, H=256, I=128, E=64)
+    ids = wl.topk_ids.clone()
+    if zipf is not None:
+        g = torch.Generator().manual_seed(11)
+        p = 1.0 / torch.arange(1, 65, dtype=torch.float64) ** zipf
+        draw = torch.multinomial(p.expand(700, 64), wl.k, replacement=False, generator=g)
+        ids = draw.int().cuda()
+    ids[5, 3] = -1
+    ids[690, 7] = 64
+    shape = moe.layer_shape(wl.x, wl.w13, ids, 0, torch.bfloat16)
+    L = moe.moe_plan(shape)
+    assert wl.T * wl.k > 2048 and L.off_xq > L.off_index_scratch   # chunked build planned
+    ws = torch.zeros(moe.moe_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    st = torch.full((1,), 777, dtype=torch.int32, device="cuda")
+    got = run_layer(wl, topk_ids=ids, workspace=ws, dev_status=st).float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert st.item() == (1 << 6)
+    v = moe.workspace_views(ws, shape)
+    ref = oracle.align(ids.cpu().numpy(), wl.E, L.block_m)
+    for n in ("counts", "offsets", "sorted_ids", "tile_expert", "tiles", "inv_pos", "num_tiles"):
+        np.testing.assert_array_equal(v[n].cpu().numpy().reshape(-1), ref[n].reshape(-1), n)
+    assert_layer_close(got, oracle_layer(wl, topk_ids=ids.cpu()), "bf16", "chunked index")
