@@ -76,6 +76,18 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float) -> float:
+    """The largest of every rank's `x` (each rank times its own replica; the
+    step takes as long as the slowest).  One process: `x` itself."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons in the background."""
 
@@ -167,6 +179,9 @@ class Layer:
         import moe_expert_layer_align_gb300 as moe
         self.moe, self.wl, self.stream, self.opts = moe, wl, stream, opts
         dev = wl.x.device
+        # The inputs were drawn on the current stream, whose freed blocks the
+        # allocations below may reuse: order the layer's stream after it.
+        stream.wait_stream(torch.cuda.current_stream(dev))
         self.fp8 = wl.mode == "fp8"
         self.w13 = wl.w13q if self.fp8 else wl.w13
         self.w2 = wl.w2q if self.fp8 else wl.w2
@@ -181,10 +196,11 @@ class Layer:
         else:
             self.hi_lo = None
             self.ids, self.w = wl.topk_ids, wl.topk_w
-        shape = moe.layer_shape(wl.x, self.w13, self.ids, 0, torch.bfloat16)
+        out_dtype = torch.float32 if wl.out == "f32" else torch.bfloat16
+        shape = moe.layer_shape(wl.x, self.w13, self.ids, 0, out_dtype)
         self.shape = shape
         self.ws = torch.empty(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device=dev)
-        self.out = torch.empty(wl.x.shape, dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty(wl.x.shape, dtype=out_dtype, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
         self.kernels_per_step = 5 + (1 if self.fp8 else 0) + (2 if self.hi_lo is not None else 0)
@@ -288,7 +304,7 @@ def e2e_time(wl, stream, steps, warmup):
     hx = wl.x.cpu().pin_memory()
     hid = None if dev_layer.hi_lo is not None else wl.topk_ids.cpu().pin_memory()
     hw = None if dev_layer.hi_lo is not None else wl.topk_w.cpu().pin_memory()
-    hout = torch.empty(wl.x.shape, dtype=torch.bfloat16).pin_memory()
+    hout = torch.empty(wl.x.shape, dtype=dev_layer.out.dtype).pin_memory()
     dx = wl.x                        # the layer reads these buffers
     did, dw = dev_layer.ids, dev_layer.w
 
@@ -313,7 +329,7 @@ def e2e_time(wl, stream, steps, warmup):
     us = s.elapsed_time(e) * 1e3 / steps
     h2d = hx.numel() * 2 + (0 if hid is None else hid.numel() * 4 + hw.numel() * 4)
     return {"value": us, "unit": "us", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": hout.numel() * 2}
+            "d2h_bytes_per_step": hout.numel() * hout.element_size()}
 
 
 def oracle_baseline(wl, topk_ids, topk_w, budget_s=15.0, max_tokens=None):
@@ -445,11 +461,7 @@ def run_cuda(args):
     barrier()
     times, wall = time_layer(layer, stream, flush, args.steps, args.warmup)
     barrier()
-    us = float(np.mean(times))
-    if ws_ > 1:
-        t = torch.tensor([us], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        us = float(t.item())
+    us = max_over_ranks(float(np.mean(times)))
     st = int(layer.status.item())
 
     result = None

@@ -82,7 +82,8 @@ cudaError_t launch_align_split(const int32_t* ids, int T, int k, int E, int bm, 
                                const IndexPtrs& idx, int32_t* scratch, int32_t* dev_status,
                                cudaStream_t st, bool pdl);
 cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* inv_pos,
-                           uint8_t* xq, float* xs, float* xs_rows, cudaStream_t st, bool pdl);
+                           uint8_t* xq, float* xs, float* xs_rows, int rows_cap, cudaStream_t st,
+                           bool pdl);
 // (inv_pos / xs_rows may be null: then only the per-token scales are written)
 cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
                        const int32_t* sorted_ids, int sentinel, void* A, float* As,

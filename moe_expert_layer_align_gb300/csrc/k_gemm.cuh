@@ -134,9 +134,20 @@ struct WorkUnit {
 template <int BN, int BSRC>
 __device__ __forceinline__ int4 load_tile(int q, const GemmParams& p, const int4* smem_tiles) {
   if (BSRC == kDense) return make_int4(0, q * BN, min(BN, p.dense_rows - q * BN), 0);
-  if (smem_tiles) return smem_tiles[q];
   // L2-coherent load: the Down GEMM may read the task map before its PDL wait
-  return __ldcg(reinterpret_cast<const int4*>(p.tiles) + q);
+  const int4 t = smem_tiles ? smem_tiles[q] : __ldcg(reinterpret_cast<const int4*>(p.tiles) + q);
+  // Every address below derives from this entry: row 0 of tile q is q*BN
+  // by construction, and an entry that is not a well-formed one (a workspace
+  // overwritten between the stages) becomes an empty tile of expert 0
+  // rather than an out-of-range access.
+  const bool ok = t.x >= 0 && t.x < p.E && t.z >= 0 && t.z <= BN;
+  return make_int4(ok ? t.x : 0, q * BN, ok ? t.z : 0, 0);
+}
+
+// Token of sorted row `a`'s assignment, or -1 for padding and any value
+// outside [0, T*k).
+__device__ __forceinline__ int assignment_token(int a, const GemmParams& p) {
+  return static_cast<unsigned>(a) < static_cast<unsigned>(p.T * p.topk) ? a / p.topk : -1;
 }
 
 __device__ __forceinline__ WorkUnit make_unit(int u, int num_tiles, int4 t, const GemmParams& p) {
@@ -254,7 +265,8 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     smem_tiles = si.tiles;
   } else {
     if (!early) pdl_wait();
-    num_tiles = (BSRC == kDense) ? (p.dense_rows + BN - 1) / BN : __ldcg(p.num_tiles);
+    num_tiles = (BSRC == kDense) ? (p.dense_rows + BN - 1) / BN
+                                 : min(max(__ldcg(p.num_tiles), 0), p.tiles_cap);
   }
   pdl_launch_dependents();   // dependents read nothing of ours before their own wait
   const int units = num_tiles * p.m_tiles * p.splits;
@@ -527,7 +539,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           const int n = lane + 32 * i;
           int row = -1;
           if (n < w.rows && n < BN)
-            row = p.scale_by_token ? row_assign(w.row0 + n) / p.topk : w.row0 + n;
+            row = p.scale_by_token ? assignment_token(row_assign(w.row0 + n), p) : w.row0 + n;
           srow[i] = row;
         }
         const int blk = (BSRC == kGather) ? ((lane < 16 ? w.mt * 64 : p.I + w.mt * 64) >> 7) : w.mt;
@@ -600,7 +612,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kR; ++i) {
           const int n = r0 + kRowStep * i;
-          tok[i] = n < w.rows ? row_assign(w.row0 + n) / p.topk : -1;
+          tok[i] = n < w.rows ? assignment_token(row_assign(w.row0 + n), p) : -1;
         }
       }
       int tok_next[kR];
@@ -631,7 +643,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kR; ++i) {
             const int n = r0 + kRowStep * i;
-            tok_next[i] = n < tn.z ? row_assign(tn.y + n) / p.topk : -1;
+            tok_next[i] = n < tn.z ? assignment_token(row_assign(tn.y + n), p) : -1;
           }
           tok_ready = true;
         }

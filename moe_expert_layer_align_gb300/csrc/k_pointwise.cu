@@ -33,7 +33,8 @@ __global__ void __launch_bounds__(128) moe_quant_x_kernel(const __nv_bfloat16* _
                                                           const int32_t* __restrict__ inv_pos,
                                                           uint8_t* __restrict__ xq,
                                                           float* __restrict__ xs,
-                                                          float* __restrict__ xs_rows) {
+                                                          float* __restrict__ xs_rows,
+                                                          int rows_cap) {
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
@@ -53,15 +54,18 @@ __global__ void __launch_bounds__(128) moe_quant_x_kernel(const __nv_bfloat16* _
   if (inv_pos != nullptr)
     for (int j = lane; j < k; j += 32) {
       const int pos = __ldg(inv_pos + static_cast<size_t>(t) * k + j);
-      if (pos >= 0) xs_rows[static_cast<size_t>(pos) * G + g] = s;
+      if (static_cast<unsigned>(pos) < static_cast<unsigned>(rows_cap))
+        xs_rows[static_cast<size_t>(pos) * G + g] = s;
     }
 }
 
 cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* inv_pos,
-                           uint8_t* xq, float* xs, float* xs_rows, cudaStream_t st, bool pdl) {
+                           uint8_t* xq, float* xs, float* xs_rows, int rows_cap, cudaStream_t st,
+                           bool pdl) {
   const dim3 grid(T, (H / 128 + 3) / 4);
   return launch_kernel(moe_quant_x_kernel, grid, dim3(128), 0, st, pdl,
-                       static_cast<const __nv_bfloat16*>(x), T, H, k, inv_pos, xq, xs, xs_rows);
+                       static_cast<const __nv_bfloat16*>(x), T, H, k, inv_pos, xq, xs, xs_rows,
+                       rows_cap);
 }
 
 // ---------------------------------------------------------------- act
@@ -165,6 +169,7 @@ __global__ void __launch_bounds__(128)
     for (int b = 0; b < kCombineBatch; ++b) {
       const int j = j0 + b;
       pos[b] = j < k ? __ldg(inv_pos + static_cast<size_t>(t) * k + j) : -1;
+      if (pos[b] >= rows_cap) pos[b] = -1;   // only rows of the index are read
       w[b] = j < k ? __ldg(topk_w + static_cast<size_t>(t) * k + j) : 0.f;
     }
 #pragma unroll

@@ -460,7 +460,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
     // with the shared-memory index the scales stay per token (the Gate-Up
     // epilogue looks tokens up in its own index)
     e = launch_quant_x(x, p.T, p.H, p.k, p.smem_index ? nullptr : ip.inv_pos, xq, xs,
-                       p.smem_index ? nullptr : xs_rows, s, chain());
+                       p.smem_index ? nullptr : xs_rows, p.rows_cap, s, chain());
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
 

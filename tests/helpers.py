@@ -9,6 +9,10 @@ import torch
 BF16_REL_L2 = 1e-2
 BF16_MAX_ABS_FRAC = 3e-2
 FP8_REL_L2 = 5e-3
+# Router: scores within SCORE_TOL of the fp64 oracle; top-k ids equal except
+# where the oracle's k-th and (k+1)-th scores lie within TIE_GAP.
+SCORE_TOL = 2e-3
+TIE_GAP = 1e-5
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:
@@ -64,3 +68,38 @@ def run_layer(wl, topk_ids=None, topk_w=None, block_m=0, opts=None, dev_status=N
     return moe.moe_forward(wl.x, wl.w13q, wl.w2q, ids, w, scales=(wl.w13s, wl.w2s),
                            out_dtype=out_dtype, block_m=block_m, opts=opts,
                            dev_status=dev_status, workspace=workspace)
+
+
+def check_topk(ids_gpu, ids_ref, scores_ref, k, scores_gpu=None):
+    """The selected id sets must match except where the oracle's k-th and
+    (k+1)-th scores lie within TIE_GAP; the GPU's own order must be
+    descending in its scores."""
+    for t in range(ids_ref.shape[0]):
+        if scores_gpu is not None:
+            assert np.all(np.diff(scores_gpu[t][ids_gpu[t]]) <= 0), t
+        if set(ids_gpu[t]) == set(ids_ref[t]):
+            continue
+        s = np.sort(scores_ref[t])[::-1]
+        assert s[k - 1] - s[k] < TIE_GAP, (t, ids_gpu[t], ids_ref[t])
+
+
+def oracle_layer_sampled(wl, ids, w, sel):
+    """Oracle rows of the tokens `sel` only.  A token's output depends on its
+    own x row, ids, weights and the experts it routes to, so the oracle is
+    fed just those: the sampled x rows and the used experts' weights, with
+    the ids renumbered into that expert subset (a pure selection of inputs,
+    no arithmetic)."""
+    import oracle
+    sel = np.asarray(sel)
+    ids_s = np.asarray(ids)[sel]
+    used, inv = np.unique(ids_s, return_inverse=True)
+    ids_c = inv.reshape(ids_s.shape).astype(np.int32)
+    w_s = np.asarray(w)[sel]
+    rows = torch.from_numpy(sel).long().to(wl.x.device)
+    ex = torch.from_numpy(used).long().to(wl.x.device)
+    x = bits16(wl.x[rows])
+    if wl.mode == "bf16":
+        return oracle.moe_bf16(x, bits16(wl.w13[ex]), bits16(wl.w2[ex]), ids_c, w_s)
+    xq, xs = oracle.quant_x(x)
+    return oracle.moe_fp8(xq, xs, u8(wl.w13q[ex]), wl.w13s[ex].cpu().numpy(), u8(wl.w2q[ex]),
+                          wl.w2s[ex].cpu().numpy(), ids_c, w_s)

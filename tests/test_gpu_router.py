@@ -8,26 +8,9 @@ import torch
 
 import oracle
 from moe_expert_layer_align_gb300 import workloads
-from helpers import assert_layer_close, bits16, oracle_layer, run_layer
+from helpers import SCORE_TOL, assert_layer_close, bits16, check_topk, oracle_layer, run_layer
 
 pytestmark = pytest.mark.gpu
-
-SCORE_TOL = 2e-3
-TIE_GAP = 1e-5
-
-
-def check_topk(ids_gpu, ids_ref, scores_ref, k, scores_gpu=None):
-    """The selected id sets must match except where the oracle's k-th and
-    (k+1)-th scores lie within TIE_GAP; the GPU's own order must be
-    descending in its scores."""
-    for t in range(ids_ref.shape[0]):
-        if scores_gpu is not None:
-            assert np.all(np.diff(scores_gpu[t][ids_gpu[t]]) <= 0), t
-        if set(ids_gpu[t]) == set(ids_ref[t]):
-            continue
-        s = np.sort(scores_ref[t])[::-1]
-        assert s[k - 1] - s[k] < TIE_GAP, (t, ids_gpu[t], ids_ref[t])
-
 
 @pytest.mark.parametrize("T", [4, 16, 64, 256, 300])
 def test_router_matches_oracle(T):
