@@ -55,7 +55,7 @@ size_t gemm_index_smem_bytes(int nwarps, int E, int tk, int rows_cap, int tiles_
 
 // Shared memory of one GEMM instantiation without the index, and its warps.
 size_t gemm_smem_bytes(int fp8, int bn, int bsrc);
-int gemm_warps(int bn, int bsrc);
+int gemm_warps(int fp8, int bn, int bsrc);
 constexpr size_t kMaxGemmSmem = 227 * 1024;
 
 // Launch the persistent GEMM (defined per mode in k_gemm_{bf16,fp8}.cu).

@@ -60,7 +60,6 @@
 
 namespace moe {
 
-constexpr int kRoleThreads = 192;           // TMA, MMA and 4 epilogue warps
 constexpr int kTileM = 128;                 // weight rows per tile (MMA M)
 constexpr int kKBytes = 128;                // K bytes per pipeline stage
 constexpr int kABytes = kTileM * kKBytes;   // 16 KB weight tile per stage
@@ -77,6 +76,13 @@ template <int FP8, int BN, int BSRC = kDirect, int ME = 1>
 struct GemmShape {
   static constexpr int kStages = stages_for(FP8, BN, ME);
   static constexpr int kAStage = ME * kABytes;
+  // Epilogue warps: four (one per TMEM lane quadrant), or eight for FP8
+  // with wide token tiles, where the per-K-block promotion is the busiest
+  // role; the second warp of a quadrant then takes the upper half of the
+  // columns.
+  static constexpr int kEpiWarps = (FP8 && BN >= 64) ? 8 : 4;
+  static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kRoleThreads = 64 + kEpiThreads;   // + TMA and MMA warps
   // token-row gather warps (gathered operand only) and block size
   static constexpr int kGatherWarps = BSRC == kGather ? (BN >= 128 ? 2 : 1) : 0;
   static constexpr int kGatherThreads = 32 * kGatherWarps;
@@ -97,7 +103,9 @@ struct GemmShape {
   static constexpr int kOffBar = kOffB + kStages * kBBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;  // + drain
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffIdx = (kOffMisc + 16 + 15) & ~15;       // shared-memory index
+  // FP8: the token-operand scales of one K block, double-buffered [2][BN]
+  static constexpr int kOffScale = (kOffMisc + 16 + 15) & ~15;
+  static constexpr int kOffIdx = kOffScale + (FP8 ? 2 * BN * 4 : 0);  // shared-memory index
   static constexpr size_t kSmemBytes = 1024 + kOffIdx;             // without the index
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0");
   static_assert(ME == 1 || !FP8, "FP8 promotion keeps one weight tile per unit");
@@ -208,6 +216,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
   const uint32_t bar_drain = bar_acce + 8 * S::kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 4);
+  float* sx_buf = reinterpret_cast<float*>(smem + S::kOffScale);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -221,7 +230,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     }
     for (int b = 0; b < S::kAccBufs; ++b) {
       mbar_init(bar_accf + 8 * b, 1);
-      mbar_init(bar_acce + 8 * b, 4);  // one arrival per epilogue warp
+      mbar_init(bar_acce + 8 * b, S::kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -424,24 +433,25 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < kRoleThreads / 32) {
+  } else if (warp < S::kRoleThreads / 32) {
     // ------------------------------------------------------------ epilogue
     if (early) pdl_wait();   // reads scales, writes outputs the chain reads
     if (smem_idx && p.write_index && blockIdx.x == 0) {
       // The later stages read the index from global memory.
       const int et = threadIdx.x - 64;
-      for (int e = et; e < p.E; e += 128) p.index_out.counts[e] = si.sc.tot[e];
-      for (int e = et; e <= p.E; e += 128) p.index_out.offsets[e] = si.sc.offs[e];
-      for (int pos = et; pos < p.rows_cap; pos += 128) {
+      constexpr int kET = S::kEpiThreads;
+      for (int e = et; e < p.E; e += kET) p.index_out.counts[e] = si.sc.tot[e];
+      for (int e = et; e <= p.E; e += kET) p.index_out.offsets[e] = si.sc.offs[e];
+      for (int pos = et; pos < p.rows_cap; pos += kET) {
         const int a = si.rows[pos];
         p.index_out.sorted_ids[pos] = a;
         if (a < tk) p.index_out.inv_pos[a] = pos;
       }
-      for (int a = et; a < tk; a += 128) {
+      for (int a = et; a < tk; a += kET) {
         const int e = si.ids[a];
         if (e < 0 || e >= p.E) p.index_out.inv_pos[a] = -1;
       }
-      for (int q = et; q < p.tiles_cap; q += 128) {
+      for (int q = et; q < p.tiles_cap; q += kET) {
         const int4 t = si.tiles[q];
         p.index_out.tile_expert[q] = t.x;
         reinterpret_cast<int4*>(p.index_out.tiles)[q] = t;
@@ -453,6 +463,10 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     }
     const int qd = warp & 3;          // TMEM lane quadrant this warp may read
     const int r = qd * 32 + lane;     // row of the 128-row weight tile
+    // column range of this warp: all BN columns, or one half of them when
+    // two warps share the quadrant (FP8 with eight epilogue warps)
+    constexpr int kWarpCols = BN / (S::kEpiWarps / 4);
+    const int c_base = ((warp - 2) >> 2) * kWarpCols;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(qd * 32) << 16);
     int ab = 0;
     uint32_t aph = 0;
@@ -530,62 +544,110 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           col_ok = col < p.M;
         }
         float* outp = p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0) * p.M + col;
-        // Per-column scale rows: lane l serves columns l, l+32, ...
-        constexpr int kCPerLane = BN / 32 > 0 ? BN / 32 : 1;
+        // The token-operand scale of column n is the same for every row, so
+        // the four epilogue warps stage it in shared memory once per K block
+        // (epilogue thread et loads column et) and read it back as broadcast
+        // 16-byte loads.  One named barrier per K block publishes the next
+        // block's scales; the buffer written is never the one being read.
+        const int et = threadIdx.x - 64;
         const int KB = p.kt_total;
-        int srow[kCPerLane];
-#pragma unroll
-        for (int i = 0; i < kCPerLane; ++i) {
-          const int n = lane + 32 * i;
-          int row = -1;
-          if (n < w.rows && n < BN)
-            row = p.scale_by_token ? assignment_token(row_assign(w.row0 + n), p) : w.row0 + n;
-          srow[i] = row;
-        }
+        int srow = -1;
+        if (et < BN && et < w.rows)
+          srow = p.scale_by_token ? assignment_token(row_assign(w.row0 + et), p) : w.row0 + et;
+        const float* bsp = srow >= 0 ? p.b_scale + static_cast<size_t>(srow) * KB : nullptr;
         const int blk = (BSRC == kGather) ? ((lane < 16 ? w.mt * 64 : p.I + w.mt * 64) >> 7) : w.mt;
         const float* wsp = p.w_scale + (static_cast<size_t>(w.e) * (p.M >> 7) + blk) * KB;
-        float acc[BN];
+        // Scales are fetched two K blocks ahead of their use: the epilogue is
+        // the busy role here, so a load issued in the block that needs it
+        // would put its latency on the critical path.
+        auto sx_at = [&](int kt) { return (bsp && kt < w.kt1) ? __ldg(bsp + kt) : 0.f; };
+        auto sw_at = [&](int kt) { return kt < w.kt1 ? __ldg(wsp + kt) : 0.f; };
+        if (et < BN) sx_buf[et] = sx_at(w.kt0);
+        float sx_n1 = sx_at(w.kt0 + 1), sx_n2 = sx_at(w.kt0 + 2);
+        float sw_0 = sw_at(w.kt0), sw_1 = sw_at(w.kt0 + 1), sw_2 = sw_at(w.kt0 + 2);
+        named_barrier_sync(1, S::kEpiThreads);
+        // this warp's columns c_base.. in packed pairs (fma.rn.f32x2: two
+        // fp32 FMAs, each rounded as fmaf)
+        uint64_t acc2[kWarpCols / 2];
 #pragma unroll
-        for (int j = 0; j < BN; ++j) acc[j] = 0.f;
+        for (int j = 0; j < kWarpCols / 2; ++j) acc2[j] = 0ull;
+        const int wrows = w.rows - c_base;   // valid columns from c_base on
         bool ok = true;
+        int cur = 0;
         for (int kt = w.kt0; kt < w.kt1; ++kt) {
-          const float sw = __ldg(wsp + kt);
-          float sx[kCPerLane];
-#pragma unroll
-          for (int i = 0; i < kCPerLane; ++i)
-            sx[i] = srow[i] >= 0 ? __ldg(p.b_scale + static_cast<size_t>(srow[i]) * KB + kt) : 0.f;
+          const float sw = sw_0;
+          sw_0 = sw_1;
+          sw_1 = sw_2;
+          sw_2 = sw_at(kt + 3);
+          const float sx_stage = sx_n1;   // published below for kt + 1
+          sx_n1 = sx_n2;
+          sx_n2 = sx_at(kt + 3);
           if (!mbar_wait(bar_accf + 8 * ab, aph)) {
             report_timeout(p, abort_flag);
             ok = false;
-            break;
           }
-          tc_fence_after();
+          if (ok) {
+            tc_fence_after();
+            const float* sxb = sx_buf + cur * BN;
+            const uint64_t sw2 = pack_f32x2(sw, sw);
+            // TMEM reads two 16-column chunks at a time, one wait per pair
+            constexpr int kLdBatch = kWarpCols / 16 < 2 ? kWarpCols / 16 : 2;
 #pragma unroll
-          for (int c = 0; c < BN / 16; ++c) {
-            if (c * 16 < w.rows) {
-              uint32_t v[16];
-              tmem_ld16(t_lane + static_cast<uint32_t>(ab * BN + c * 16), v);
-              tmem_ld_wait();
+            for (int c0 = 0; c0 < kWarpCols / 16; c0 += kLdBatch) {
+              if (c0 * 16 < wrows) {
+                uint32_t v[kLdBatch][16];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int n = c * 16 + j;
-                const float s = sw * __shfl_sync(0xffffffffu, sx[n >> 5], n & 31);
-                acc[n] = fmaf(__uint_as_float(v[j]), s, acc[n]);
+                for (int g = 0; g < kLdBatch; ++g)
+                  if ((c0 + g) * 16 < wrows)
+                    tmem_ld16(t_lane + static_cast<uint32_t>(ab * BN + c_base + (c0 + g) * 16),
+                              v[g]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < kLdBatch; ++g) {
+                  if ((c0 + g) * 16 >= wrows) continue;
+                  tmem_ld_bind(v[g]);
+                  const int c = c0 + g;
+#pragma unroll
+                  for (int q4 = 0; q4 < 4; ++q4) {
+                    const float4 s4 =
+                        *reinterpret_cast<const float4*>(sxb + c_base + c * 16 + 4 * q4);
+                    const int h = (c * 16 + 4 * q4) / 2;
+                    const uint64_t s01 = mul_f32x2(pack_f32x2(s4.x, s4.y), sw2);
+                    const uint64_t s23 = mul_f32x2(pack_f32x2(s4.z, s4.w), sw2);
+                    acc2[h] = fma_f32x2(pack_u32x2(v[g][4 * q4 + 0], v[g][4 * q4 + 1]), s01, acc2[h]);
+                    acc2[h + 1] =
+                        fma_f32x2(pack_u32x2(v[g][4 * q4 + 2], v[g][4 * q4 + 3]), s23, acc2[h + 1]);
+                  }
+                }
               }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
+            if (++ab == S::kAccBufs) {
+              ab = 0;
+              aph ^= 1u;
+            }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
-          if (++ab == S::kAccBufs) {
-            ab = 0;
-            aph ^= 1u;
+          cur ^= 1;
+          if (et < BN) sx_buf[cur * BN + et] = sx_stage;
+          // Every epilogue warp reaches this barrier once per K block, also
+          // after a timeout; the OR of the abort state it returns ends all
+          // four loops at the same K block.
+          if (named_barrier_or(1, S::kEpiThreads, !ok || *abort_flag)) {
+            ok = false;
+            break;
           }
         }
         if (!ok) break;
 #pragma unroll
-        for (int n = 0; n < BN; ++n)
-          if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = acc[n];
+        for (int h = 0; h < kWarpCols / 2; ++h) {
+          float a0, a1;
+          unpack_f32x2(acc2[h], a0, a1);
+          const int n = c_base + 2 * h;
+          if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = a0;
+          if (n + 1 < w.rows && col_ok) outp[static_cast<size_t>(n + 1) * p.M] = a1;
+        }
       }
     }
   } else if (BSRC == kGather) {
@@ -595,7 +657,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     // copied: their MMA columns are never stored.
     constexpr int kR = S::kRowsPerGatherThread;
     constexpr int kRowStep = 4 * (S::kGatherWarps > 0 ? S::kGatherWarps : 1);
-    const int t = threadIdx.x - kRoleThreads;
+    const int t = threadIdx.x - S::kRoleThreads;
     const int c = t & 7;
     const int r0 = t >> 3;
     const uint8_t* rows = static_cast<const uint8_t*>(p.b_rows) + c * 16;

@@ -32,10 +32,19 @@ size_t gemm_smem_bytes(int fp8, int bn, int bsrc) {
   return fp8 ? smem_bytes_bn<1, kDirect>(bn) : smem_bytes_bn<0, kDirect>(bn);
 }
 
-int gemm_warps(int bn, int bsrc) {
-  return bsrc == kGather ? (bn >= 128 ? GemmShape<0, 128, kGather>::kWarps
-                                      : GemmShape<0, 16, kGather>::kWarps)
-                         : GemmShape<0, 16, kDirect>::kWarps;
+template <int FP8>
+int gemm_warps_t(int bn, int bsrc) {
+  switch (bn) {
+    case 16: return bsrc == kGather ? GemmShape<FP8, 16, kGather>::kWarps : GemmShape<FP8, 16, kDirect>::kWarps;
+    case 32: return bsrc == kGather ? GemmShape<FP8, 32, kGather>::kWarps : GemmShape<FP8, 32, kDirect>::kWarps;
+    case 64: return bsrc == kGather ? GemmShape<FP8, 64, kGather>::kWarps : GemmShape<FP8, 64, kDirect>::kWarps;
+    case 128: return bsrc == kGather ? GemmShape<FP8, 128, kGather>::kWarps : GemmShape<FP8, 128, kDirect>::kWarps;
+    default: return bsrc == kGather ? GemmShape<FP8, 256, kGather>::kWarps : GemmShape<FP8, 256, kDirect>::kWarps;
+  }
+}
+
+int gemm_warps(int fp8, int bn, int bsrc) {
+  return fp8 ? gemm_warps_t<1>(bn, bsrc) : gemm_warps_t<0>(bn, bsrc);
 }
 
 size_t gemm_index_smem_bytes(int nwarps, int E, int tk, int rows_cap, int tiles_cap) {

@@ -162,7 +162,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
     bool fits = tk <= kSmemIndexMaxAssignments && o && o->smem_index;
     for (int bsrc : {static_cast<int>(kGather), static_cast<int>(kDirect)}) {
       const size_t need = gemm_smem_bytes(p->fp8, p->bm, bsrc) +
-                          gemm_index_smem_bytes(gemm_warps(p->bm, bsrc), s->E, tk, p->rows_cap,
+                          gemm_index_smem_bytes(gemm_warps(p->fp8, p->bm, bsrc), s->E, tk, p->rows_cap,
                                                 p->tiles_cap);
       if (need > kMaxGemmSmem) fits = false;
     }
