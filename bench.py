@@ -69,6 +69,45 @@ def ncu_traffic(kernel: str, T: int):
     return e.get("dram_bytes_per_launch")
 
 
+def record_traffic(csv_path: str, cfg: int, T: int, command: str):
+    """Store the DRAM bytes per launch of the expert GEMMs from an ncu capture
+    (exported with `ncu -i <report> --page raw --csv > <csv_path>`) in
+    profiles/traffic.json, keyed by workload and stage and stamped with the
+    hash of the GEMM sources it was taken on."""
+    import csv
+    rows = list(csv.reader(open(csv_path)))
+    hdr, data = rows[0], rows[2:]
+    col = {h: i for i, h in enumerate(hdr)}
+    stage_of = {"0": "gateup", "1": "down", "2": "router"}
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    d = json.load(open(p)) if os.path.exists(p) else {}
+    d["_what"] = ("DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the "
+                  "expert GEMMs from ncu --set full captures; source_hash covers the GEMM "
+                  "sources each was taken on (bench.py reports null for a stale one).")
+    for r in data:
+        name = r[col["Kernel Name"]]
+        if "moe_gemm_kernel" not in name:
+            continue
+        targs = name[name.index("<") + 1: name.index(">")].replace(" ", "").split(",")
+        stage = stage_of.get(targs[2], "gemm")
+        rd = float(r[col["dram__bytes_read.sum"]].replace(",", ""))
+        wr = float(r[col["dram__bytes_write.sum"]].replace(",", ""))
+        unit_r, unit_w = rows[1][col["dram__bytes_read.sum"]], rows[1][col["dram__bytes_write.sum"]]
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+        rd *= scale.get(unit_r, 1)
+        wr *= scale.get(unit_w, 1)
+        dur = float(r[col["gpu__time_duration.sum"]].replace(",", ""))
+        dur *= {"ns": 1, "nsecond": 1, "us": 1e3, "usecond": 1e3, "ms": 1e6,
+                "msecond": 1e6}.get(rows[1][col["gpu__time_duration.sum"]], 1)
+        d[f"c{cfg}:{stage}@T={T}"] = {
+            "kernel": name.split("(")[0].replace("void ", ""),
+            "source_hash": gemm_source_hash(), "duration_ns": dur,
+            "dram_bytes_read": int(rd), "dram_bytes_write": int(wr),
+            "dram_bytes_per_launch": int(rd + wr), "command": command}
+    json.dump(d, open(p, "w"), indent=1, sort_keys=True)
+    print(json.dumps({k: v for k, v in d.items() if k.startswith(f"c{cfg}:")}, indent=1))
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -562,7 +601,14 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ncu", action="store_true", help="profiler mode (no bench line)")
+    ap.add_argument("--record-traffic", metavar="CSV",
+                    help="store DRAM bytes per GEMM launch of --config/--T from an ncu raw-page "
+                         "CSV export in profiles/traffic.json (no GPU needed)")
+    ap.add_argument("--traffic-command", default="",
+                    help="the ncu command the CSV came from (recorded beside the numbers)")
     args = ap.parse_args()
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, args.config, args.T, args.traffic_command)
     if args.ncu:
         return run_ncu(args)
     if args.warmup < 3:

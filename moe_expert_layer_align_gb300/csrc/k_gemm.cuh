@@ -65,7 +65,7 @@ constexpr int kKBytes = 128;                // K bytes per pipeline stage
 constexpr int kABytes = kTileM * kKBytes;   // 16 KB weight tile per stage
 
 __host__ __device__ constexpr int stages_for(int fp8, int bn, int me) {
-  return me == 1 ? (bn <= 32 ? 8 : bn == 64 ? (fp8 ? 7 : 8) : bn == 128 ? (fp8 ? 5 : 6) : 4)
+  return me == 1 ? (bn <= 64 ? 8 : bn == 128 ? (fp8 ? 5 : 6) : 4)
                  : (196608 / (me * kABytes + bn * kKBytes) < 8 ? 196608 / (me * kABytes + bn * kKBytes)
                                                                : 8);
 }
@@ -109,7 +109,8 @@ struct GemmShape {
   static constexpr size_t kSmemBytes = 1024 + kOffIdx;             // without the index
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0");
   static_assert(ME == 1 || !FP8, "FP8 promotion keeps one weight tile per unit");
-  static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+                "tcgen05.alloc takes a power of two from 32 to 512 columns");
 };
 
 // Shared-memory index: build scratch, staged ids, sorted rows, task map.
@@ -364,9 +365,14 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       int ab = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); ok && it.valid(); it.advance()) {
         if (*abort_flag) break;
-        const WorkUnit w = make_unit(u, num_tiles, make_int4(0, 0, 0, 0), p);  // K range only
+        const WorkUnit w = it.take(p);
+        // The MMA's N is the tile's valid rows rounded up to 16: columns of
+        // padding rows are never computed (nor stored), so a wide token tile
+        // costs a narrow one's MMA time when few of its rows are valid.
+        const int n_eff = min(BN, max(16, (w.rows + 15) & ~15));
+        const uint32_t idesc = (S::kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(n_eff >> 3) << 17);
         if (!FP8) {
           if (!mbar_wait(bar_acce + 8 * ab, aph ^ 1u)) {
             report_timeout(p, abort_flag);
@@ -401,9 +407,9 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
             for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
               const uint32_t acc = FP8 ? (k > 0) : (kt > w.kt0 || k > 0);
               if (FP8)
-                mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, S::kIdesc, acc);
+                mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
               else
-                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, S::kIdesc, acc);
+                mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
             }
           }
           tc_commit(bar_empty + 8 * stage);
@@ -677,8 +683,14 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           tok[i] = n < w.rows ? assignment_token(row_assign(w.row0 + n), p) : -1;
         }
       }
+      // The next unit's rows are looked up in two steps spread over this
+      // unit's first stages (its task-map entry, then its sorted rows), so
+      // neither dependent load stalls the copies of the current unit.
       int tok_next[kR];
       tok_ready = false;
+      const int nk = w.kt1 - w.kt0;
+      const int step_a = nk > 1 ? 1 : 0;           // sorted-row loads issued
+      const int step_b = nk > 2 ? 2 : nk - 1;      // turned into token rows
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u)) {
           report_timeout(p, abort_flag);
@@ -699,15 +711,22 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           stage = 0;
           phase ^= 1u;
         }
-        if (kt == w.kt0 && it.has_next()) {
-          // the next unit's task-map entry has landed by now: fetch its rows
-          const int4 tn = it.next;
+        if (it.has_next()) {
+          const int i_kt = kt - w.kt0;
+          if (i_kt == step_a) {
+            const int4 tn = it.next;
 #pragma unroll
-          for (int i = 0; i < kR; ++i) {
-            const int n = r0 + kRowStep * i;
-            tok_next[i] = n < tn.z ? assignment_token(row_assign(tn.y + n), p) : -1;
+            for (int i = 0; i < kR; ++i) {
+              const int n = r0 + kRowStep * i;
+              tok_next[i] = n < tn.z ? row_assign(tn.y + n) : -1;   // assignment for now
+            }
           }
-          tok_ready = true;
+          if (i_kt == step_b) {
+#pragma unroll
+            for (int i = 0; i < kR; ++i)
+              tok_next[i] = tok_next[i] >= 0 ? assignment_token(tok_next[i], p) : -1;
+            tok_ready = true;
+          }
         }
       }
       if (tok_ready) {
