@@ -127,7 +127,30 @@ typedef struct {
   /* 1: one 128-row weight tile per GEMM work unit even for large token tiles
    * (where the plan pairs two to halve the token-tile traffic per MMA). */
   int32_t single_weight_tile;
+  /* Shared experts (SGLang's shared-expert fusion, which DeepSeek-V3, GLM4-MoE
+   * and Llama 4 layers use): w13 / w2 (and FP8 scales) hold E routed experts
+   * followed by num_shared_experts experts that every token selects with
+   * weight shared_expert_weight (0 is read as 1.0); they become extra
+   * assignments of the index (slots k.. of each token), so the grouped GEMMs
+   * run them with the routed ones.  0 = none; at most 8. */
+  int32_t num_shared_experts;
+  float shared_expert_weight;
+  /* Expert parallelism, local part: the E routed experts held here are the
+   * global ids [ep_first_expert, ep_first_expert + E) of ep_num_experts; an
+   * assignment to another valid id is dropped without a flag (another rank
+   * holds that expert), ids outside [0, ep_num_experts) are invalid (dropped
+   * and flagged).  The output is this rank's partial sum.  0 = off. */
+  int32_t ep_first_expert;
+  int32_t ep_num_experts;
 } moe_forward_opts;
+
+/* Options of moe_align_ex: the same shared-expert and expert-parallel mapping
+ * of topk_ids onto the experts of the index as moe_forward_opts. */
+typedef struct {
+  int32_t num_shared_experts;
+  int32_t ep_first_expert;
+  int32_t ep_num_experts;
+} moe_align_opts;
 
 /* Where moe_forward keeps its intermediates inside the caller's workspace
  * (byte offsets from the workspace base) and the plan it runs. */
@@ -174,6 +197,17 @@ MOE_API size_t moe_workspace_bytes(const moe_shape* shape, const moe_forward_opt
 MOE_API moe_status moe_align(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
                      int32_t block_m, const moe_index* idx, int32_t* dev_status,
                      void* stream);
+
+/* moe_align with shared experts and / or the expert-parallel local mapping
+ * (opts nullable = moe_align).  The index then covers T*(k + n_shared)
+ * assignments a = t*(k + n_shared) + j over E + n_shared experts (shared
+ * expert s of token t is slot k + s, expert E + s); size its buffers with
+ * moe_index_tiles_cap(T, k + n_shared, E + n_shared, block_m).  Mapped ids
+ * are staged on chip: T*(k + n_shared) <= 32768, else MOE_ERR_SHAPE.  Remote
+ * ids (expert parallelism) get inv_pos -1 like invalid ones but no flag. */
+MOE_API moe_status moe_align_ex(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E,
+                        int32_t block_m, const moe_align_opts* opts, const moe_index* idx,
+                        int32_t* dev_status, void* stream);
 
 /* The whole layer.  Inputs:
  *   x        bf16 [T][H]

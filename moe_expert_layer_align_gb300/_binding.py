@@ -45,7 +45,13 @@ class moe_scales(ctypes.Structure):
 class moe_forward_opts(ctypes.Structure):
     _fields_ = [("disable_pdl", _i32), ("split_gateup", _i32), ("split_down", _i32),
                 ("grid_ctas", _i32), ("stage_events", _vp * 8), ("separate_act", _i32),
-                ("smem_index", _i32), ("single_weight_tile", _i32)]
+                ("smem_index", _i32), ("single_weight_tile", _i32),
+                ("num_shared_experts", _i32), ("shared_expert_weight", ctypes.c_float),
+                ("ep_first_expert", _i32), ("ep_num_experts", _i32)]
+
+
+class moe_align_opts(ctypes.Structure):
+    _fields_ = [("num_shared_experts", _i32), ("ep_first_expert", _i32), ("ep_num_experts", _i32)]
 
 
 class moe_workspace_layout(ctypes.Structure):
@@ -70,6 +76,8 @@ def _load() -> ctypes.CDLL:
         "moe_plan": (_i32, [P(moe_shape), P(moe_forward_opts), P(moe_workspace_layout)]),
         "moe_workspace_bytes": (_sz, [P(moe_shape), P(moe_forward_opts)]),
         "moe_align": (_i32, [_vp, _i32, _i32, _i32, _i32, P(moe_index), _vp, _vp]),
+        "moe_align_ex": (_i32, [_vp, _i32, _i32, _i32, _i32, P(moe_align_opts), P(moe_index),
+                                _vp, _vp]),
         "moe_forward": (_i32, [P(moe_shape), _vp, _vp, _vp, _vp, _vp, P(moe_scales), _vp, _vp,
                                _sz, _vp, _vp]),
         "moe_forward_ex": (_i32, [P(moe_shape), _vp, _vp, _vp, _vp, _vp, P(moe_scales), _vp,
@@ -93,7 +101,7 @@ def _load() -> ctypes.CDLL:
 lib = _load()
 SYMBOLS = ("moe_index_tiles_cap", "moe_plan", "moe_workspace_bytes", "moe_align", "moe_forward",
            "moe_forward_ex", "moe_combine", "moe_router_prepare", "moe_router_workspace_bytes",
-           "moe_router_topk", "moe_forward_static", "moe_status_str")
+           "moe_router_topk", "moe_forward_static", "moe_status_str", "moe_align_ex")
 # Largest workspace moe_forward_static can serve (MOE_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 128 << 20
 
@@ -141,8 +149,13 @@ def moe_index_tiles_cap(T, k, E, block_m) -> int:
 
 def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
               stage_events=None, separate_act=False, smem_index=False,
-              single_weight_tile=False) -> moe_forward_opts:
+              single_weight_tile=False, num_shared_experts=0, shared_expert_weight=0.0,
+              ep_first_expert=0, ep_num_experts=0) -> moe_forward_opts:
     o = moe_forward_opts()
+    o.num_shared_experts = num_shared_experts
+    o.shared_expert_weight = shared_expert_weight
+    o.ep_first_expert = ep_first_expert
+    o.ep_num_experts = ep_num_experts
     o.disable_pdl = int(disable_pdl)
     o.separate_act = int(separate_act)
     o.smem_index = int(smem_index)
@@ -186,9 +199,28 @@ def moe_align(topk_ids: torch.Tensor, E: int, block_m: int, index: dict | None =
     return idx
 
 
-def layer_shape(x, w13, topk_ids, block_m=0, out_dtype=None) -> moe_shape:
+def moe_align_ex(topk_ids: torch.Tensor, E: int, block_m: int, num_shared_experts=0,
+                 ep_first_expert=0, ep_num_experts=0, index: dict | None = None,
+                 dev_status: torch.Tensor | None = None, stream=None) -> dict:
+    """moe_align with shared experts and / or the expert-parallel local range:
+    the index covers T*(k + n_shared) assignments over E + n_shared experts."""
+    T, k = topk_ids.shape
+    kk, Ei = k + num_shared_experts, E + num_shared_experts
+    idx = index if index is not None else alloc_index(T, kk, Ei, block_m, topk_ids.device)
+    ci = moe_index(*[_ptr(idx[n]) for n in ("counts", "offsets", "sorted_ids", "tile_expert",
+                                            "tiles", "inv_pos", "num_tiles")])
+    o = moe_align_opts(num_shared_experts, ep_first_expert, ep_num_experts)
+    _check(lib.moe_align_ex(_ptr(topk_ids), T, k, E, block_m, ctypes.byref(o), ctypes.byref(ci),
+                            _ptr(dev_status), _stream(stream)), "moe_align_ex")
+    return idx
+
+
+def layer_shape(x, w13, topk_ids, block_m=0, out_dtype=None, n_shared=0) -> moe_shape:
+    """Shape of a layer call; w13 holds the routed experts and then `n_shared`
+    shared ones, so the shape's E (routed) is w13's first extent - n_shared."""
     T, H = x.shape
     E, I2, _ = w13.shape
+    E -= n_shared
     fp8 = w13.dtype in (torch.uint8, torch.float8_e4m3fn)
     out_bf16 = (out_dtype or torch.bfloat16) == torch.bfloat16
     return make_shape(T, H, I2 // 2, E, topk_ids.shape[1], block_m, fp8, out_bf16)
@@ -199,7 +231,8 @@ def moe_forward(x, w13, w2, topk_ids, topk_w, *, scales=None, out=None, out_dtyp
     """The whole layer.  BF16: w13/w2 bf16.  FP8: w13/w2 uint8 e4m3 codes and
     scales = (w13_scale, w2_scale).  Returns `out` [T, H] (bf16 or fp32)."""
     shape = layer_shape(x, w13, topk_ids, block_m,
-                        out.dtype if out is not None else out_dtype)
+                        out.dtype if out is not None else out_dtype,
+                        opts.num_shared_experts if opts is not None else 0)
     if out is None:
         out = torch.empty(x.shape, dtype=torch.bfloat16 if shape.out_dtype else torch.float32,
                           device=x.device)
@@ -280,6 +313,8 @@ def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None) -> dic
     quantised x, Gate-Up partials, activation, Down partials)."""
     L = moe_plan(shape, opts)
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
+    ns = opts.num_shared_experts if opts is not None else 0
+    E, k = E + ns, k + ns   # experts and assignments per token of the index
     rc, tc = L.rows_cap, L.tiles_cap
     fp8 = shape.mode == MOE_FP8_W8A8
 

@@ -23,9 +23,26 @@
 #pragma once
 #include <cstdint>
 
+#include <climits>
+
+#include "internal.h"
 #include "ptx.cuh"
 
 namespace moe {
+
+// Index expert of assignment a under `m` (IdMap): a routed expert (0..E-1),
+// a shared one (E..), -1 for an invalid id, or kRemoteId for a valid id of
+// another rank's experts (dropped without a flag).
+constexpr int kRemoteId = INT_MIN;
+__device__ __forceinline__ int mapped_id(const int32_t* ids, int a, const IdMap& m) {
+  if (m.plain()) return ids[a];
+  const int t = a / m.kk, j = a - t * m.kk;
+  if (j >= m.k) return m.E + (j - m.k);
+  const int e = ids[static_cast<size_t>(t) * m.k + j];
+  if (m.Eg == 0) return (e >= 0 && e < m.E) ? e : -1;
+  if (e < 0 || e >= m.Eg) return -1;
+  return (e >= m.e0 && e < m.e0 + m.E) ? e - m.e0 : kRemoteId;
+}
 
 __device__ __forceinline__ int lanemask_lt() {
   int m;
@@ -60,10 +77,12 @@ struct IndexScratch {
   int32_t* offs;   // [E + 1]: padded offsets
   int32_t* tot;    // [E]: per-expert counts
   int32_t* flag;   // [1]: an invalid id was seen
+  int remote_ok;   // kRemoteId entries are another rank's: dropped, not flagged
   static __host__ __device__ constexpr size_t words(int nwarps, int E) {
     return static_cast<size_t>(nwarps) * E + (E + 1) + E + 1;
   }
-  __device__ void carve(int32_t* base, int nwarps, int E) {
+  __device__ void carve(int32_t* base, int nwarps, int E, int remote = 0) {
+    remote_ok = remote;
     cnt = base;
     offs = cnt + nwarps * E;
     tot = offs + E + 1;
@@ -114,7 +133,7 @@ __device__ __forceinline__ void index_count_and_scan(const int32_t* src, int tk,
     const bool in = a < end;
     const int e = in ? src[a] : -1;
     const bool valid = in && e >= 0 && e < E;
-    if (in && !valid) *sc.flag = 1;
+    if (in && !valid && !(sc.remote_ok && e == kRemoteId)) *sc.flag = 1;
     const unsigned grp = peer_mask(valid ? e : (1 << bits), bits);
     if (valid && lane == __ffs(grp) - 1) sc.cnt[warp * E + e] += __popc(grp);
     __syncwarp();

@@ -14,6 +14,23 @@ enum BSource : int {
   kDense = 2,   // rows 0..dense_rows-1 tiled by BN (router GEMM)
 };
 
+// How the layer's assignments map onto the experts of the index (and of the
+// weight tensors).  Token t has kk = k + n_shared assignments: slots j < k are
+// its routed ids topk_ids[t][j], slots k..kk-1 the shared experts E..E+n_shared-1,
+// which every token selects (SGLang's shared-expert fusion: the shared expert
+// becomes one more expert of the grouped GEMM).  Expert parallelism: the E
+// routed experts held here are the global ids [e0, e0 + E) of Eg; a routed id
+// of another rank's range is dropped without a flag (that rank computes it);
+// ids outside [0, Eg) (outside [0, E) without expert parallelism) are invalid.
+struct IdMap {
+  int k;    // routed slots per token (columns of topk_ids)
+  int kk;   // assignments per token: k + shared experts
+  int E;    // routed experts held here
+  int e0;   // global id of the first of them
+  int Eg;   // routed experts in all; 0: no expert parallelism
+  __host__ __device__ bool plain() const { return kk == k && Eg == 0; }
+};
+
 struct GemmParams {
   int M;             // output columns: 2I (Gate-Up), H (Down), 2E (router)
   int K;             // reduction length in elements
@@ -41,7 +58,8 @@ struct GemmParams {
   // top-k ids in its prologue instead of reading tiles / sorted_ids.
   int smem_index;
   const int32_t* topk_ids;   // [T][topk], an input of the layer call
-  int T, E, tiles_cap;
+  int T, E, tiles_cap;       // E: experts of the index (routed here + shared)
+  IdMap idmap;               // topk_ids -> index experts (shared-memory index)
   int write_index;           // CTA 0 also writes the index to `index_out` and the
   struct {                   // expert-id status bit to dev_status
     int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
@@ -72,15 +90,17 @@ cudaError_t launch_gemm_fp8(int bn, int bsrc, int grid, cudaStream_t st, bool pd
 struct IndexPtrs {
   int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
 };
+// k and E below count assignments per token and experts of the index (map.kk
+// and map.E + shared experts); `map` turns topk_ids into index experts.
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                          const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st,
-                         bool pdl);
+                         bool pdl, const IdMap& map);
 // The same index built by three kernels over chunks of assignments (count,
 // scan, scatter); `scratch` holds align_split_scratch_words(T, k, E) ints.
 size_t align_split_scratch_words(int T, int k, int E);
 cudaError_t launch_align_split(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                                const IndexPtrs& idx, int32_t* scratch, int32_t* dev_status,
-                               cudaStream_t st, bool pdl);
+                               cudaStream_t st, bool pdl, const IdMap& map);
 cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* inv_pos,
                            uint8_t* xq, float* xs, float* xs_rows, int rows_cap, cudaStream_t st,
                            bool pdl);
@@ -88,9 +108,12 @@ cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* in
 cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
                        const int32_t* sorted_ids, int sentinel, void* A, float* As,
                        cudaStream_t st, bool pdl);
+// k assignments per token, the first k_routed weighted by topk_w[t][j], the
+// others (shared experts) by w_shared.
 cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H,
                            const int32_t* inv_pos, const float* topk_w, int T, int k,
-                           void* out, int out_bf16, cudaStream_t st, bool pdl);
+                           int k_routed, float w_shared, void* out, int out_bf16,
+                           cudaStream_t st, bool pdl);
 cudaError_t launch_router_prepare(const float* wr, int E, int H, void* hi_lo,
                                   cudaStream_t st);
 cudaError_t launch_router_topk(const float* P, int splits, int rows_cap, int T, int E,

@@ -17,10 +17,10 @@ constexpr int kAlignMaxStagedIds = 32768;  // ids staged in shared memory up to 
 
 __global__ void __launch_bounds__(kAlignThreads)
     moe_align_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int tiles_cap,
-                     IndexPtrs idx, int32_t* dev_status, int stage_ids) {
+                     IndexPtrs idx, int32_t* dev_status, int stage_ids, IdMap map) {
   extern __shared__ int32_t sm[];
   IndexScratch sc;
-  sc.carve(sm, kAlignWarps, E);
+  sc.carve(sm, kAlignWarps, E, map.Eg != 0);
   // [T*k] staged ids (optional), 16-byte aligned for vector stores
   int32_t* sids = sm + ((IndexScratch::words(kAlignWarps, E) + 3) & ~static_cast<size_t>(3));
 
@@ -31,7 +31,10 @@ __global__ void __launch_bounds__(kAlignThreads)
   pdl_launch_dependents();
 
   if (tid == 0 && dev_status) *dev_status = 0;
-  if (stage_ids) {
+  if (stage_ids && !map.plain()) {
+    // shared experts / expert parallelism: stage the index experts
+    for (int i = tid; i < tk; i += kAlignThreads) sids[i] = mapped_id(ids, i, map);
+  } else if (stage_ids) {
     // 16-byte loads, several in flight per thread (one dependent load per
     // iteration made this loop the kernel's cost at 32K assignments)
     const int n4 = (reinterpret_cast<uintptr_t>(ids) & 15) ? 0 : tk / 4;
@@ -65,9 +68,11 @@ __global__ void __launch_bounds__(kAlignThreads)
 }
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
-                         const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st, bool pdl) {
+                         const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st, bool pdl,
+                         const IdMap& map) {
   const int tk = T * k;
   const int stage_ids = tk <= kAlignMaxStagedIds ? 1 : 0;
+  if (!stage_ids && !map.plain()) return cudaErrorInvalidValue;   // mapped ids are staged
   const size_t smem =
       sizeof(int32_t) * (((IndexScratch::words(kAlignWarps, E) + 3) & ~static_cast<size_t>(3)) +
                          (stage_ids ? tk : 0));
@@ -82,7 +87,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int ti
     configured[dev] = 1;
   }
   return launch_kernel(moe_align_kernel, dim3(1), dim3(kAlignThreads), smem, st, pdl, ids, T, k, E,
-                       bm, tiles_cap, idx, dev_status, stage_ids);
+                       bm, tiles_cap, idx, dev_status, stage_ids, map);
 }
 
 // ---------------------------------------------------------------- split build
@@ -103,23 +108,27 @@ __host__ __device__ inline size_t chunk_smem_words(int E) {
   return ((IndexScratch::words(kSplitWarps, E) + 3) & ~static_cast<size_t>(3)) + kChunk;
 }
 
-__device__ __forceinline__ int stage_chunk(const int32_t* ids, int tk, int32_t* chunk) {
+__device__ __forceinline__ int stage_chunk(const int32_t* ids, int tk, int32_t* chunk,
+                                           const IdMap& map) {
   const int a0 = blockIdx.x * kChunk;
   const int n = min(kChunk, tk - a0);
-  for (int i = threadIdx.x; i < n; i += kSplitThreads) chunk[i] = __ldg(ids + a0 + i);
+  if (map.plain())
+    for (int i = threadIdx.x; i < n; i += kSplitThreads) chunk[i] = __ldg(ids + a0 + i);
+  else
+    for (int i = threadIdx.x; i < n; i += kSplitThreads) chunk[i] = mapped_id(ids, a0 + i, map);
   return n;
 }
 
 __global__ void __launch_bounds__(kSplitThreads)
     moe_align_count_kernel(const int32_t* __restrict__ ids, int tk, int E, int bm,
-                           int32_t* __restrict__ hist, int32_t* __restrict__ flags) {
+                           int32_t* __restrict__ hist, int32_t* __restrict__ flags, IdMap map) {
   extern __shared__ int32_t sm[];
   IndexScratch sc;
-  sc.carve(sm, kSplitWarps, E);
+  sc.carve(sm, kSplitWarps, E, map.Eg != 0);
   int32_t* chunk = sm + (chunk_smem_words(E) - kChunk);
   pdl_wait();
   pdl_launch_dependents();
-  const int n = stage_chunk(ids, tk, chunk);
+  const int n = stage_chunk(ids, tk, chunk, map);
   index_count_and_scan(chunk, n, E, bm, sc);
   for (int e = threadIdx.x; e < E; e += kSplitThreads)
     hist[static_cast<size_t>(blockIdx.x) * E + e] = sc.tot[e];
@@ -165,14 +174,14 @@ __global__ void __launch_bounds__(kAlignThreads)
 
 __global__ void __launch_bounds__(kSplitThreads)
     moe_align_scatter_kernel(const int32_t* __restrict__ ids, int tk, int E, int bm,
-                             const int32_t* __restrict__ base, IndexPtrs idx) {
+                             const int32_t* __restrict__ base, IndexPtrs idx, IdMap map) {
   extern __shared__ int32_t sm[];
   IndexScratch sc;
-  sc.carve(sm, kSplitWarps, E);
+  sc.carve(sm, kSplitWarps, E, map.Eg != 0);
   int32_t* chunk = sm + (chunk_smem_words(E) - kChunk);
   pdl_wait();
   pdl_launch_dependents();
-  const int n = stage_chunk(ids, tk, chunk);
+  const int n = stage_chunk(ids, tk, chunk, map);
   index_count_and_scan(chunk, n, E, bm, sc);   // in-chunk per-warp bases
   for (int e = threadIdx.x; e < E; e += kSplitThreads)
     sc.offs[e] = idx.offsets[e] + base[static_cast<size_t>(blockIdx.x) * E + e];
@@ -194,21 +203,21 @@ size_t align_split_scratch_words(int T, int k, int E) {
 
 cudaError_t launch_align_split(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                                const IndexPtrs& idx, int32_t* scratch, int32_t* dev_status,
-                               cudaStream_t st, bool pdl) {
+                               cudaStream_t st, bool pdl, const IdMap& map) {
   const int tk = T * k;
   const int nb = (tk + kChunk - 1) / kChunk;
   int32_t* hist = scratch;
   int32_t* flags = scratch + static_cast<size_t>(nb) * E;
   const size_t chunk_smem = 4 * chunk_smem_words(E);
   cudaError_t e = launch_kernel(moe_align_count_kernel, dim3(nb), dim3(kSplitThreads), chunk_smem,
-                                st, pdl, ids, tk, E, bm, hist, flags);
+                                st, pdl, ids, tk, E, bm, hist, flags, map);
   if (e != cudaSuccess) return e;
   e = launch_kernel(moe_align_scan_kernel, dim3(1), dim3(kAlignThreads),
                     4 * IndexScratch::words(1, E), st, true, hist,
                     static_cast<const int32_t*>(flags), nb, tk, E, bm, tiles_cap, idx, dev_status);
   if (e != cudaSuccess) return e;
   return launch_kernel(moe_align_scatter_kernel, dim3(nb), dim3(kSplitThreads), chunk_smem, st,
-                       true, ids, tk, E, bm, static_cast<const int32_t*>(hist), idx);
+                       true, ids, tk, E, bm, static_cast<const int32_t*>(hist), idx, map);
 }
 
 }  // namespace moe

@@ -125,8 +125,8 @@ struct SmemIndex {
   __host__ __device__ static size_t bytes(int nwarps, int E, int tk, int rows_cap, int tiles_cap) {
     return 4 * words_before_tiles(nwarps, E, tk, rows_cap) + 16 * static_cast<size_t>(tiles_cap);
   }
-  __device__ void carve(int32_t* base, int nwarps, int E, int tk, int rows_cap) {
-    sc.carve(base, nwarps, E);
+  __device__ void carve(int32_t* base, int nwarps, int E, int tk, int rows_cap, int remote) {
+    sc.carve(base, nwarps, E, remote);
     ids = base + IndexScratch::words(nwarps, E);
     rows = ids + tk;
     tiles = reinterpret_cast<int4*>(base + words_before_tiles(nwarps, E, tk, rows_cap));
@@ -249,8 +249,9 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
   if (smem_idx) {
     // The top-k ids are an input of the call: complete before its first
     // kernel started, so they are read without waiting on the predecessor.
-    si.carve(reinterpret_cast<int32_t*>(smem + S::kOffIdx), S::kWarps, p.E, tk, p.rows_cap);
-    for (int i = threadIdx.x; i < tk; i += S::kThreads) si.ids[i] = __ldg(p.topk_ids + i);
+    si.carve(reinterpret_cast<int32_t*>(smem + S::kOffIdx), S::kWarps, p.E, tk, p.rows_cap,
+             p.idmap.Eg != 0);
+    for (int i = threadIdx.x; i < tk; i += S::kThreads) si.ids[i] = mapped_id(p.topk_ids, i, p.idmap);
     index_count_and_scan(si.ids, tk, p.E, BN, si.sc);
     index_scatter(si.ids, tk, p.E, si.sc, [&](int pos, int a) { si.rows[pos] = a; },
                   [](int) {});

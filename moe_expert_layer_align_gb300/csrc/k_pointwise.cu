@@ -151,7 +151,8 @@ constexpr int kCombineBatch = 8;   // assignments whose rows are loaded together
 __global__ void __launch_bounds__(128)
     moe_combine_kernel(const float* __restrict__ Y, int splits, int rows_cap, int H,
                        const int32_t* __restrict__ inv_pos, const float* __restrict__ topk_w,
-                       int T, int k, void* __restrict__ out, int out_bf16) {
+                       int T, int k, int k_routed, float w_shared, void* __restrict__ out,
+                       int out_bf16) {
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
@@ -170,7 +171,9 @@ __global__ void __launch_bounds__(128)
       const int j = j0 + b;
       pos[b] = j < k ? __ldg(inv_pos + static_cast<size_t>(t) * k + j) : -1;
       if (pos[b] >= rows_cap) pos[b] = -1;   // only rows of the index are read
-      w[b] = j < k ? __ldg(topk_w + static_cast<size_t>(t) * k + j) : 0.f;
+      // routed slots weigh topk_w[t][j]; the shared experts' slots w_shared
+      w[b] = j < k_routed ? __ldg(topk_w + static_cast<size_t>(t) * k_routed + j)
+                          : (j < k ? w_shared : 0.f);
     }
 #pragma unroll
     for (int b = 0; b < kCombineBatch; ++b)
@@ -209,11 +212,12 @@ __global__ void __launch_bounds__(128)
 }
 
 cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H, const int32_t* inv_pos,
-                           const float* topk_w, int T, int k, void* out, int out_bf16,
+                           const float* topk_w, int T, int k,
+                           int k_routed, float w_shared, void* out, int out_bf16,
                            cudaStream_t st, bool pdl) {
   const dim3 grid(T, (H / 4 + 127) / 128);
   return launch_kernel(moe_combine_kernel, grid, dim3(128), 0, st, pdl, Y, splits, rows_cap, H,
-                       inv_pos, topk_w, T, k, out, out_bf16);
+                       inv_pos, topk_w, T, k, k_routed, w_shared, out, out_bf16);
 }
 
 // ---------------------------------------------------------------- router

@@ -27,7 +27,11 @@ constexpr int kSmemIndexMaxAssignments = 4096;
 constexpr int kSplitIndexMinAssignments = 2048;
 
 struct Plan {
+  // k, E: assignments per token and experts of the index and the weights
+  // (routed + shared); the IdMap maps topk_ids onto them.
   int T, H, I, E, k, bm, fp8, out_bf16;
+  IdMap map;
+  float w_shared;
   int tiles_cap, rows_cap;
   int s1, kts1, kt1, mt1;  // Gate-Up: splits, k-tiles per split, k-tiles, weight tiles
   int s2, kts2, kt2, mt2;  // Down
@@ -133,15 +137,36 @@ moe_status check_shape(const moe_shape* s) {
   return MOE_OK;
 }
 
+// Shared experts and the expert-parallel range (moe_forward_opts /
+// moe_align_opts) as an IdMap; MOE_ERR_SHAPE on inconsistent values.
+moe_status make_idmap(int k, int E, int n_shared, int e0, int Eg, IdMap* m) {
+  if (n_shared < 0 || n_shared > 8 || E + n_shared > 512) return MOE_ERR_SHAPE;
+  if (Eg < 0 || (Eg > 0 && (e0 < 0 || e0 + E > Eg)) || (Eg == 0 && e0 != 0)) return MOE_ERR_SHAPE;
+  m->k = k;
+  m->kk = k + n_shared;
+  m->E = E;
+  m->e0 = Eg > 0 ? e0 : 0;
+  m->Eg = Eg;
+  return MOE_OK;
+}
+
 moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
   moe_status st = check_shape(s);
   if (st != MOE_OK) return st;
   std::memset(p, 0, sizeof(*p));
-  p->T = s->T, p->H = s->H, p->I = s->I, p->E = s->E, p->k = s->k;
+  const int n_shared = o ? o->num_shared_experts : 0;
+  st = make_idmap(s->k, s->E, n_shared, o ? o->ep_first_expert : 0, o ? o->ep_num_experts : 0,
+                  &p->map);
+  if (st != MOE_OK) return st;
+  if (static_cast<int64_t>(s->T) * p->map.kk >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
+  p->w_shared = (o && o->shared_expert_weight != 0.f) ? o->shared_expert_weight : 1.0f;
+  p->T = s->T, p->H = s->H, p->I = s->I;
+  p->E = s->E + n_shared;   // experts in the weights and the index
+  p->k = p->map.kk;         // assignments per token
   p->fp8 = s->mode == MOE_FP8_W8A8;
   p->out_bf16 = s->out_dtype == MOE_OUT_BF16;
-  p->bm = s->block_m ? s->block_m : auto_bm(s->T, s->k, s->E, p->fp8);
-  const int64_t tc = tiles_cap_of(s->T, s->k, s->E, p->bm);
+  p->bm = s->block_m ? s->block_m : auto_bm(p->T, p->k, p->E, p->fp8);
+  const int64_t tc = tiles_cap_of(p->T, p->k, p->E, p->bm);
   if (tc * p->bm >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
   p->tiles_cap = static_cast<int>(tc);
   p->rows_cap = static_cast<int>(tc * p->bm);
@@ -154,7 +179,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
   // weight tile per unit: pair two weight tiles per unit there.
   p->me1 = (!p->fp8 && p->bm >= 128 && p->mt1 % 2 == 0 && !(o && o->single_weight_tile)) ? 2 : 1;
   p->me2 = (!p->fp8 && p->bm >= 128 && p->mt2 % 2 == 0 && !(o && o->single_weight_tile)) ? 2 : 1;
-  const int est = est_tiles(s->T, s->k, s->E, p->bm, p->tiles_cap);
+  const int est = est_tiles(p->T, p->k, p->E, p->bm, p->tiles_cap);
   choose_split(p->mt1 / p->me1, p->kt1, est, p->bm, &p->s1, &p->kts1);
   choose_split(p->mt2 / p->me2, p->kt2, est, p->bm, &p->s2, &p->kts2);
   if (o && o->split_gateup > 0) {
@@ -170,30 +195,30 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
   // top-k ids in shared memory when it fits next to the pipeline (no index
   // kernel).  Measured no faster than the index kernel, so not the default.
   {
-    const int tk = s->T * s->k;
+    const int tk = p->T * p->k;
     bool fits = tk <= kSmemIndexMaxAssignments && o && o->smem_index;
     for (int bsrc : {static_cast<int>(kGather), static_cast<int>(kDirect)}) {
       const size_t need = gemm_smem_bytes(p->fp8, p->bm, bsrc) +
-                          gemm_index_smem_bytes(gemm_warps(p->fp8, p->bm, bsrc), s->E, tk, p->rows_cap,
+                          gemm_index_smem_bytes(gemm_warps(p->fp8, p->bm, bsrc), p->E, tk, p->rows_cap,
                                                 p->tiles_cap);
       if (need > kMaxGemmSmem) fits = false;
     }
     p->smem_index = fits;
   }
   // many assignments: build the index over chunks, one CTA each
-  p->split_index = !p->smem_index && static_cast<int64_t>(s->T) * s->k > kSplitIndexMinAssignments;
+  p->split_index = !p->smem_index && static_cast<int64_t>(p->T) * p->k > kSplitIndexMinAssignments;
   // workspace layout
-  const size_t tk = static_cast<size_t>(s->T) * s->k;
+  const size_t tk = static_cast<size_t>(p->T) * p->k;
   const size_t rc = p->rows_cap;
   const size_t sizes[kNumOff] = {
-      4u * s->E,
-      4u * (s->E + 1),
+      4u * p->E,
+      4u * (p->E + 1),
       4 * rc,
       4u * p->tiles_cap,
       16u * p->tiles_cap,
       4 * tk,
       4,
-      p->split_index ? 4 * align_split_scratch_words(s->T, s->k, s->E) : 0,
+      p->split_index ? 4 * align_split_scratch_words(p->T, p->k, p->E) : 0,
       p->fp8 ? static_cast<size_t>(s->T) * s->H : 0,
       p->fp8 ? 4 * static_cast<size_t>(s->T) * (s->H / 128) : 0,
       p->fp8 ? 4 * rc * (s->H / 128) : 0,
@@ -399,8 +424,34 @@ moe_status moe_align(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E, i
   IndexPtrs ip{idx->counts, idx->offsets, idx->sorted_ids, idx->tile_expert,
                idx->tiles,  idx->inv_pos,  idx->num_tiles};
   const int tc = static_cast<int>(tiles_cap_of(T, k, E, block_m));
+  IdMap plain{k, k, E, 0, 0};
   return cuda_status(launch_align(topk_ids, T, k, E, block_m, tc, ip, dev_status,
-                                  static_cast<cudaStream_t>(stream), false));
+                                  static_cast<cudaStream_t>(stream), false, plain));
+}
+
+moe_status moe_align_ex(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E, int32_t block_m,
+                        const moe_align_opts* opts, const moe_index* idx, int32_t* dev_status,
+                        void* stream) {
+  if (!opts) return moe_align(topk_ids, T, k, E, block_m, idx, dev_status, stream);
+  if (!topk_ids || !idx || !idx->counts || !idx->offsets || !idx->sorted_ids ||
+      !idx->tile_expert || !idx->tiles || !idx->inv_pos || !idx->num_tiles)
+    return MOE_ERR_ARG;
+  if (T < 1 || k < 1 || E < 1 || E > 512 || k > E || !valid_bm(block_m, 0))
+    return MOE_ERR_SHAPE;
+  IdMap m;
+  moe_status st = make_idmap(k, E, opts->num_shared_experts, opts->ep_first_expert,
+                             opts->ep_num_experts, &m);
+  if (st != MOE_OK) return st;
+  const int64_t tk = static_cast<int64_t>(T) * m.kk;
+  if (!m.plain() && tk > 32768) return MOE_ERR_SHAPE;   // mapped ids are staged on chip
+  if (tk >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
+  if (!aligned(idx->tiles, 16)) return MOE_ERR_ALIGN;
+  IndexPtrs ip{idx->counts, idx->offsets, idx->sorted_ids, idx->tile_expert,
+               idx->tiles,  idx->inv_pos,  idx->num_tiles};
+  const int Ei = E + opts->num_shared_experts;
+  const int tc = static_cast<int>(tiles_cap_of(T, m.kk, Ei, block_m));
+  return cuda_status(launch_align(topk_ids, T, m.kk, Ei, block_m, tc, ip, dev_status,
+                                  static_cast<cudaStream_t>(stream), false, m));
 }
 
 moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13, const void* w2,
@@ -460,10 +511,12 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   record(opts, 0, s);
   if (p.split_index) {
     e = launch_align_split(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip,
-                           reinterpret_cast<int32_t*>(at(kOffIdxScratch)), dev_status, s, chain());
+                           reinterpret_cast<int32_t*>(at(kOffIdxScratch)), dev_status, s, chain(),
+                           p.map);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else if (!p.smem_index) {
-    e = launch_align(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s, chain());
+    e = launch_align(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s, chain(),
+                     p.map);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
 
@@ -499,6 +552,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g1.topk_ids = topk_ids;
   g1.T = p.T;
   g1.E = p.E;
+  g1.idmap = p.map;
   g1.tiles_cap = p.tiles_cap;
   g1.write_index = p.smem_index;
   g1.index_out = {ip.counts, ip.offsets, ip.sorted_ids, ip.tile_expert, ip.tiles, ip.inv_pos,
@@ -538,6 +592,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g2.topk_ids = topk_ids;
   g2.T = p.T;
   g2.E = p.E;
+  g2.idmap = p.map;
   g2.tiles_cap = p.tiles_cap;
   g2.early_weights = 1;   // the index is complete before this grid launches
   g2.out = Y;
@@ -549,7 +604,8 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   record(opts, 5, s);
-  e = launch_combine(Y, p.s2, p.rows_cap, p.H, ip.inv_pos, topk_w, p.T, p.k, out, p.out_bf16, s,
+  e = launch_combine(Y, p.s2, p.rows_cap, p.H, ip.inv_pos, topk_w, p.T, p.k, p.map.k, p.w_shared,
+                     out, p.out_bf16, s,
                      pdl);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(opts, 6, s);
@@ -572,7 +628,8 @@ moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t rows_cap,
     return MOE_ERR_SHAPE;
   if (!aligned(y, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
   return cuda_status(launch_combine(y, splits, rows_cap, shape->H, inv_pos, topk_w, shape->T,
-                                    shape->k, out, shape->out_dtype == MOE_OUT_BF16,
+                                    shape->k, shape->k, 1.0f, out,
+                                    shape->out_dtype == MOE_OUT_BF16,
                                     static_cast<cudaStream_t>(stream), false));
 }
 

@@ -240,6 +240,34 @@ def moe_fp8(xq, xs, w13q, w13s, w2q, w2s, topk_ids, topk_w, sel=None, return_act
     return out
 
 
+# ------------------------------------------------------------------ variants
+# Two variants of the layer that the pages' serving stack uses, written as
+# what they are: the plain layer applied to re-mapped routing.
+
+def shared_routing(topk_ids, topk_w, E: int, n_shared: int, weight: float = 1.0):
+    """Shared-expert fusion (SGLang's MoE kernels for DeepSeek-V3 / GLM4-MoE /
+    Llama 4): the shared experts E..E+n_shared-1 are extra experts that every
+    token selects with `weight`.  Returns the routing of the plain layer over
+    E + n_shared experts: topk_ids[T][k + n_shared], topk_w likewise."""
+    ids = _c(topk_ids, np.int32)
+    w = _c(topk_w, np.float32)
+    T = ids.shape[0]
+    sid = np.broadcast_to(np.arange(E, E + n_shared, dtype=np.int32), (T, n_shared))
+    sw = np.full((T, n_shared), weight, np.float32)
+    return np.concatenate([ids, sid], 1), np.concatenate([w, sw], 1)
+
+
+def ep_local_ids(topk_ids, e0: int, E_local: int):
+    """Expert parallelism, one rank's part (SGLang MoE tuning guide, section 1:
+    EP places whole experts on ranks): the rank holds the global experts
+    [e0, e0 + E_local) as its local 0..E_local-1; an assignment to any other
+    expert is not this rank's (-1: dropped, contributes 0).  The rank's output
+    is its partial sum; the ranks' outputs add up to the full layer."""
+    ids = _c(topk_ids, np.int32)
+    loc = ids - e0
+    return np.where((ids >= e0) & (ids < e0 + E_local), loc, -1).astype(np.int32)
+
+
 # ------------------------------------------------------------------ router
 
 def router_split(wr):

@@ -121,3 +121,36 @@ def test_router_host_checks():
                                  1 << 30, None) == moe.MOE_ERR_ARG
     assert B.lib.moe_router_topk(g[0], g[1], 64, 2048, 128, 8, 0, 1.0, g[2], g[3], g[4], g[5],
                                  16, None) == moe.MOE_ERR_WORKSPACE
+
+
+def test_shared_expert_and_ep_options_are_checked_and_planned():
+    s = moe.make_shape(64, 2048, 768, 128, 8)
+    L0 = moe.moe_plan(s)
+    L = moe.moe_plan(s, moe.make_opts(num_shared_experts=1))
+    assert L.tiles_cap == moe.moe_index_tiles_cap(64, 9, 129, L.block_m)
+    assert L.total_bytes >= L0.total_bytes
+    Le = moe.moe_plan(moe.make_shape(64, 2048, 768, 32, 8), moe.make_opts(ep_first_expert=32,
+                                                                          ep_num_experts=128))
+    assert Le.tiles_cap == moe.moe_index_tiles_cap(64, 8, 32, Le.block_m)
+    bad = [moe.make_opts(num_shared_experts=9), moe.make_opts(num_shared_experts=-1),
+           moe.make_opts(ep_first_expert=100, ep_num_experts=128),     # 100 + 128 > 128
+           moe.make_opts(ep_first_expert=3)]                           # a range without EP
+    for o in bad:
+        assert moe.moe_workspace_bytes(s, o) == 0
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_plan(s, o)
+        assert ei.value.status == moe.MOE_ERR_SHAPE
+
+
+def test_align_ex_host_checks():
+    g = [0x100000 * (i + 1) for i in range(7)]
+    idx = B.moe_index(*g)
+    o = B.moe_align_opts(1, 0, 0)
+    # mapped ids are staged on chip: at most 32768 assignments
+    assert B.lib.moe_align_ex(g[0], 8192, 4, 8, 16, ctypes.byref(o), ctypes.byref(idx), None,
+                              None) == moe.MOE_ERR_SHAPE
+    o = B.moe_align_opts(0, 6, 8)                                    # 6 + 8 > 8
+    assert B.lib.moe_align_ex(g[0], 8, 2, 8, 16, ctypes.byref(o), ctypes.byref(idx), None,
+                              None) == moe.MOE_ERR_SHAPE
+    assert B.lib.moe_align_ex(None, 8, 2, 8, 16, ctypes.byref(o), ctypes.byref(idx), None,
+                              None) == moe.MOE_ERR_ARG
