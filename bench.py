@@ -238,11 +238,22 @@ class Layer:
         out_dtype = torch.float32 if wl.out == "f32" else torch.bfloat16
         shape = moe.layer_shape(wl.x, self.w13, self.ids, 0, out_dtype)
         self.shape = shape
-        self.ws = torch.empty(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device=dev)
+        if self.hi_lo is not None:
+            self.plan = moe.moe_plan_routed(shape, opts)
+            ws_bytes = moe.moe_routed_workspace_bytes(shape, opts)
+        else:
+            self.plan = moe.moe_plan(shape, opts)
+            ws_bytes = moe.moe_workspace_bytes(shape, opts)
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         self.out = torch.empty(wl.x.shape, dtype=out_dtype, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.graph = None
-        self.kernels_per_step = 5 + (1 if self.fp8 else 0) + (2 if self.hi_lo is not None else 0)
+        # launches per step: [router GEMM + (fused routing | top-k, align[, x-quant])]
+        # or align[, x-quant]; Gate-Up; [act]; Down; combine
+        L = self.plan
+        front = (2 if L.route_fused else 3 + (1 if self.fp8 else 0)) if self.hi_lo is not None \
+            else (0 if L.smem_index else 1) + (1 if self.fp8 else 0)
+        self.kernels_per_step = front + 3 + (0 if L.fused_act else 1)
         if graph:
             with torch.cuda.stream(stream):
                 self.call()                       # warm the launch path before capture
@@ -261,7 +272,14 @@ class Layer:
     def call(self):
         wl = self.wl
         if self.hi_lo is not None:
-            self.route()
+            # router in the path: one chain (router GEMM, then routing + index)
+            self.moe.moe_forward_routed(wl.x, self.hi_lo, wl.k, self.w13, self.w2,
+                                        score_fn=wl.router_fn, scale=wl.router_scale,
+                                        scales=self.scales, out=self.out, scores=self.scores,
+                                        topk_ids=self.ids, topk_w=self.w, workspace=self.ws,
+                                        dev_status=self.status, stream=self.stream,
+                                        opts=self.opts)
+            return
         self.moe.moe_forward(wl.x, self.w13, self.w2, self.ids, self.w, scales=self.scales,
                              out=self.out, workspace=self.ws, dev_status=self.status,
                              stream=self.stream, opts=self.opts)
@@ -298,22 +316,22 @@ def time_layer(layer, stream, flush, steps, warmup):
 def stage_times(wl, stream, flush, steps):
     """Per-stage device time (us) from events recorded between the stages,
     captured with the layer in a CUDA graph (recording events between stages
-    serialises them: PDL overlap is lost in this pass).  The in-path router is
-    timed as its own graph."""
+    serialises them: PDL overlap is lost in this pass).  With the router in
+    the path, "router" is its GEMM and "align" the fused routing kernel (top-k,
+    x-quant and index) where the plan fuses them."""
     import moe_expert_layer_align_gb300 as moe
     n = len(moe.STAGES) + 1
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-    for ev in evs:                  # torch creates the CUDA event on first record
+    ev_router = torch.cuda.Event(enable_timing=True)
+    for ev in evs + [ev_router]:    # torch creates the CUDA event on first record
         ev.record(stream)
-    layer = Layer(wl, stream, opts=moe.make_opts(stage_events=evs), graph=True)
+    routed = wl.wr is not None
+    opts = moe.make_opts(stage_events=evs)
+    if routed:
+        opts.stage_events[7] = ev_router.cuda_event
+    layer = Layer(wl, stream, opts=opts, graph=True)
     acc = np.zeros(n - 1)
     router = 0.0
-    rgraph = None
-    if layer.hi_lo is not None:
-        rgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(rgraph, stream=stream):
-            layer.route()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(steps):
         with torch.cuda.stream(stream):
             flush.zero_()
@@ -321,16 +339,10 @@ def stage_times(wl, stream, flush, steps):
         stream.synchronize()
         for i in range(n - 1):
             acc[i] += evs[i].elapsed_time(evs[i + 1]) * 1e3
-        if rgraph is not None:
-            with torch.cuda.stream(stream):
-                flush.zero_()
-                s0.record(stream)
-                rgraph.replay()
-                s1.record(stream)
-            stream.synchronize()
-            router += s0.elapsed_time(s1) * 1e3
+        if routed:
+            router += ev_router.elapsed_time(evs[0]) * 1e3
     out = dict(zip(moe.STAGES, (acc / steps).tolist()))
-    if rgraph is not None:
+    if routed:
         out = {"router": router / steps, **out}
     return out
 

@@ -142,6 +142,12 @@ typedef struct {
    * and flagged).  The output is this rank's partial sum.  0 = off. */
   int32_t ep_first_expert;
   int32_t ep_num_experts;
+  /* moe_forward_routed: 1 = run the router's top-k, the FP8 quantisation of x
+   * and the routing index as one grid (up to 2048 assignments) instead of
+   * three kernels.  Bit-identical results; measured slower on the Zipf-routed
+   * Qwen3-shaped FP8 layer at T=64 (its last CTA builds the index alone after
+   * every token's top-k), so off by default. */
+  int32_t fuse_routing;
 } moe_forward_opts;
 
 /* Options of moe_align_ex: the same shared-expert and expert-parallel mapping
@@ -162,6 +168,7 @@ typedef struct {
   int32_t smem_index;  /* 1: GEMM CTAs rebuild the index in shared memory; the
                           Gate-Up writes it out (no separate index kernel) */
   int32_t weight_tiles_per_unit;  /* Gate-Up | Down << 8 (1 or 2 each) */
+  int32_t route_fused;  /* moe_forward_routed: router top-k, x-quant and index in one grid */
   size_t off_counts, off_offsets, off_sorted_ids, off_tile_expert, off_tiles,
       off_inv_pos, off_num_tiles;
   size_t off_index_scratch; /* per-chunk histograms of the split index build */
@@ -172,6 +179,8 @@ typedef struct {
   size_t off_a;    /* activation: bf16 [rows_cap][I] or e4m3 [rows_cap][I]  */
   size_t off_as;   /* FP8: fp32 act scales   [rows_cap][I/128]              */
   size_t off_y;    /* fp32 Down partials     [S2][rows_cap][H] (sorted rows)*/
+  size_t off_router;        /* moe_forward_routed: router GEMM partial sums   */
+  size_t off_route_counter; /* moe_forward_routed: ticket counter (4 bytes)   */
   size_t total_bytes;
 } moe_workspace_layout;
 
@@ -251,6 +260,28 @@ MOE_API moe_status moe_forward_ex(const moe_shape* shape, const void* x,
 MOE_API moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t rows_cap,
                        const float* y, const int32_t* inv_pos,
                        const float* topk_w, void* out, void* stream);
+
+/* The layer with its router in the path (HPC-Ops × SGLang, section "Router
+ * GEMM" feeding section "MoE"): the two-bf16 router GEMM over hi_lo (from
+ * moe_router_prepare) scores x, its top-k becomes the layer's routing, and the
+ * layer runs as in moe_forward — one chain of launches on `stream`.  With
+ * opts->fuse_routing and up to 2048 assignments the router's top-k, the FP8
+ * quantisation of x and the routing index run as one grid (whose last CTA to
+ * finish builds the index) instead of three launches.  Outputs besides `out`: scores fp32 [T][E],
+ * topk_ids int32 [T][k], topk_w fp32 [T][k] (caller-owned).  score_fn and
+ * scale as in moe_router_topk; router shapes as moe_router_workspace_bytes
+ * accepts (E a multiple of 64, k <= 32).  Not combined with shared experts,
+ * expert parallelism or the shared-memory index (MOE_ERR_SHAPE).  The
+ * workspace is sized by moe_routed_workspace_bytes / moe_plan_routed (the
+ * router's partial sums and a 4-byte ticket counter are added). */
+MOE_API moe_status moe_plan_routed(const moe_shape* shape, const moe_forward_opts* opts,
+                           moe_workspace_layout* layout);
+MOE_API size_t moe_routed_workspace_bytes(const moe_shape* shape, const moe_forward_opts* opts);
+MOE_API moe_status moe_forward_routed(const moe_shape* shape, const void* x, const void* hi_lo,
+                              int32_t score_fn, float scale, const void* w13, const void* w2,
+                              const moe_scales* scales, float* scores, int32_t* topk_ids,
+                              float* topk_w, void* out, void* workspace, size_t ws_bytes,
+                              int32_t* dev_status, void* stream, const moe_forward_opts* opts);
 
 /* Router weight preparation ("a precision-aware BF16 formulation", HPC-Ops ×
  * SGLang, section Router GEMM): from fp32 wr[E][H] writes bf16

@@ -47,7 +47,7 @@ class moe_forward_opts(ctypes.Structure):
                 ("grid_ctas", _i32), ("stage_events", _vp * 8), ("separate_act", _i32),
                 ("smem_index", _i32), ("single_weight_tile", _i32),
                 ("num_shared_experts", _i32), ("shared_expert_weight", ctypes.c_float),
-                ("ep_first_expert", _i32), ("ep_num_experts", _i32)]
+                ("ep_first_expert", _i32), ("ep_num_experts", _i32), ("fuse_routing", _i32)]
 
 
 class moe_align_opts(ctypes.Structure):
@@ -58,10 +58,11 @@ class moe_workspace_layout(ctypes.Structure):
     _fields_ = [("block_m", _i32), ("tiles_cap", _i32), ("rows_cap", _i32),
                 ("split_gateup", _i32), ("split_down", _i32), ("grid_gateup", _i32),
                 ("grid_down", _i32), ("fused_act", _i32), ("smem_index", _i32),
-                ("weight_tiles_per_unit", _i32)] + [
+                ("weight_tiles_per_unit", _i32), ("route_fused", _i32)] + [
         (n, _sz) for n in ("off_counts", "off_offsets", "off_sorted_ids", "off_tile_expert",
                            "off_tiles", "off_inv_pos", "off_num_tiles", "off_index_scratch", "off_xq", "off_xs",
-                           "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "total_bytes")]
+                           "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "off_router",
+                           "off_route_counter", "total_bytes")]
 
 
 def _load() -> ctypes.CDLL:
@@ -90,6 +91,11 @@ def _load() -> ctypes.CDLL:
         "moe_forward_static": (_i32, [P(moe_shape), _vp, _vp, _vp, _vp, _vp, P(moe_scales),
                                       _vp, _vp, _vp]),
         "moe_status_str": (ctypes.c_char_p, [_i32]),
+        "moe_plan_routed": (_i32, [P(moe_shape), P(moe_forward_opts), P(moe_workspace_layout)]),
+        "moe_routed_workspace_bytes": (_sz, [P(moe_shape), P(moe_forward_opts)]),
+        "moe_forward_routed": (_i32, [P(moe_shape), _vp, _vp, _i32, ctypes.c_float, _vp, _vp,
+                                      P(moe_scales), _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp,
+                                      P(moe_forward_opts)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -101,7 +107,8 @@ def _load() -> ctypes.CDLL:
 lib = _load()
 SYMBOLS = ("moe_index_tiles_cap", "moe_plan", "moe_workspace_bytes", "moe_align", "moe_forward",
            "moe_forward_ex", "moe_combine", "moe_router_prepare", "moe_router_workspace_bytes",
-           "moe_router_topk", "moe_forward_static", "moe_status_str", "moe_align_ex")
+           "moe_router_topk", "moe_forward_static", "moe_status_str", "moe_align_ex",
+           "moe_plan_routed", "moe_routed_workspace_bytes", "moe_forward_routed")
 # Largest workspace moe_forward_static can serve (MOE_STATIC_SCRATCH_BYTES).
 STATIC_SCRATCH_BYTES = 128 << 20
 
@@ -150,8 +157,9 @@ def moe_index_tiles_cap(T, k, E, block_m) -> int:
 def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
               stage_events=None, separate_act=False, smem_index=False,
               single_weight_tile=False, num_shared_experts=0, shared_expert_weight=0.0,
-              ep_first_expert=0, ep_num_experts=0) -> moe_forward_opts:
+              ep_first_expert=0, ep_num_experts=0, fuse_routing=False) -> moe_forward_opts:
     o = moe_forward_opts()
+    o.fuse_routing = int(fuse_routing)
     o.num_shared_experts = num_shared_experts
     o.shared_expert_weight = shared_expert_weight
     o.ep_first_expert = ep_first_expert
@@ -308,10 +316,52 @@ def moe_router_topk(x, hi_lo, k, score_fn=MOE_SCORE_SOFTMAX, scale=1.0, *, score
     return scores, topk_ids, topk_w
 
 
-def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None) -> dict:
-    """Views of the intermediates moe_forward left in `workspace` (index,
-    quantised x, Gate-Up partials, activation, Down partials)."""
-    L = moe_plan(shape, opts)
+def moe_plan_routed(shape: moe_shape, opts: moe_forward_opts | None = None) -> moe_workspace_layout:
+    L = moe_workspace_layout()
+    _check(lib.moe_plan_routed(ctypes.byref(shape), ctypes.byref(opts) if opts else None,
+                               ctypes.byref(L)), "moe_plan_routed")
+    return L
+
+
+def moe_routed_workspace_bytes(shape: moe_shape, opts: moe_forward_opts | None = None) -> int:
+    return int(lib.moe_routed_workspace_bytes(ctypes.byref(shape),
+                                              ctypes.byref(opts) if opts else None))
+
+
+def moe_forward_routed(x, hi_lo, k, w13, w2, *, score_fn=MOE_SCORE_SOFTMAX, scale=1.0,
+                       scales=None, out=None, out_dtype=None, scores=None, topk_ids=None,
+                       topk_w=None, workspace=None, block_m=0, dev_status=None, stream=None,
+                       opts=None):
+    """The layer with its router in the path: returns (out, scores, topk_ids,
+    topk_w); the routing outputs are written by the call."""
+    T, H = x.shape
+    E = hi_lo.shape[0] // 2
+    dev = x.device
+    scores = scores if scores is not None else torch.empty((T, E), dtype=torch.float32, device=dev)
+    topk_ids = topk_ids if topk_ids is not None else torch.empty((T, k), dtype=torch.int32, device=dev)
+    topk_w = topk_w if topk_w is not None else torch.empty((T, k), dtype=torch.float32, device=dev)
+    shape = layer_shape(x, w13, topk_ids, block_m, out.dtype if out is not None else out_dtype)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16 if shape.out_dtype else torch.float32,
+                          device=dev)
+    need = moe_routed_workspace_bytes(shape, opts)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    sc = moe_scales(_ptr(scales[0]), _ptr(scales[1])) if scales is not None else None
+    _check(lib.moe_forward_routed(ctypes.byref(shape), _ptr(x), _ptr(hi_lo), score_fn, scale,
+                                  _ptr(w13), _ptr(w2), ctypes.byref(sc) if sc else None,
+                                  _ptr(scores), _ptr(topk_ids), _ptr(topk_w), _ptr(out),
+                                  _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                  _stream(stream), ctypes.byref(opts) if opts else None),
+           "moe_forward_routed")
+    return out, scores, topk_ids, topk_w
+
+
+def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None, routed=False) -> dict:
+    """Views of the intermediates moe_forward (moe_forward_routed with
+    routed=True) left in `workspace` (index, quantised x, Gate-Up partials,
+    activation, Down partials)."""
+    L = moe_plan_routed(shape, opts) if routed else moe_plan(shape, opts)
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     ns = opts.num_shared_experts if opts is not None else 0
     E, k = E + ns, k + ns   # experts and assignments per token of the index

@@ -64,6 +64,7 @@ struct GemmParams {
   struct {                   // expert-id status bit to dev_status
     int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
   } index_out;
+  unsigned int* zero_word;   // if set, CTA 0 zeroes it at start (the next kernel's ticket counter)
   int early_weights;         // contiguous token operand: stream weights before the wait
   int scale_by_token;        // FP8 gathered operand: b_scale rows are tokens
 };
@@ -116,6 +117,26 @@ cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H,
                            cudaStream_t st, bool pdl);
 cudaError_t launch_router_prepare(const float* wr, int E, int H, void* hi_lo,
                                   cudaStream_t st);
+
+// Router top-k + FP8 x-quant + routing index in one grid (k_route.cu).
+struct RouteIndexParams {
+  const float* P;            // router GEMM split-K partials [splits][rows_cap_r][2E]
+  int splits, rows_cap_r, T, E, k, score_fn;
+  float scale;
+  float* scores;             // [T][E]
+  int32_t* ids;              // [T][k]
+  float* w;                  // [T][k]
+  const void* x;             // bf16 [T][H]; xq null: no quantisation
+  int H;
+  uint8_t* xq;               // e4m3 [T][H]
+  float* xs;                 // [T][H/128]
+  int Ei, bm, tiles_cap;     // index: experts, row tile, tiles
+  IndexPtrs idx;
+  int32_t* dev_status;
+  unsigned int* counter;     // ticket counter, zero at launch
+};
+size_t route_index_smem_bytes(int T, int k, int Ei);
+cudaError_t launch_route_index(const RouteIndexParams& q, cudaStream_t st, bool pdl);
 cudaError_t launch_router_topk(const float* P, int splits, int rows_cap, int T, int E,
                                int k, int score_fn, float scale, float* scores,
                                int32_t* ids, float* w, cudaStream_t st, bool pdl);

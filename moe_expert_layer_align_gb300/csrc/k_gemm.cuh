@@ -224,6 +224,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
   const int tk = p.T * p.topk;
 
   if (threadIdx.x == 0) {
+    if (p.zero_word && blockIdx.x == 0) *p.zero_word = 0u;
     for (int s = 0; s < S::kStages; ++s) {
       // the TMA thread's expect-tx arrival, plus one per gather thread
       mbar_init(bar_full + 8 * s, 1 + S::kGatherThreads);

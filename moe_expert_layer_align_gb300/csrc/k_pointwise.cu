@@ -6,22 +6,9 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "route_common.cuh"
 
 namespace moe {
-
-// FP8 rule for one group of 128 channels held 4 per lane by a warp:
-// s = amax/448 (1 when amax is 0); q = e4m3 RNE-satfinite(v / s) (IEEE fp32
-// division).  Returns the 4 codes packed little-endian; writes s via *scale.
-__device__ __forceinline__ uint32_t quant_group4(const float (&v)[4], float* scale) {
-  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-  const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
-  *scale = s;
-  const uint16_t lo = cvt_e4m3x2(__fdiv_rn(v[1], s), __fdiv_rn(v[0], s));
-  const uint16_t hi = cvt_e4m3x2(__fdiv_rn(v[3], s), __fdiv_rn(v[2], s));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
 
 // ---------------------------------------------------------------- x quant
 // x bf16 [T][H] -> xq e4m3 [T][H], xs [T][H/128]; one warp per group.  The
@@ -245,11 +232,7 @@ cudaError_t launch_router_prepare(const float* wr, int E, int H, void* hi_lo, cu
   return cudaGetLastError();
 }
 
-// One warp per token: scores from the split-K partials of the two GEMMs
-// (P[s][t][0..E) = x.hi, P[s][t][E..2E) = x.lo), score = acc_hi + acc_lo/256;
-// softmax (or sigmoid); k rounds of warp arg-max over the raw scores (ties to
-// the lower id); weights renormalised over the selected ids, times `scale`.
-constexpr int kRouterMaxE = 512;
+// One warp per token (router_topk_warp).
 
 __global__ void __launch_bounds__(128)
     moe_router_topk_kernel(const float* __restrict__ P, int splits, int rows_cap, int T, int E,
@@ -258,87 +241,7 @@ __global__ void __launch_bounds__(128)
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  constexpr int kPer = kRouterMaxE / 32;
-  float s[kPer];
-  const size_t slice = static_cast<size_t>(rows_cap) * 2 * E;
-  const int per = (E + 31) / 32;   // slots this warp really uses
-  float mx = -INFINITY;
-  const float* row = P + static_cast<size_t>(t) * 2 * E;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = lane + 32 * i;
-    float v = -INFINITY;
-    if (i < per && e < E) {
-      float hi = __ldg(row + e), lo = __ldg(row + E + e);
-#pragma unroll 4
-      for (int sp = 1; sp < splits; ++sp) {
-        hi += __ldg(row + sp * slice + e);
-        lo += __ldg(row + sp * slice + E + e);
-      }
-      v = hi + lo * (1.0f / 256.0f);
-      scores[static_cast<size_t>(t) * E + e] = v;
-    }
-    s[i] = v;
-    mx = fmaxf(mx, v);
-  }
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
-  float prob[kPer];
-  float z = 0.f;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = lane + 32 * i;
-    float pv = 0.f;
-    if (e < E) pv = score_fn == 0 ? expf(s[i] - mx) : 1.0f / (1.0f + expf(-s[i]));
-    prob[i] = pv;
-    z += pv;
-  }
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
-  float psel = 0.f, my_p = 0.f;
-  int my_id = -1;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && (s[i] > bv || (s[i] == bv && e < bi))) {
-        bv = s[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    // owner lane removes the winner and reports its probability
-    float pw = 0.f;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      if (lane + 32 * i == bi) {
-        pw = score_fn == 0 ? prob[i] / z : prob[i];
-        s[i] = -INFINITY;
-      }
-    const int owner = bi & 31;
-    pw = __shfl_sync(0xffffffffu, pw, owner);
-    psel += pw;
-    if (lane == j) {
-      my_id = bi;
-      my_p = pw;
-    }
-  }
-  if (lane < k) {
-    ids[static_cast<size_t>(t) * k + lane] = my_id;
-    w[static_cast<size_t>(t) * k + lane] = scale * (my_p / psel);
-  }
+  if (t < T) router_topk_warp(P, splits, rows_cap, t, E, k, score_fn, scale, scores, ids, w);
 }
 
 cudaError_t launch_router_topk(const float* P, int splits, int rows_cap, int T, int E, int k,

@@ -38,14 +38,20 @@ struct Plan {
   int me1, me2;            // weight tiles per work unit (2: large token tiles, bf16)
   int fused_act;           // SiLU-and-mul in the Gate-Up epilogue
   int smem_index;          // GEMM CTAs rebuild the index in shared memory
-  size_t off[15];
+  size_t off[17];
   int split_index;         // index built by the count / scan / scatter kernels
   size_t total;
+  // in-path router (moe_forward_routed)
+  int routed;
+  int route_fused;         // router top-k, x-quant and index in one grid
+  int rp_bn, rp_rows_cap, rp_splits, rp_kts, rp_kt, rp_mt;
+  size_t rp_bytes;
 };
 
 enum {
   kOffCounts, kOffOffsets, kOffSorted, kOffTileExpert, kOffTiles, kOffInvPos, kOffNumTiles,
-  kOffIdxScratch, kOffXq, kOffXs, kOffXsRows, kOffG, kOffA, kOffAs, kOffY, kNumOff
+  kOffIdxScratch, kOffXq, kOffXs, kOffXsRows, kOffG, kOffA, kOffAs, kOffY, kOffRouterP,
+  kOffCounter, kNumOff
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -137,6 +143,13 @@ moe_status check_shape(const moe_shape* s) {
   return MOE_OK;
 }
 
+// Router plan: row tile, split-K count and workspace for the partial sums.
+struct RouterPlan {
+  int bn, rows_cap, splits, kts, kt, mt;
+  size_t bytes;
+};
+bool router_plan(int T, int H, int E, RouterPlan* r);
+
 // Shared experts and the expert-parallel range (moe_forward_opts /
 // moe_align_opts) as an IdMap; MOE_ERR_SHAPE on inconsistent values.
 moe_status make_idmap(int k, int E, int n_shared, int e0, int Eg, IdMap* m) {
@@ -150,10 +163,21 @@ moe_status make_idmap(int k, int E, int n_shared, int e0, int Eg, IdMap* m) {
   return MOE_OK;
 }
 
-moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
+moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, bool routed = false) {
   moe_status st = check_shape(s);
   if (st != MOE_OK) return st;
   std::memset(p, 0, sizeof(*p));
+  if (routed) {
+    // the router's ids arrive in-chain: the shared-memory index (which reads
+    // them before waiting on the previous stage) is off, and the id mapping
+    // variants are not combined with the in-path router
+    RouterPlan r;
+    if (!router_plan(s->T, s->H, s->E, &r) || s->k > 32) return MOE_ERR_SHAPE;
+    if (o && (o->smem_index || o->num_shared_experts || o->ep_num_experts)) return MOE_ERR_SHAPE;
+    p->routed = 1;
+    p->rp_bn = r.bn, p->rp_rows_cap = r.rows_cap, p->rp_splits = r.splits, p->rp_kts = r.kts;
+    p->rp_kt = r.kt, p->rp_mt = r.mt, p->rp_bytes = r.bytes;
+  }
   const int n_shared = o ? o->num_shared_experts : 0;
   st = make_idmap(s->k, s->E, n_shared, o ? o->ep_first_expert : 0, o ? o->ep_num_experts : 0,
                   &p->map);
@@ -207,6 +231,9 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
   }
   // many assignments: build the index over chunks, one CTA each
   p->split_index = !p->smem_index && static_cast<int64_t>(p->T) * p->k > kSplitIndexMinAssignments;
+  // in-path router with few assignments: top-k, x-quant and index in one grid
+  p->route_fused = p->routed && o && o->fuse_routing && !p->split_index && p->map.plain() &&
+                   route_index_smem_bytes(p->T, p->k, p->E) <= 128 * 1024;
   // workspace layout
   const size_t tk = static_cast<size_t>(p->T) * p->k;
   const size_t rc = p->rows_cap;
@@ -226,6 +253,8 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p) {
       rc * s->I * (p->fp8 ? 1 : 2),
       p->fp8 ? 4 * rc * (s->I / 128) : 0,
       4 * static_cast<size_t>(p->s2) * rc * s->H,
+      p->routed ? p->rp_bytes : 0,
+      p->routed ? 4u : 0u,
   };
   size_t cur = 0;
   for (int i = 0; i < kNumOff; ++i) {
@@ -255,6 +284,9 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->off_tiles = p.off[kOffTiles];
   L->off_inv_pos = p.off[kOffInvPos];
   L->off_num_tiles = p.off[kOffNumTiles];
+  L->route_fused = p.route_fused;
+  L->off_router = p.off[kOffRouterP];
+  L->off_route_counter = p.off[kOffCounter];
   L->off_index_scratch = p.off[kOffIdxScratch];
   L->off_xq = p.off[kOffXq];
   L->off_xs = p.off[kOffXs];
@@ -367,12 +399,6 @@ cudaError_t launch_gemm(int fp8, int bn, int bsrc, int grid, cudaStream_t st, bo
              : launch_gemm_bf16(bn, bsrc, grid, st, pdl, a, b, p, me);
 }
 
-// Router plan: row tile, split-K count and workspace for the partial sums.
-struct RouterPlan {
-  int bn, rows_cap, splits, kts, kt, mt;
-  size_t bytes;
-};
-
 bool router_plan(int T, int H, int E, RouterPlan* r) {
   if (T < 1 || H < 128 || H % 128 || E < 64 || E > 512 || E % 64) return false;
   r->bn = T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128;
@@ -454,13 +480,23 @@ moe_status moe_align_ex(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E
                                   static_cast<cudaStream_t>(stream), false, m));
 }
 
-moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13, const void* w2,
-                          const int32_t* topk_ids, const float* topk_w, const moe_scales* scales,
-                          void* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
-                          void* stream, const moe_forward_opts* opts) {
-  Plan p;
-  moe_status st = make_plan(shape, opts, &p);
-  if (st != MOE_OK) return st;
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// The in-path router of a moe_forward_routed call.
+struct RouteCall {
+  const void* hi_lo;
+  int score_fn;
+  float scale;
+  float* scores;
+};
+
+moe_status forward_impl(const Plan& p, const void* x, const void* w13, const void* w2,
+                        const int32_t* topk_ids, const float* topk_w, const moe_scales* scales,
+                        void* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                        void* stream, const moe_forward_opts* opts, const RouteCall* rc) {
   if (!x || !w13 || !w2 || !topk_ids || !topk_w || !out || !workspace) return MOE_ERR_ARG;
   if (p.fp8 && (!scales || !scales->w13_scale || !scales->w2_scale)) return MOE_ERR_ARG;
   if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
@@ -508,8 +544,67 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
     return r;
   };
 
-  record(opts, 0, s);
-  if (p.split_index) {
+  if (rc) {
+    // router GEMM over [hi; lo] (dense token rows); it also zeroes the ticket
+    // counter of the fused routing kernel that follows
+    record(opts, 7, s);
+    CUtensorMap tmR, tmXr;
+    if (!make_map_3d(&tmR, rc->hi_lo, 2, p.H, 2ull * p.map.E, 1, 128) ||
+        !make_map_2d(&tmXr, x, 2, p.H, p.T, p.rp_bn))
+      return MOE_ERR_CUDA;
+    GemmParams gr = {};
+    gr.M = 2 * p.map.E;
+    gr.K = p.H;
+    gr.m_tiles = p.rp_mt;
+    gr.splits = p.rp_splits;
+    gr.kt_per_split = p.rp_kts;
+    gr.kt_total = p.rp_kt;
+    gr.dense_rows = p.T;
+    gr.out = reinterpret_cast<float*>(at(kOffRouterP));
+    gr.rows_cap = p.rp_rows_cap;
+    gr.zero_word = p.route_fused ? reinterpret_cast<unsigned int*>(at(kOffCounter)) : nullptr;
+    const int units_r = p.rp_mt * p.rp_splits * (p.rp_rows_cap / p.rp_bn);
+    e = launch_gemm_bf16(p.rp_bn, kDense, std::min(sms, units_r), s, chain(), tmR, tmXr, gr);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    record(opts, 0, s);
+    if (p.route_fused) {
+      RouteIndexParams q = {};
+      q.P = reinterpret_cast<const float*>(at(kOffRouterP));
+      q.splits = p.rp_splits;
+      q.rows_cap_r = p.rp_rows_cap;
+      q.T = p.T;
+      q.E = p.map.E;
+      q.k = p.k;
+      q.score_fn = rc->score_fn;
+      q.scale = rc->scale;
+      q.scores = rc->scores;
+      q.ids = const_cast<int32_t*>(topk_ids);
+      q.w = const_cast<float*>(topk_w);
+      q.x = x;
+      q.H = p.H;
+      q.xq = p.fp8 ? xq : nullptr;
+      q.xs = xs;
+      q.Ei = p.E;
+      q.bm = p.bm;
+      q.tiles_cap = p.tiles_cap;
+      q.idx = ip;
+      q.dev_status = dev_status;
+      q.counter = reinterpret_cast<unsigned int*>(at(kOffCounter));
+      e = launch_route_index(q, s, chain());
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+    } else {
+      e = launch_router_topk(reinterpret_cast<const float*>(at(kOffRouterP)), p.rp_splits,
+                             p.rp_rows_cap, p.T, p.map.E, p.k, rc->score_fn, rc->scale,
+                             rc->scores, const_cast<int32_t*>(topk_ids),
+                             const_cast<float*>(topk_w), s, chain());
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+  } else {
+    record(opts, 0, s);
+  }
+  if (p.route_fused) {
+    // routing index and x-quant done by the fused routing kernel
+  } else if (p.split_index) {
     e = launch_align_split(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip,
                            reinterpret_cast<int32_t*>(at(kOffIdxScratch)), dev_status, s, chain(),
                            p.map);
@@ -521,7 +616,7 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   }
 
   record(opts, 1, s);
-  if (p.fp8) {
+  if (p.fp8 && !p.route_fused) {
     // with the shared-memory index the scales stay per token (the Gate-Up
     // epilogue looks tokens up in its own index)
     e = launch_quant_x(x, p.T, p.H, p.k, p.smem_index ? nullptr : ip.inv_pos, xq, xs,
@@ -546,8 +641,10 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   g1.topk = p.k;
   g1.sentinel = tk;
   g1.w_scale = p.fp8 ? scales->w13_scale : nullptr;
-  g1.b_scale = p.fp8 ? (p.smem_index ? xs : xs_rows) : nullptr;
-  g1.scale_by_token = p.smem_index;
+  // per-token scales where no index-ordered copy was written
+  const bool by_token = p.smem_index || p.route_fused;
+  g1.b_scale = p.fp8 ? (by_token ? xs : xs_rows) : nullptr;
+  g1.scale_by_token = by_token;
   g1.smem_index = p.smem_index;
   g1.topk_ids = topk_ids;
   g1.T = p.T;
@@ -610,6 +707,53 @@ moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   record(opts, 6, s);
   return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status moe_forward_ex(const moe_shape* shape, const void* x, const void* w13, const void* w2,
+                          const int32_t* topk_ids, const float* topk_w, const moe_scales* scales,
+                          void* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
+                          void* stream, const moe_forward_opts* opts) {
+  Plan p;
+  moe_status st = make_plan(shape, opts, &p);
+  if (st != MOE_OK) return st;
+  return forward_impl(p, x, w13, w2, topk_ids, topk_w, scales, out, workspace, ws_bytes,
+                      dev_status, stream, opts, nullptr);
+}
+
+moe_status moe_plan_routed(const moe_shape* shape, const moe_forward_opts* opts,
+                           moe_workspace_layout* layout) {
+  if (!layout) return MOE_ERR_ARG;
+  Plan p;
+  moe_status st = make_plan(shape, opts, &p, true);
+  if (st != MOE_OK) return st;
+  fill_layout(p, layout);
+  return MOE_OK;
+}
+
+size_t moe_routed_workspace_bytes(const moe_shape* shape, const moe_forward_opts* opts) {
+  Plan p;
+  return make_plan(shape, opts, &p, true) == MOE_OK ? p.total : 0;
+}
+
+moe_status moe_forward_routed(const moe_shape* shape, const void* x, const void* hi_lo,
+                              int32_t score_fn, float scale, const void* w13, const void* w2,
+                              const moe_scales* scales, float* scores, int32_t* topk_ids,
+                              float* topk_w, void* out, void* workspace, size_t ws_bytes,
+                              int32_t* dev_status, void* stream, const moe_forward_opts* opts) {
+  Plan p;
+  moe_status st = make_plan(shape, opts, &p, true);
+  if (st != MOE_OK) return st;
+  if (!hi_lo || !scores) return MOE_ERR_ARG;
+  if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_ARG;
+  if (!aligned(hi_lo, 16) || !aligned(scores, 4)) return MOE_ERR_ALIGN;
+  RouteCall rc{hi_lo, score_fn, scale, scores};
+  return forward_impl(p, x, w13, w2, topk_ids, topk_w, scales, out, workspace, ws_bytes,
+                      dev_status, stream, opts, &rc);
 }
 
 moe_status moe_forward(const moe_shape* shape, const void* x, const void* w13, const void* w2,

@@ -154,3 +154,19 @@ def test_align_ex_host_checks():
                               None) == moe.MOE_ERR_SHAPE
     assert B.lib.moe_align_ex(None, 8, 2, 8, 16, ctypes.byref(o), ctypes.byref(idx), None,
                               None) == moe.MOE_ERR_ARG
+
+
+def test_routed_plan():
+    s = moe.make_shape(64, 2048, 768, 128, 8, 0, True)
+    assert moe.moe_plan_routed(s).route_fused == 0          # opt-in
+    L = moe.moe_plan_routed(s, moe.make_opts(fuse_routing=True))
+    assert L.route_fused == 1 and L.off_router >= L.off_y and L.off_route_counter > L.off_router
+    assert moe.moe_routed_workspace_bytes(s) == L.total_bytes > moe.moe_workspace_bytes(s)
+    assert moe.moe_plan_routed(moe.make_shape(512, 2048, 768, 128, 8, 0, True),
+                               moe.make_opts(fuse_routing=True)).route_fused == 0
+    for o in (moe.make_opts(smem_index=True), moe.make_opts(num_shared_experts=1),
+              moe.make_opts(ep_first_expert=0, ep_num_experts=256)):
+        with pytest.raises(moe.MoeError):
+            moe.moe_plan_routed(s, o)
+    with pytest.raises(moe.MoeError):           # router E must be a multiple of 64
+        moe.moe_plan_routed(moe.make_shape(64, 2048, 768, 100, 8))

@@ -72,7 +72,7 @@ def test_full_size_layer(cfg, T, n, bases):
         np.testing.assert_allclose(w[sel].sum(1), wl.router_scale, rtol=1e-5)
 
     # the whole index, bit-exact
-    v = moe.workspace_views(layer.ws, layer.shape)
+    v = moe.workspace_views(layer.ws, layer.shape, routed=wl.wr is not None)
     L = v["layout"]
     ref = oracle.align(ids, wl.E, L.block_m)
     assert ref["invalid"] == 0

@@ -66,3 +66,43 @@ def test_routed_fp8_layer(T):
     got = run_layer(wl, topk_ids=ids, topk_w=w).float().cpu().numpy()
     ref = oracle_layer(wl, topk_ids=ids.cpu(), topk_w=w.cpu())
     assert_layer_close(got, ref, "fp8", f"routed T={T}")
+
+
+@pytest.mark.parametrize("fuse", [True, False])
+@pytest.mark.parametrize("T", [4, 64, 256, 300])
+@pytest.mark.parametrize("mode", ["fp8", "bf16"])
+def test_forward_routed_equals_router_then_layer(T, mode, fuse):
+    # One chain (router GEMM, then the fused top-k + x-quant + index grid up to
+    # 2048 assignments, separate kernels above) against the two public calls
+    # it replaces: every output bit-identical, and the layer against the oracle.
+    import moe_expert_layer_align_gb300 as moe
+    cfg = 5 if mode == "fp8" else 3
+    wl = workloads.make(cfg, T, "cpu", H=512, I=256, E=64, k=8).to("cuda")
+    if wl.wr is None:
+        g = torch.Generator().manual_seed(31)
+        wl.wr = (torch.randn(64, 512, generator=g) / 512 ** 0.5).cuda()
+    hi_lo = moe.moe_router_prepare(wl.wr)
+    w13, w2 = (wl.w13q, wl.w2q) if mode == "fp8" else (wl.w13, wl.w2)
+    sc = (wl.w13s, wl.w2s) if mode == "fp8" else None
+    shape = moe.layer_shape(wl.x, w13, torch.empty(T, 8), 0, torch.bfloat16)
+    opts = moe.make_opts(fuse_routing=fuse)
+    L = moe.moe_plan_routed(shape, opts)
+    assert L.route_fused == int(fuse and T * 8 <= 2048)
+    ws = torch.zeros(moe.moe_routed_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
+    st = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    out, scores, ids, w = moe.moe_forward_routed(wl.x, hi_lo, 8, w13, w2, scales=sc,
+                                                 workspace=ws, dev_status=st, opts=opts)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    s2, ids2, w2_ = moe.moe_router_topk(wl.x, hi_lo, 8)
+    ws2 = torch.zeros(moe.moe_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    out2 = moe.moe_forward(wl.x, w13, w2, ids2, w2_, scales=sc, workspace=ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(scores, s2) and torch.equal(ids, ids2) and torch.equal(w, w2_)
+    assert torch.equal(out, out2)
+    v1 = moe.workspace_views(ws, shape, opts, routed=True)
+    v2 = moe.workspace_views(ws2, shape)
+    for n in ("counts", "offsets", "sorted_ids", "tile_expert", "tiles", "inv_pos", "num_tiles"):
+        assert torch.equal(v1[n], v2[n]), n
+    ref = oracle_layer(wl, topk_ids=ids.cpu(), topk_w=w.cpu())
+    assert_layer_close(out.float().cpu().numpy(), ref, mode, f"routed {mode} T={T}")
