@@ -16,7 +16,9 @@ Passages followed (see the C file for details):
   * router — same post, section "Router GEMM", "a precision-aware BF16
     formulation";
   * FP8 — OCP E4M3 format; per-128 block scales of the SGLang MoE Triton
-    tuning guide, section 4.1 (block_shape [128, 128]).
+    tuning guide, section 4.1 (block_shape [128, 128]);
+  * w8a16 — the HPC-Ops post's operator table, row MoE ("BF16 hidden
+    states; FP8 E4M3 expert weights").
 """
 from __future__ import annotations
 
@@ -94,6 +96,9 @@ def lib() -> ctypes.CDLL:
             L.oracle_moe_fp8.argtypes = [_c_int] * 5 + [
                 _u8p, _f32p, _u8p, _f32p, _u8p, _f32p, _i32p, _f32p, _i32p, _c_int, _f64p,
                 ctypes.c_void_p, ctypes.c_void_p]
+            L.oracle_moe_w8a16.restype = None
+            L.oracle_moe_w8a16.argtypes = [_c_int] * 5 + [
+                _u16p, _u8p, _f32p, _u8p, _f32p, _i32p, _f32p, _i32p, _c_int, _f64p]
             L.oracle_router_split.restype = None
             L.oracle_router_split.argtypes = [_f32p, ctypes.c_int64, _u16p, _u16p]
             L.oracle_router_scores.restype = None
@@ -237,6 +242,26 @@ def moe_fp8(xq, xs, w13q, w13s, w2q, w2s, topk_ids, topk_w, sel=None, return_act
                          as_.ctypes.data if return_act else None)
     if return_act:
         return out, aq, as_
+    return out
+
+
+def moe_w8a16(x_bits, w13q, w13s, w2q, w2s, topk_ids, topk_w, sel=None) -> np.ndarray:
+    """fp64 output rows of the w8a16 layer: bf16 x, e4m3 weights with fp32
+    128x128 block scales dequantised exactly, no activation quantisation."""
+    x = _c(x_bits, np.uint16)
+    w13q = _c(w13q, np.uint8)
+    w13s = _c(w13s, np.float32)
+    w2q = _c(w2q, np.uint8)
+    w2s = _c(w2s, np.float32)
+    ids = _c(topk_ids, np.int32)
+    w = _c(topk_w, np.float32)
+    T, H = x.shape
+    E, I2, _ = w13q.shape
+    k = ids.shape[1]
+    s = _sel(sel, T)
+    out = np.zeros((s.size, H), np.float64)
+    lib().oracle_moe_w8a16(T, H, I2 // 2, E, k, x.ravel(), w13q.ravel(), w13s.ravel(),
+                           w2q.ravel(), w2s.ravel(), ids.ravel(), w.ravel(), s, s.size, out)
     return out
 
 

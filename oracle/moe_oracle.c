@@ -18,7 +18,7 @@
  *   - oracle_quant_group: the per-token-per-128-channel rule used for FP8
  *     activations (s = amax/448, 1 if amax == 0; q = e4m3(v/s)) in fp32, the
  *     precision the kernel takes the decision in.
- *   - oracle_moe_bf16 / oracle_moe_fp8: the layer as the conventional unfused
+ *   - oracle_moe_bf16 / oracle_moe_fp8 / oracle_moe_w8a16: the layer as the conventional unfused
  *     path states it (HPC-Ops × SGLang, section "MoE", paragraph on the
  *     conventional path: route, Gate-Up, activation (+quant), Down, top-k
  *     weighted reduce), per token, in fp64.  FP8 operands are dequantised
@@ -292,6 +292,69 @@ void oracle_moe_bf16(int T, int H, int I, int E, int k, const uint16_t* x,
  * oracle_quant_group on its fp32 rounding, then dequantised exactly.
  * If act_q / act_s are non-NULL they receive, per selected token and slot j,
  * the activation codes [n_sel][k][I] and scales [n_sel][k][I/128]. */
+/* w8a16 layer (the HPC-Ops MoE precision, operator table: "BF16 hidden
+ * states; FP8 E4M3 expert weights"): bf16 x as is, weights e4m3 with one fp32
+ * scale per 128x128 block dequantised exactly (e4m3_value(q) * scale, in
+ * fp64); the activation is not quantised.  Same step order and conventions
+ * as oracle_moe_bf16. */
+void oracle_moe_w8a16(int T, int H, int I, int E, int k, const uint16_t* x,
+                      const uint8_t* w13q, const float* w13s, const uint8_t* w2q,
+                      const float* w2s, const int32_t* ids, const float* w,
+                      const int32_t* sel, int n_sel, double* out) {
+  (void)T;
+  const int HB = H / 128, IB = I / 128;
+  double* xt = (double*)malloc(sizeof(double) * (size_t)H);
+  double* g = (double*)malloc(sizeof(double) * (size_t)I);
+  double* u = (double*)malloc(sizeof(double) * (size_t)I);
+  double* act = (double*)malloc(sizeof(double) * (size_t)I);
+  double* y = (double*)malloc(sizeof(double) * (size_t)H);
+  for (int si = 0; si < n_sel; ++si) {
+    int t = sel[si];
+    double* o = out + (size_t)si * H;
+    for (int h = 0; h < H; ++h) o[h] = 0.0;
+    for (int h = 0; h < H; ++h) xt[h] = bf16_value(x[(size_t)t * H + h]);
+    for (int j = 0; j < k; ++j) {
+      int e = ids[(size_t)t * k + j];
+      if (e < 0 || e >= E) continue; /* dropped assignment contributes 0 */
+      const uint8_t* q13 = w13q + (size_t)e * 2 * I * H;
+      const float* s13 = w13s + (size_t)e * (2 * I / 128) * HB;
+      const uint8_t* q2 = w2q + (size_t)e * H * I;
+      const float* s2 = w2s + (size_t)e * (H / 128) * IB;
+#pragma omp parallel for schedule(static)
+      for (int i = 0; i < I; ++i) {
+        double sg = 0.0, su = 0.0;
+        const int ru = I + i;   /* up row */
+        for (int h = 0; h < H; ++h) {
+          const double wg = oracle_e4m3_decode(q13[(size_t)i * H + h]) *
+                            (double)s13[(size_t)(i / 128) * HB + h / 128];
+          const double wu = oracle_e4m3_decode(q13[(size_t)ru * H + h]) *
+                            (double)s13[(size_t)(ru / 128) * HB + h / 128];
+          sg += xt[h] * wg;
+          su += xt[h] * wu;
+        }
+        g[i] = sg;
+        u[i] = su;
+      }
+      for (int i = 0; i < I; ++i) act[i] = silu(g[i]) * u[i];
+#pragma omp parallel for schedule(static)
+      for (int h = 0; h < H; ++h) {
+        double s = 0.0;
+        for (int i = 0; i < I; ++i)
+          s += act[i] * oracle_e4m3_decode(q2[(size_t)h * I + i]) *
+               (double)s2[(size_t)(h / 128) * IB + i / 128];
+        y[h] = s;
+      }
+      double wj = (double)w[(size_t)t * k + j];
+      for (int h = 0; h < H; ++h) o[h] += wj * y[h];
+    }
+  }
+  free(xt);
+  free(g);
+  free(u);
+  free(act);
+  free(y);
+}
+
 void oracle_moe_fp8(int T, int H, int I, int E, int k, const uint8_t* xq,
                     const float* xs, const uint8_t* w13q, const float* w13s,
                     const uint8_t* w2q, const float* w2s, const int32_t* ids,

@@ -83,3 +83,60 @@ def test_shared_expert_index_holds_every_token_in_order():
     rows = idx["sorted_ids"][o[E]: o[E] + T]
     np.testing.assert_array_equal(rows, np.arange(T) * (k + 1) + k)   # slot k of every token
     assert idx["counts"][E] == T
+
+
+# ---------------------------------------------------------------- w8a16
+
+def w8_case(T, H, I, E, k, seed, pow2_scales=False):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, H, generator=g).bfloat16()
+    q13 = torch.randint(0, 256, (E, 2 * I, H), generator=g, dtype=torch.uint8)
+    q2 = torch.randint(0, 256, (E, H, I), generator=g, dtype=torch.uint8)
+    q13[(q13 & 0x7F) == 0x7F] = 0          # no NaN codes
+    q2[(q2 & 0x7F) == 0x7F] = 0
+    if pow2_scales:
+        s13 = 2.0 ** torch.randint(-12, -4, (E, 2 * I // 128, H // 128), generator=g).float()
+        s2 = 2.0 ** torch.randint(-12, -4, (E, H // 128, I // 128), generator=g).float()
+    else:
+        s13 = torch.rand(E, 2 * I // 128, H // 128, generator=g) * 1e-3 + 1e-4
+        s2 = torch.rand(E, H // 128, I // 128, generator=g) * 1e-3 + 1e-4
+    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).int()
+    w = torch.rand(T, k, generator=g) + 0.1
+    return x, q13, s13, q2, s2, ids, w
+
+
+def test_w8a16_with_power_of_two_scales_is_the_bf16_layer():
+    # e4m3 values times 2^n are exact in bf16: the w8a16 oracle must then equal
+    # the bf16 oracle fed those dequantised weights
+    x, q13, s13, q2, s2, ids, w = w8_case(5, 256, 128, 3, 2, 1, pow2_scales=True)
+    deq13 = torch.from_numpy(oracle.e4m3_decode(q13.numpy())).float() * \
+        s13.repeat_interleave(128, 1).repeat_interleave(128, 2)
+    deq2 = torch.from_numpy(oracle.e4m3_decode(q2.numpy())).float() * \
+        s2.repeat_interleave(128, 1).repeat_interleave(128, 2)
+    assert torch.equal(deq13.bfloat16().float(), deq13) and torch.equal(deq2.bfloat16().float(), deq2)
+    got = oracle.moe_w8a16(bits(x), q13.numpy(), s13.numpy(), q2.numpy(), s2.numpy(),
+                           ids.numpy(), w.numpy())
+    ref = oracle.moe_bf16(bits(x), bits(deq13.bfloat16()), bits(deq2.bfloat16()), ids.numpy(),
+                          w.numpy())
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_w8a16_brute_force_and_block_scales():
+    # each scale acts on its own 128x128 block only: a numpy restatement with
+    # the scales expanded per element, per token and slot
+    x, q13, s13, q2, s2, ids, w = w8_case(3, 256, 256, 2, 2, 2)
+    got = oracle.moe_w8a16(bits(x), q13.numpy(), s13.numpy(), q2.numpy(), s2.numpy(),
+                           ids.numpy(), w.numpy())
+    dq = lambda q, s: oracle.e4m3_decode(q.numpy()) * np.repeat(np.repeat(  # noqa: E731
+        s.numpy().astype(np.float64), 128, 1), 128, 2)
+    W13, W2 = dq(q13, s13), dq(q2, s2)
+    X = val(x)
+    I = 256
+    ref = np.zeros((3, 256))
+    for t in range(3):
+        for j in range(2):
+            e = ids[t, j].item()
+            g = W13[e, :I] @ X[t]
+            u = W13[e, I:] @ X[t]
+            ref[t] += w[t, j].item() * (W2[e] @ (g / (1 + np.exp(-g)) * u))
+    np.testing.assert_allclose(got, ref, rtol=1e-9, atol=1e-12)
