@@ -214,9 +214,10 @@ class Layer:
     moe_forward — captured in a CUDA graph.  Router weights are split into
     their two bf16 parts once, before any timing."""
 
-    def __init__(self, wl, stream, opts=None, graph=True):
+    def __init__(self, wl, stream, opts=None, graph=True, w8a16=False):
         import moe_expert_layer_align_gb300 as moe
         self.moe, self.wl, self.stream, self.opts = moe, wl, stream, opts
+        self.w8a16 = w8a16          # FP8 workload's weights with bf16 activations
         dev = wl.x.device
         # The inputs were drawn on the current stream, whose freed blocks the
         # allocations below may reuse: order the layer's stream after it.
@@ -236,7 +237,7 @@ class Layer:
             self.hi_lo = None
             self.ids, self.w = wl.topk_ids, wl.topk_w
         out_dtype = torch.float32 if wl.out == "f32" else torch.bfloat16
-        shape = moe.layer_shape(wl.x, self.w13, self.ids, 0, out_dtype)
+        shape = moe.layer_shape(wl.x, self.w13, self.ids, 0, out_dtype, 0, w8a16)
         self.shape = shape
         if self.hi_lo is not None:
             self.plan = moe.moe_plan_routed(shape, opts)
@@ -251,8 +252,9 @@ class Layer:
         # launches per step: [router GEMM + (fused routing | top-k, align[, x-quant])]
         # or align[, x-quant]; Gate-Up; [act]; Down; combine
         L = self.plan
-        front = (2 if L.route_fused else 3 + (1 if self.fp8 else 0)) if self.hi_lo is not None \
-            else (0 if L.smem_index else 1) + (1 if self.fp8 else 0)
+        quant = 1 if (self.fp8 and not w8a16) else 0
+        front = (2 if L.route_fused else 3 + quant) if self.hi_lo is not None \
+            else (0 if L.smem_index else 1) + quant
         self.kernels_per_step = front + 3 + (0 if L.fused_act else 1)
         if graph:
             with torch.cuda.stream(stream):
@@ -282,7 +284,7 @@ class Layer:
             return
         self.moe.moe_forward(wl.x, self.w13, self.w2, self.ids, self.w, scales=self.scales,
                              out=self.out, workspace=self.ws, dev_status=self.status,
-                             stream=self.stream, opts=self.opts)
+                             stream=self.stream, opts=self.opts, w8a16=self.w8a16)
 
     def run(self):
         # replay() launches on the current stream: make it ours
@@ -313,7 +315,7 @@ def time_layer(layer, stream, flush, steps, warmup):
     return np.array([s.elapsed_time(e) * 1e3 for s, e in evs]), wall  # us
 
 
-def stage_times(wl, stream, flush, steps):
+def stage_times(wl, stream, flush, steps, w8a16=False):
     """Per-stage device time (us) from events recorded between the stages,
     captured with the layer in a CUDA graph (recording events between stages
     serialises them: PDL overlap is lost in this pass).  With the router in
@@ -329,7 +331,7 @@ def stage_times(wl, stream, flush, steps):
     opts = moe.make_opts(stage_events=evs)
     if routed:
         opts.stage_events[7] = ev_router.cuda_event
-    layer = Layer(wl, stream, opts=opts, graph=True)
+    layer = Layer(wl, stream, opts=opts, graph=True, w8a16=w8a16)
     acc = np.zeros(n - 1)
     router = 0.0
     for _ in range(steps):
@@ -347,11 +349,11 @@ def stage_times(wl, stream, flush, steps):
     return out
 
 
-def e2e_time(wl, stream, steps, warmup):
+def e2e_time(wl, stream, steps, warmup, w8a16=False):
     """The public API with host (pinned) inputs and result: H2D of x (and of
     the top-k ids and weights when the router is outside the path), the step,
     D2H of the output."""
-    dev_layer = Layer(wl, stream, graph=False)
+    dev_layer = Layer(wl, stream, graph=False, w8a16=w8a16)
     hx = wl.x.cpu().pin_memory()
     hid = None if dev_layer.hi_lo is not None else wl.topk_ids.cpu().pin_memory()
     hw = None if dev_layer.hi_lo is not None else wl.topk_w.cpu().pin_memory()
@@ -383,7 +385,7 @@ def e2e_time(wl, stream, steps, warmup):
             "d2h_bytes_per_step": hout.numel() * hout.element_size()}
 
 
-def oracle_baseline(wl, topk_ids, topk_w, budget_s=15.0, max_tokens=None):
+def oracle_baseline(wl, topk_ids, topk_w, budget_s=15.0, max_tokens=None, w8a16=False):
     """The oracle on the host cores over a bounded sample of the batch's
     tokens; latency scaled to the whole batch.  (In-path router: its fp64
     scores over the whole batch are timed and added.)"""
@@ -391,7 +393,11 @@ def oracle_baseline(wl, topk_ids, topk_w, budget_s=15.0, max_tokens=None):
     from tests.helpers import bits16, u8
     ids = topk_ids.cpu().numpy()
     w = topk_w.cpu().numpy()
-    if wl.mode == "bf16":
+    if w8a16:
+        args = (bits16(wl.x), u8(wl.w13q), wl.w13s.cpu().numpy(), u8(wl.w2q),
+                wl.w2s.cpu().numpy(), ids, w)
+        fn = oracle.moe_w8a16
+    elif wl.mode == "bf16":
         args = (bits16(wl.x), bits16(wl.w13), bits16(wl.w2), ids, w)
         fn = oracle.moe_bf16
     else:
@@ -498,8 +504,11 @@ def run_cuda(args):
 
     cfg = args.config
     wl = make_workload(cfg, args.T, "cuda")
-    fp8 = wl.mode == "fp8"
-    layer = Layer(wl, stream)
+    w8 = bool(args.w8a16)
+    if w8 and wl.mode != "fp8":
+        raise SystemExit("--w8a16 needs a workload with e4m3 weights (--config 4 or 5)")
+    fp8 = wl.mode == "fp8" and not w8      # e4m3 activations and tensor rate
+    layer = Layer(wl, stream, w8a16=w8)
     stream.synchronize()
     nums = layer_numbers(wl, layer.ids)
 
@@ -517,11 +526,12 @@ def run_cuda(args):
 
     result = None
     if rank == 0:
-        stg = stage_times(wl, stream, flush, max(3, min(args.steps, 10)))
+        stg = stage_times(wl, stream, flush, max(3, min(args.steps, 10)), w8)
         t_bytes, t_flops = roofline_times(nums, pk, fp8)
         gu_us = stg["gateup"]
         achieved = nums["gateup_bytes"] / (gu_us * 1e-6) / 1e9
-        kname = f"moe_gemm_kernel<{'e4m3' if fp8 else 'bf16'}, gather> (Gate-Up)"
+        kname = ("moe_gemm_w8_kernel<gather> (Gate-Up, e4m3 weights dequantised to bf16)" if w8
+                 else f"moe_gemm_kernel<{'e4m3' if fp8 else 'bf16'}, gather> (Gate-Up)")
         roof = {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                 "peak_kind": f"{pk_kind} burst copy (MEASURED_PEAKS.json hbm_gbs)",
@@ -531,7 +541,7 @@ def run_cuda(args):
         if not args.no_sweep:
             for T in workloads.CONFIGS[cfg]["sweep"]:
                 w2l = make_workload(cfg, T, "cuda", base=wl)
-                L2 = Layer(w2l, stream)
+                L2 = Layer(w2l, stream, w8a16=w8)
                 stream.synchronize()
                 n2 = layer_numbers(w2l, L2.ids)
                 tt, _ = time_layer(L2, stream, flush, 20, 3)
@@ -544,18 +554,21 @@ def run_cuda(args):
                               "bound": "hbm" if tb >= tf else "tensor",
                               "roofline_frac": max(tb, tf) / u})
                 del L2, w2l
-        e2e = e2e_time(wl, stream, max(args.steps, 5), args.warmup)
+        e2e = e2e_time(wl, stream, max(args.steps, 5), args.warmup, w8)
         clk.__exit__()
         clocks = clk.summary()
         clocks["window"] = "timed region, stage pass, sweep and e2e pass"
-        cpu = None if args.no_cpu else oracle_baseline(wl.to("cpu"), layer.ids, layer.w)
+        cpu = None if args.no_cpu else oracle_baseline(wl.to("cpu"), layer.ids, layer.w,
+                                                       w8a16=w8)
         plan = moe.moe_plan(layer.shape)
         result = {
             "metric": METRIC, "value": us, "unit": "us", "n_gpus": ws_, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if fp8 else ("w8a16 (e4m3 weights, bf16 activations)" if w8 else "bf16"),
             "data": "synthetic (seeded; random-init experts of the named shape)",
             "config": workload_config(cfg, args.T, wl, nums, {
+                **({"precision": "w8a16: the workload's e4m3 weights, bf16 activations"} if w8 else {}),
                 "replicas": ws_, "block_m": plan.block_m,
                 "split_k": [plan.split_gateup, plan.split_down],
                 "l2": f"flushed before every step ({flush.numel() >> 20} MiB write)",
@@ -593,7 +606,7 @@ def run_ncu(args):
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
     wl = make_workload(args.config, args.T, "cuda")
-    layer = Layer(wl, stream, graph=False)
+    layer = Layer(wl, stream, graph=False, w8a16=args.w8a16)
     for _ in range(args.warmup + args.steps):
         layer.run()
     stream.synchronize()
@@ -613,6 +626,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ncu", action="store_true", help="profiler mode (no bench line)")
+    ap.add_argument("--w8a16", action="store_true",
+                    help="e4m3-weight workloads (4, 5) with bf16 activations (MOE_W8A16)")
     ap.add_argument("--record-traffic", metavar="CSV",
                     help="store DRAM bytes per GEMM launch of --config/--T from an ncu raw-page "
                          "CSV export in profiles/traffic.json (no GPU needed)")

@@ -54,7 +54,13 @@ typedef enum {
   MOE_ERR_CUDA = 8        /* CUDA runtime / driver error */
 } moe_status;
 
-typedef enum { MOE_BF16 = 0, MOE_FP8_W8A8 = 1 } moe_mode;
+/* Precision of a layer call.  MOE_BF16: bf16 weights and activations.
+ * MOE_FP8_W8A8: e4m3 weights with fp32 128x128 block scales and e4m3
+ * activations (per token / row, per 128 channels).  MOE_W8A16: e4m3 weights
+ * with fp32 128x128 block scales and bf16 activations (HPC-Ops × SGLang,
+ * operator table, row MoE); the weights are dequantised to bf16 on chip
+ * (code * scale, round to nearest even) and the layer runs as MOE_BF16. */
+typedef enum { MOE_BF16 = 0, MOE_FP8_W8A8 = 1, MOE_W8A16 = 2 } moe_mode;
 typedef enum { MOE_OUT_F32 = 0, MOE_OUT_BF16 = 1 } moe_out;
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
 

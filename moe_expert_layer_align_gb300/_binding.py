@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_ARG, MOE_ERR_SHAPE, MOE_ERR_DTYPE, MOE_ERR_ALIGN = 0, 1, 2, 3, 4
 MOE_ERR_WORKSPACE, MOE_ERR_EXPERT_ID, MOE_ERR_TIMEOUT, MOE_ERR_CUDA = 5, 6, 7, 8
-MOE_BF16, MOE_FP8_W8A8 = 0, 1
+MOE_BF16, MOE_FP8_W8A8, MOE_W8A16 = 0, 1, 2
 MOE_OUT_F32, MOE_OUT_BF16 = 0, 1
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 # Stage indices of moe_forward_opts.stage_events.
@@ -145,9 +145,10 @@ def device_status_bits(word: int) -> list[int]:
 
 # ---------------------------------------------------------------- shapes
 
-def make_shape(T, H, I, E, k, block_m=0, fp8=False, out_bf16=True) -> moe_shape:
-    return moe_shape(T, H, I, E, k, block_m, MOE_FP8_W8A8 if fp8 else MOE_BF16,
-                     MOE_OUT_BF16 if out_bf16 else MOE_OUT_F32)
+def make_shape(T, H, I, E, k, block_m=0, fp8=False, out_bf16=True, mode=None) -> moe_shape:
+    """mode: MOE_BF16 / MOE_FP8_W8A8 / MOE_W8A16 (default from `fp8`)."""
+    m = mode if mode is not None else (MOE_FP8_W8A8 if fp8 else MOE_BF16)
+    return moe_shape(T, H, I, E, k, block_m, m, MOE_OUT_BF16 if out_bf16 else MOE_OUT_F32)
 
 
 def moe_index_tiles_cap(T, k, E, block_m) -> int:
@@ -223,24 +224,29 @@ def moe_align_ex(topk_ids: torch.Tensor, E: int, block_m: int, num_shared_expert
     return idx
 
 
-def layer_shape(x, w13, topk_ids, block_m=0, out_dtype=None, n_shared=0) -> moe_shape:
+def layer_shape(x, w13, topk_ids, block_m=0, out_dtype=None, n_shared=0,
+                w8a16=False) -> moe_shape:
     """Shape of a layer call; w13 holds the routed experts and then `n_shared`
-    shared ones, so the shape's E (routed) is w13's first extent - n_shared."""
+    shared ones, so the shape's E (routed) is w13's first extent - n_shared.
+    e4m3 weights mean the FP8 layer, or with w8a16 the bf16-activation one."""
     T, H = x.shape
     E, I2, _ = w13.shape
     E -= n_shared
     fp8 = w13.dtype in (torch.uint8, torch.float8_e4m3fn)
     out_bf16 = (out_dtype or torch.bfloat16) == torch.bfloat16
-    return make_shape(T, H, I2 // 2, E, topk_ids.shape[1], block_m, fp8, out_bf16)
+    return make_shape(T, H, I2 // 2, E, topk_ids.shape[1], block_m, fp8, out_bf16,
+                      MOE_W8A16 if (fp8 and w8a16) else None)
 
 
 def moe_forward(x, w13, w2, topk_ids, topk_w, *, scales=None, out=None, out_dtype=None,
-                workspace=None, block_m=0, dev_status=None, stream=None, opts=None):
+                workspace=None, block_m=0, dev_status=None, stream=None, opts=None,
+                w8a16=False):
     """The whole layer.  BF16: w13/w2 bf16.  FP8: w13/w2 uint8 e4m3 codes and
-    scales = (w13_scale, w2_scale).  Returns `out` [T, H] (bf16 or fp32)."""
+    scales = (w13_scale, w2_scale); w8a16=True keeps the activations bf16
+    (MOE_W8A16).  Returns `out` [T, H] (bf16 or fp32)."""
     shape = layer_shape(x, w13, topk_ids, block_m,
                         out.dtype if out is not None else out_dtype,
-                        opts.num_shared_experts if opts is not None else 0)
+                        opts.num_shared_experts if opts is not None else 0, w8a16)
     if out is None:
         out = torch.empty(x.shape, dtype=torch.bfloat16 if shape.out_dtype else torch.float32,
                           device=x.device)

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 ROOT = os.path.dirname(HERE)
 
 SOURCES = ["moe_api.cu", "k_align.cu", "k_pointwise.cu", "k_route.cu", "k_gemm_bf16.cu",
-           "k_gemm_bf16_direct.cu", "k_gemm_fp8.cu", "moe_static.cu"]
+           "k_gemm_bf16_direct.cu", "k_gemm_fp8.cu", "k_gemm_w8.cu", "moe_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                   "-Xcompiler", "-fvisibility=hidden", "-I", os.path.join(ROOT, "include")]

@@ -87,6 +87,11 @@ cudaError_t launch_gemm_fp8(int bn, int bsrc, int grid, cudaStream_t st, bool pd
                             const CUtensorMap& tmA, const CUtensorMap& tmB,
                             const GemmParams& p);
 
+// w8a16: FP8 weights (tmA over e4m3 bytes, 64-byte boxes, no swizzle) and
+// bf16 token rows; the epilogue is the bf16 GEMM's (k_gemm_w8.cu).
+cudaError_t launch_gemm_w8(int bn, int bsrc, int grid, cudaStream_t st, bool pdl,
+                           const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p);
+
 // Index build, pointwise stages (k_align.cu, k_pointwise.cu).
 struct IndexPtrs {
   int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;

@@ -30,6 +30,7 @@ struct Plan {
   // k, E: assignments per token and experts of the index and the weights
   // (routed + shared); the IdMap maps topk_ids onto them.
   int T, H, I, E, k, bm, fp8, out_bf16;
+  int w8;                  // w8a16: e4m3 weights dequantised on chip, bf16 activations
   IdMap map;
   float w_shared;
   int tiles_cap, rows_cap;
@@ -132,9 +133,12 @@ void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int*
 
 moe_status check_shape(const moe_shape* s) {
   if (!s) return MOE_ERR_ARG;
-  if (s->mode != MOE_BF16 && s->mode != MOE_FP8_W8A8) return MOE_ERR_DTYPE;
+  if (s->mode != MOE_BF16 && s->mode != MOE_FP8_W8A8 && s->mode != MOE_W8A16)
+    return MOE_ERR_DTYPE;
   if (s->out_dtype != MOE_OUT_F32 && s->out_dtype != MOE_OUT_BF16) return MOE_ERR_DTYPE;
   const int fp8 = s->mode == MOE_FP8_W8A8;
+  const int w8 = s->mode == MOE_W8A16;
+  if (w8 && (s->H % 128 || s->I % 128 || s->block_m == 256)) return MOE_ERR_SHAPE;
   if (s->T < 1 || s->H < 128 || s->I < 64 || s->E < 1 || s->E > 512 || s->k < 1 || s->k > s->E)
     return MOE_ERR_SHAPE;
   if (s->H % 128 || s->I % (fp8 ? 128 : 64)) return MOE_ERR_SHAPE;
@@ -188,6 +192,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   p->E = s->E + n_shared;   // experts in the weights and the index
   p->k = p->map.kk;         // assignments per token
   p->fp8 = s->mode == MOE_FP8_W8A8;
+  p->w8 = s->mode == MOE_W8A16;
   p->out_bf16 = s->out_dtype == MOE_OUT_BF16;
   p->bm = s->block_m ? s->block_m : auto_bm(p->T, p->k, p->E, p->fp8);
   const int64_t tc = tiles_cap_of(p->T, p->k, p->E, p->bm);
@@ -201,8 +206,10 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   p->mt2 = s->H / 128;
   // Large token tiles (prefill) are L2-bandwidth bound with one 128-row
   // weight tile per unit: pair two weight tiles per unit there.
-  p->me1 = (!p->fp8 && p->bm >= 128 && p->mt1 % 2 == 0 && !(o && o->single_weight_tile)) ? 2 : 1;
-  p->me2 = (!p->fp8 && p->bm >= 128 && p->mt2 % 2 == 0 && !(o && o->single_weight_tile)) ? 2 : 1;
+  p->me1 = (!p->fp8 && !p->w8 && p->bm >= 128 && p->mt1 % 2 == 0 &&
+             !(o && o->single_weight_tile)) ? 2 : 1;
+  p->me2 = (!p->fp8 && !p->w8 && p->bm >= 128 && p->mt2 % 2 == 0 &&
+             !(o && o->single_weight_tile)) ? 2 : 1;
   const int est = est_tiles(p->T, p->k, p->E, p->bm, p->tiles_cap);
   choose_split(p->mt1 / p->me1, p->kt1, est, p->bm, &p->s1, &p->kts1);
   choose_split(p->mt2 / p->me2, p->kt2, est, p->bm, &p->s2, &p->kts2);
@@ -220,7 +227,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   // kernel).  Measured no faster than the index kernel, so not the default.
   {
     const int tk = p->T * p->k;
-    bool fits = tk <= kSmemIndexMaxAssignments && o && o->smem_index;
+    bool fits = tk <= kSmemIndexMaxAssignments && o && o->smem_index && !p->w8;
     for (int bsrc : {static_cast<int>(kGather), static_cast<int>(kDirect)}) {
       const size_t need = gemm_smem_bytes(p->fp8, p->bm, bsrc) +
                           gemm_index_smem_bytes(gemm_warps(p->fp8, p->bm, bsrc), p->E, tk, p->rows_cap,
@@ -345,16 +352,18 @@ bool make_map_2d(CUtensorMap* m, const void* base, int esize, uint64_t cols, uin
 
 // 3-D K-major map [experts][rows][cols], box {128 bytes of K, box_rows, 1}.
 bool make_map_3d(CUtensorMap* m, const void* base, int esize, uint64_t cols, uint64_t rows,
-                 uint64_t experts, uint32_t box_rows) {
+                 uint64_t experts, uint32_t box_rows, bool raw64 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {cols, rows, experts};
   const cuuint64_t strides[2] = {cols * esize, cols * rows * esize};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), box_rows, 1};
+  // raw64: 64-byte rows, no swizzle (e4m3 weight stages of the w8a16 GEMM)
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>((raw64 ? 64 : 128) / esize), box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            raw64 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -363,17 +372,18 @@ bool make_map_3d(CUtensorMap* m, const void* base, int esize, uint64_t cols, uin
 // {128 bytes, 16, 2, 4, 1} brings 64 gate rows and their 64 up rows,
 // interleaved 16 by 16, in a single copy.
 bool make_map_gateup(CUtensorMap* m, const void* base, int esize, uint64_t cols, uint64_t I,
-                     uint64_t experts) {
+                     uint64_t experts, bool raw64 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
   const uint64_t row = cols * esize;
   const cuuint64_t dims[5] = {cols, 16, 2, I / 16, experts};
   const cuuint64_t strides[4] = {row, I * row, 16 * row, 2 * I * row};
-  const cuuint32_t box[5] = {static_cast<cuuint32_t>(128 / esize), 16, 2, 4, 1};
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>((raw64 ? 64 : 128) / esize), 16, 2, 4, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            raw64 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -498,11 +508,11 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
                         void* out, void* workspace, size_t ws_bytes, int32_t* dev_status,
                         void* stream, const moe_forward_opts* opts, const RouteCall* rc) {
   if (!x || !w13 || !w2 || !topk_ids || !topk_w || !out || !workspace) return MOE_ERR_ARG;
-  if (p.fp8 && (!scales || !scales->w13_scale || !scales->w2_scale)) return MOE_ERR_ARG;
+  if ((p.fp8 || p.w8) && (!scales || !scales->w13_scale || !scales->w2_scale)) return MOE_ERR_ARG;
   if (!aligned(x, 16) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) ||
       !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(workspace, 256))
     return MOE_ERR_ALIGN;
-  if (p.fp8 && (!aligned(scales->w13_scale, 4) || !aligned(scales->w2_scale, 4)))
+  if ((p.fp8 || p.w8) && (!aligned(scales->w13_scale, 4) || !aligned(scales->w2_scale, 4)))
     return MOE_ERR_ALIGN;
   if (ws_bytes < p.total) return MOE_ERR_WORKSPACE;
 
@@ -521,13 +531,14 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   void* A = at(kOffA);
   float* As = reinterpret_cast<float*>(at(kOffAs));
   float* Y = reinterpret_cast<float*>(at(kOffY));
-  const int esize = p.fp8 ? 1 : 2;
+  const int esize = p.fp8 ? 1 : 2;              // activation bytes
+  const int wsize = (p.fp8 || p.w8) ? 1 : 2;    // weight bytes
   const int tk = p.T * p.k;
 
   CUtensorMap tmW13, tmX, tmW2, tmA;
-  if (!make_map_gateup(&tmW13, w13, esize, p.H, p.I, p.E) ||
+  if (!make_map_gateup(&tmW13, w13, wsize, p.H, p.I, p.E, p.w8) ||
       !make_map_2d(&tmX, p.fp8 ? static_cast<const void*>(xq) : x, esize, p.H, p.T, 1) ||
-      !make_map_3d(&tmW2, w2, esize, p.I, p.H, p.E, 128) ||
+      !make_map_3d(&tmW2, w2, wsize, p.I, p.H, p.E, 128, p.w8) ||
       !make_map_2d(&tmA, A, esize, p.I, p.rows_cap, p.bm))
     return MOE_ERR_CUDA;
 
@@ -640,7 +651,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.b_row_bytes = p.H * esize;
   g1.topk = p.k;
   g1.sentinel = tk;
-  g1.w_scale = p.fp8 ? scales->w13_scale : nullptr;
+  g1.w_scale = (p.fp8 || p.w8) ? scales->w13_scale : nullptr;
   // per-token scales where no index-ordered copy was written
   const bool by_token = p.smem_index || p.route_fused;
   g1.b_scale = p.fp8 ? (by_token ? xs : xs_rows) : nullptr;
@@ -659,8 +670,9 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.rows_cap = p.rows_cap;
   g1.dev_status = dev_status;
   const int units1 = g1.m_tiles * p.s1 * p.tiles_cap;
-  e = launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13, tmX, g1,
-                  p.me1);
+  e = p.w8 ? launch_gemm_w8(p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13, tmX, g1)
+           : launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13,
+                         tmX, g1, p.me1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   record(opts, 3, s);
@@ -683,7 +695,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g2.sorted_ids = ip.sorted_ids;
   g2.topk = p.k;
   g2.sentinel = tk;
-  g2.w_scale = p.fp8 ? scales->w2_scale : nullptr;
+  g2.w_scale = (p.fp8 || p.w8) ? scales->w2_scale : nullptr;
   g2.b_scale = p.fp8 ? As : nullptr;
   g2.smem_index = p.smem_index;
   g2.topk_ids = topk_ids;
@@ -696,8 +708,9 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g2.rows_cap = p.rows_cap;
   g2.dev_status = dev_status;
   const int units2 = g2.m_tiles * p.s2 * p.tiles_cap;
-  e = launch_gemm(p.fp8, p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2,
-                  p.me2);
+  e = p.w8 ? launch_gemm_w8(p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2)
+           : launch_gemm(p.fp8, p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2,
+                         p.me2);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   record(opts, 5, s);

@@ -43,11 +43,15 @@ def assert_layer_close(got, ref, mode: str, what: str = ""):
     return rel_l2, max_abs
 
 
-def oracle_layer(wl, sel=None, topk_ids=None, topk_w=None, return_act=False):
-    """Oracle output rows for a workloads.Workload (inputs copied to the host)."""
+def oracle_layer(wl, sel=None, topk_ids=None, topk_w=None, return_act=False, w8a16=False):
+    """Oracle output rows for a workloads.Workload (inputs copied to the host).
+    w8a16: the FP8 workload's weights with bf16 activations."""
     import oracle
     ids = (wl.topk_ids if topk_ids is None else topk_ids).cpu().numpy()
     w = (wl.topk_w if topk_w is None else topk_w).cpu().numpy()
+    if w8a16:
+        return oracle.moe_w8a16(bits16(wl.x), u8(wl.w13q), wl.w13s.cpu().numpy(), u8(wl.w2q),
+                                wl.w2s.cpu().numpy(), ids, w, sel)
     if wl.mode == "bf16":
         return oracle.moe_bf16(bits16(wl.x), bits16(wl.w13), bits16(wl.w2), ids, w, sel)
     xq, xs = oracle.quant_x(bits16(wl.x))
@@ -83,7 +87,7 @@ def check_topk(ids_gpu, ids_ref, scores_ref, k, scores_gpu=None):
         assert s[k - 1] - s[k] < TIE_GAP, (t, ids_gpu[t], ids_ref[t])
 
 
-def oracle_layer_sampled(wl, ids, w, sel):
+def oracle_layer_sampled(wl, ids, w, sel, w8a16=False):
     """Oracle rows of the tokens `sel` only.  A token's output depends on its
     own x row, ids, weights and the experts it routes to, so the oracle is
     fed just those: the sampled x rows and the used experts' weights, with
@@ -98,6 +102,9 @@ def oracle_layer_sampled(wl, ids, w, sel):
     rows = torch.from_numpy(sel).long().to(wl.x.device)
     ex = torch.from_numpy(used).long().to(wl.x.device)
     x = bits16(wl.x[rows])
+    if w8a16:
+        return oracle.moe_w8a16(x, u8(wl.w13q[ex]), wl.w13s[ex].cpu().numpy(), u8(wl.w2q[ex]),
+                                wl.w2s[ex].cpu().numpy(), ids_c, w_s)
     if wl.mode == "bf16":
         return oracle.moe_bf16(x, bits16(wl.w13[ex]), bits16(wl.w2[ex]), ids_c, w_s)
     xq, xs = oracle.quant_x(x)
