@@ -88,7 +88,12 @@ struct GemmShape {
   static constexpr int kGatherThreads = 32 * kGatherWarps;
   static constexpr int kThreads = kRoleThreads + kGatherThreads;
   static constexpr int kWarps = kThreads / 32;
-  static constexpr int kRowsPerGatherThread = kGatherWarps ? BN / (4 * kGatherWarps) : 1;
+  // Prefill tiles (bf16): the TMA warp also gathers the first kTmaRows token
+  // rows of every stage with the TMA's four-row gather, next to the cp.async
+  // warps' share — two gather engines instead of one.
+  static constexpr int kTmaRows = (BSRC == kGather && BN >= 128 && !FP8) ? 32 : 0;
+  static constexpr int kRowsPerGatherThread =
+      kGatherWarps ? (BN - kTmaRows) / (4 * kGatherWarps) : 1;
   static constexpr int kBBytes = BN * kKBytes;
   // TMEM accumulator buffers (each ME x BN columns): two per-unit buffers
   // for bf16 where they fit; for FP8 every 128-wide K block is its own
@@ -297,7 +302,9 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     long issued = 0;
     bool ok = true;
     constexpr uint32_t bytes =
-        S::kAStage + (BSRC == kGather ? 0u : static_cast<uint32_t>(S::kBBytes));
+        S::kAStage + (BSRC == kGather ? static_cast<uint32_t>(S::kTmaRows * kKBytes)
+                                      : static_cast<uint32_t>(S::kBBytes));
+    int tma_tok[S::kTmaRows > 0 ? S::kTmaRows : 1];   // token rows this warp gathers (lane 0)
     bool b_now = !(early && BSRC == kDirect);
     int deferred = 0;
     auto flush_deferred = [&]() {
@@ -317,6 +324,14 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); ok && it.valid(); it.advance()) {
       if (*abort_flag) break;
       const WorkUnit w = it.take(p);
+      if constexpr (S::kTmaRows > 0) {
+        // lane l looks up row l's token; padding rows read token 0 (their
+        // columns are never stored)
+        const int tl = lane < w.rows ? assignment_token(row_assign(w.row0 + lane), p) : -1;
+        const int tok = tl < 0 ? 0 : tl;
+#pragma unroll
+        for (int j = 0; j < S::kTmaRows; ++j) tma_tok[j] = __shfl_sync(0xffffffffu, tok, j);
+      }
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u)) {
           report_timeout(p, abort_flag);
@@ -340,6 +355,13 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           }
           if (BSRC != kGather && b_now)
             tma_load_2d(sB + stage * S::kBBytes, &tmB, full, kc, w.row0);
+          if constexpr (S::kTmaRows > 0) {
+#pragma unroll
+            for (int g = 0; g < S::kTmaRows / 4; ++g)
+              tma_gather4(sB + stage * S::kBBytes + g * 4 * kKBytes, &tmB, full, kc,
+                          tma_tok[4 * g], tma_tok[4 * g + 1], tma_tok[4 * g + 2],
+                          tma_tok[4 * g + 3]);
+          }
         }
         __syncwarp();
         ++issued;
@@ -681,7 +703,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       if (!tok_ready) {
 #pragma unroll
         for (int i = 0; i < kR; ++i) {
-          const int n = r0 + kRowStep * i;
+          const int n = S::kTmaRows + r0 + kRowStep * i;
           tok[i] = n < w.rows ? assignment_token(row_assign(w.row0 + n), p) : -1;
         }
       }
@@ -703,7 +725,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
         const uint8_t* src = rows + static_cast<size_t>(kt) * kKBytes;
 #pragma unroll
         for (int i = 0; i < kR; ++i) {
-          const int n = r0 + kRowStep * i;
+          const int n = S::kTmaRows + r0 + kRowStep * i;
           if (tok[i] >= 0)
             cp_async_16(b_dst + n * kKBytes + ((c ^ (n & 7)) << 4),
                         src + static_cast<size_t>(tok[i]) * p.b_row_bytes);
@@ -719,7 +741,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
             const int4 tn = it.next;
 #pragma unroll
             for (int i = 0; i < kR; ++i) {
-              const int n = r0 + kRowStep * i;
+              const int n = S::kTmaRows + r0 + kRowStep * i;
               tok_next[i] = n < tn.z ? row_assign(tn.y + n) : -1;   // assignment for now
             }
           }

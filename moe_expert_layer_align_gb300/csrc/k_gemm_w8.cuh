@@ -27,7 +27,7 @@ namespace moe {
 constexpr int kW8RawA = kTileM * 64;    // e4m3 weight stage: 128 rows x 64 K
 
 // Converted slots (6 for narrow tiles measured no faster than 3).
-__host__ __device__ constexpr int w8_conv_slots(int bn) { return bn > 0 ? 3 : 3; }
+__host__ __device__ constexpr int w8_conv_slots(int) { return 3; }
 
 __host__ __device__ constexpr int w8_raw_slots(int bn, int bsrc) {
   return ((196608 - w8_conv_slots(bn) * (kABytes + bn * kKBytes)) /

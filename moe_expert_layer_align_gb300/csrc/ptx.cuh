@@ -103,6 +103,18 @@ MOE_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Four rows r0..r3 of a 2-D tensor map whose box is one row high, at column
+// c0, into four consecutive 128-byte rows of shared memory (swizzled by the
+// map as any tiled load).
+MOE_DEV void tma_gather4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int r0,
+                         int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 MOE_DEV void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
