@@ -80,7 +80,7 @@ struct GemmShape {
   // with wide token tiles, where the per-K-block promotion is the busiest
   // role; the second warp of a quadrant then takes the upper half of the
   // columns.
-  static constexpr int kEpiWarps = (FP8 && BN >= 64) ? 8 : 4;
+  static constexpr int kEpiWarps = (FP8 && BN >= 64) ? 8 : 4;   // 16 measured slower (spills)
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kRoleThreads = 64 + kEpiThreads;   // + TMA and MMA warps
   // token-row gather warps (gathered operand only) and block size
