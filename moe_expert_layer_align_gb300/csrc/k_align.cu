@@ -11,18 +11,24 @@
 
 namespace moe {
 
-constexpr int kAlignThreads = 1024;
+constexpr int kAlignThreads = 1024;        // block size for large batches (and the scan kernel)
 constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kAlignMaxStagedIds = 32768;  // ids staged in shared memory up to this many
+
+// Block size of the one-CTA build (128 or 256 threads for small batches
+// measured slower: the per-expert loops get longer than the barriers get
+// cheaper).
+inline int align_threads(int) { return kAlignThreads; }
 
 __global__ void __launch_bounds__(kAlignThreads)
     moe_align_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int tiles_cap,
                      IndexPtrs idx, int32_t* dev_status, int stage_ids, IdMap map) {
   extern __shared__ int32_t sm[];
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
   IndexScratch sc;
-  sc.carve(sm, kAlignWarps, E, map.Eg != 0);
+  sc.carve(sm, nwarps, E, map.Eg != 0);
   // [T*k] staged ids (optional), 16-byte aligned for vector stores
-  int32_t* sids = sm + ((IndexScratch::words(kAlignWarps, E) + 3) & ~static_cast<size_t>(3));
+  int32_t* sids = sm + ((IndexScratch::words(nwarps, E) + 3) & ~static_cast<size_t>(3));
 
   const int tid = threadIdx.x;
   const int tk = T * k;
@@ -33,7 +39,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   if (tid == 0 && dev_status) *dev_status = 0;
   if (stage_ids && !map.plain()) {
     // shared experts / expert parallelism: stage the index experts
-    for (int i = tid; i < tk; i += kAlignThreads) sids[i] = mapped_id(ids, i, map);
+    for (int i = tid; i < tk; i += nthreads) sids[i] = mapped_id(ids, i, map);
   } else if (stage_ids) {
     // 16-byte loads, several in flight per thread (one dependent load per
     // iteration made this loop the kernel's cost at 32K assignments)
@@ -41,14 +47,14 @@ __global__ void __launch_bounds__(kAlignThreads)
     const int4* ids4 = reinterpret_cast<const int4*>(ids);
     int4* s4 = reinterpret_cast<int4*>(sids);
 #pragma unroll 8
-    for (int i = tid; i < n4; i += kAlignThreads) s4[i] = __ldg(ids4 + i);
-    for (int i = 4 * n4 + tid; i < tk; i += kAlignThreads) sids[i] = __ldg(ids + i);
+    for (int i = tid; i < n4; i += nthreads) s4[i] = __ldg(ids4 + i);
+    for (int i = 4 * n4 + tid; i < tk; i += nthreads) sids[i] = __ldg(ids + i);
   }
   const int32_t* src = stage_ids ? sids : ids;
 
   index_count_and_scan(src, tk, E, bm, sc);
-  for (int e = tid; e < E; e += kAlignThreads) idx.counts[e] = sc.tot[e];
-  for (int e = tid; e <= E; e += kAlignThreads) idx.offsets[e] = sc.offs[e];
+  for (int e = tid; e < E; e += nthreads) idx.counts[e] = sc.tot[e];
+  for (int e = tid; e <= E; e += nthreads) idx.offsets[e] = sc.offs[e];
   index_scatter(
       src, tk, E, sc,
       [&](int pos, int a) {
@@ -58,7 +64,7 @@ __global__ void __launch_bounds__(kAlignThreads)
       [&](int a) { idx.inv_pos[a] = -1; });
   index_pads(E, tiles_cap * bm, sc, [&](int pos) { idx.sorted_ids[pos] = tk; });
   if (tid == 0) *idx.num_tiles = sc.offs[E] / bm;
-  for (int q = tid; q < tiles_cap; q += kAlignThreads) {
+  for (int q = tid; q < tiles_cap; q += nthreads) {
     const int4 t = index_tile(q, E, bm, sc);
     idx.tile_expert[q] = t.x;
     reinterpret_cast<int4*>(idx.tiles)[q] = t;
@@ -73,8 +79,9 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int ti
   const int tk = T * k;
   const int stage_ids = tk <= kAlignMaxStagedIds ? 1 : 0;
   if (!stage_ids && !map.plain()) return cudaErrorInvalidValue;   // mapped ids are staged
+  const int threads = align_threads(tk);
   const size_t smem =
-      sizeof(int32_t) * (((IndexScratch::words(kAlignWarps, E) + 3) & ~static_cast<size_t>(3)) +
+      sizeof(int32_t) * (((IndexScratch::words(threads / 32, E) + 3) & ~static_cast<size_t>(3)) +
                          (stage_ids ? tk : 0));
   static int configured[64] = {0};
   int dev = 0;
@@ -86,7 +93,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int ti
     if (err != cudaSuccess) return err;
     configured[dev] = 1;
   }
-  return launch_kernel(moe_align_kernel, dim3(1), dim3(kAlignThreads), smem, st, pdl, ids, T, k, E,
+  return launch_kernel(moe_align_kernel, dim3(1), dim3(threads), smem, st, pdl, ids, T, k, E,
                        bm, tiles_cap, idx, dev_status, stage_ids, map);
 }
 
