@@ -11,14 +11,12 @@
 
 namespace moe {
 
-constexpr int kAlignThreads = 1024;        // block size for large batches (and the scan kernel)
+// Block size of the one-CTA build and of the scan kernel.  (128 or 256
+// threads for small batches measured slower: the per-expert loops get longer
+// than the barriers get cheaper.)
+constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kAlignMaxStagedIds = 32768;  // ids staged in shared memory up to this many
-
-// Block size of the one-CTA build (128 or 256 threads for small batches
-// measured slower: the per-expert loops get longer than the barriers get
-// cheaper).
-inline int align_threads(int) { return kAlignThreads; }
 
 __global__ void __launch_bounds__(kAlignThreads)
     moe_align_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int tiles_cap,
@@ -79,7 +77,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int ti
   const int tk = T * k;
   const int stage_ids = tk <= kAlignMaxStagedIds ? 1 : 0;
   if (!stage_ids && !map.plain()) return cudaErrorInvalidValue;   // mapped ids are staged
-  const int threads = align_threads(tk);
+  const int threads = kAlignThreads;
   const size_t smem =
       sizeof(int32_t) * (((IndexScratch::words(threads / 32, E) + 3) & ~static_cast<size_t>(3)) +
                          (stage_ids ? tk : 0));

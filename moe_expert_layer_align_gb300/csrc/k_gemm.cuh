@@ -40,12 +40,14 @@
 // the task map from global memory.
 //
 // Warp roles: warp 0 issues the TMA loads (weights; the token tile too when
-// its rows are contiguous), warp 1 (one thread) issues MMAs, warps 2..5 drain
-// TMEM, and for the gathered token operand warps 6.. copy the token rows with
-// 16-byte cp.async into the 128-byte-swizzled layout, each thread arriving on
-// the stage barrier when its copies land.  (TMA's four-row gather was tried
-// first: at one op per ~40 ns it capped the prefill Gate-Up at a third of the
-// rate of a dense load of the same bytes.)  With the accumulator in TMEM
+// its rows are contiguous), warp 1 (one thread) issues MMAs, the epilogue
+// warps (4, or 8 for FP8 with 64/128-row tiles) drain TMEM, and for the
+// gathered token operand the last 1-2 warps copy the token rows with 16-byte
+// cp.async into the 128-byte-swizzled layout, each thread arriving on the
+// stage barrier when its copies land.  TMA's four-row gather alone (one op
+// per ~40 ns) capped the prefill Gate-Up at a third of the rate of a dense
+// load of the same bytes; for 128-row bf16 tiles the TMA warp gathers 32 of
+// the rows that way next to the cp.async warps.  With the accumulator in TMEM
 // instead of registers this split costs no registers, so the Hopper argument
 // for one warp group doing everything ("occupancy first, no warp
 // specialisation") does not carry over.  Every wait is bounded
