@@ -86,7 +86,7 @@ struct GemmShape {
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kRoleThreads = 64 + kEpiThreads;   // + TMA and MMA warps
   // token-row gather warps (gathered operand only) and block size
-  static constexpr int kGatherWarps = BSRC == kGather ? (BN >= 128 ? 2 : 1) : 0;
+  static constexpr int kGatherWarps = BSRC == kGather ? (BN >= 64 ? 2 : 1) : 0;
   static constexpr int kGatherThreads = 32 * kGatherWarps;
   static constexpr int kThreads = kRoleThreads + kGatherThreads;
   static constexpr int kWarps = kThreads / 32;
