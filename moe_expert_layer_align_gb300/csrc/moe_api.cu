@@ -211,7 +211,15 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   p->me2 = (!p->fp8 && !p->w8 && p->bm >= 128 && p->mt2 % 2 == 0 &&
              !(o && o->single_weight_tile)) ? 2 : 1;
   const int est = est_tiles(p->T, p->k, p->E, p->bm, p->tiles_cap);
-  choose_split(p->mt1 / p->me1, p->kt1, est, p->bm, &p->s1, &p->kts1);
+  if (!p->fp8 && !(o && o->separate_act)) {
+    // bf16 activations: an unsplit Gate-Up applies SiLU-and-mul in its
+    // epilogue; measured faster than any split (whose partials then need the
+    // separate activation stage) at every decode size tried
+    p->s1 = 1;
+    p->kts1 = p->kt1;
+  } else {
+    choose_split(p->mt1 / p->me1, p->kt1, est, p->bm, &p->s1, &p->kts1);
+  }
   choose_split(p->mt2 / p->me2, p->kt2, est, p->bm, &p->s2, &p->kts2);
   if (o && o->split_gateup > 0) {
     p->kts1 = (p->kt1 + o->split_gateup - 1) / o->split_gateup;
