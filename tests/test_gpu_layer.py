@@ -231,3 +231,17 @@ def test_index_over_chunks_is_bitwise_the_single_block_index(zipf):
     for n in ("counts", "offsets", "sorted_ids", "tile_expert", "tiles", "inv_pos", "num_tiles"):
         np.testing.assert_array_equal(v[n].cpu().numpy().reshape(-1), ref[n].reshape(-1), n)
     assert_layer_close(got, oracle_layer(wl, topk_ids=ids.cpu()), "bf16", "chunked index")
+
+
+@pytest.mark.parametrize("cfg,T,kw", [
+    (3, 40, dict(H=256, I=128, E=512, k=8)),     # the largest expert count
+    (2, 30, dict(H=256, I=128, E=8, k=8)),       # every token picks every expert
+    (2, 17, dict(H=256, I=128, E=1, k=1)),       # one expert: a dense SwiGLU MLP
+    (2, 33, dict(H=128, I=64, E=4, k=2)),        # the smallest H and I of the bf16 layer
+    (4, 33, dict(H=128, I=128, E=4, k=2)),       # ... and of the FP8 layer
+    (3, 5000, dict(H=128, I=64, E=4, k=2)),      # many tiles per expert, chunked index
+])
+def test_shape_limits(cfg, T, kw):
+    wl = small(cfg, T, **kw)
+    got = run_layer(wl).float().cpu().numpy()
+    assert_layer_close(got, oracle_layer(wl), wl.mode, f"cfg{cfg} T={T} {kw}")
