@@ -83,6 +83,13 @@ struct GemmShape {
   // role; the second warp of a quadrant then takes the upper half of the
   // columns.
   static constexpr int kEpiWarps = (FP8 && BN >= 64) ? 8 : 4;   // 16 measured slower (spills)
+  // FP8 with 128-row token tiles runs token-major: the token tile is the
+  // MMA's M side and the weight tile its N side.  A TMEM lane is then one
+  // token, and both block scales of its K-block partial are per-thread
+  // constants (the token's, and the weight block's: one for Down, gate and
+  // up for Gate-Up), so the promotion is one packed FMA per two values with
+  // no per-column scale loads.  (Swap-AB needs a per-column token scale.)
+  static constexpr bool kTokM = FP8 && BN == 128;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kRoleThreads = 64 + kEpiThreads;   // + TMA and MMA warps
   // token-row gather warps (gathered operand only) and block size
@@ -397,7 +404,8 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
         // The MMA's N is the tile's valid rows rounded up to 16: columns of
         // padding rows are never computed (nor stored), so a wide token tile
         // costs a narrow one's MMA time when few of its rows are valid.
-        const int n_eff = min(BN, max(16, (w.rows + 15) & ~15));
+        // (Token-major tiles keep the full 128-row M: M is 64 or 128.)
+        const int n_eff = S::kTokM ? BN : min(BN, max(16, (w.rows + 15) & ~15));
         const uint32_t idesc = (S::kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(n_eff >> 3) << 17);
         if (!FP8) {
           if (!mbar_wait(bar_acce + 8 * ab, aph ^ 1u)) {
@@ -432,7 +440,9 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {  // 4 MMAs of 32 bytes of K each
               const uint32_t acc = FP8 ? (k > 0) : (kt > w.kt0 || k > 0);
-              if (FP8)
+              if (S::kTokM)   // tokens are the M side, weight rows the N side
+                mma_e4m3(d, bdesc + 2 * k, adesc + 2 * k, idesc, acc);
+              else if (FP8)
                 mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
               else
                 mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, acc);
@@ -564,6 +574,98 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
         if (++ab == S::kAccBufs) {
           ab = 0;
           aph ^= 1u;
+        }
+      } else if (S::kTokM) {
+        // Token-major FP8 tile: lane n of the accumulator is token row n of
+        // the tile, column j weight row j of the 128-row tile (Gate-Up: rows
+        // 32q..32q+15 gate, 32q+16..32q+31 up, as the weight map stages
+        // them).  Per K block a thread needs its token's scale and one
+        // weight-block scale per 16 columns, all fetched three blocks ahead.
+        const int n = qd * 32 + lane;
+        const bool live = qd * 32 < w.rows;   // warp-uniform: any valid row
+        const int KB = p.kt_total;
+        int srow = -1;
+        if (n < w.rows)
+          srow = p.scale_by_token ? assignment_token(row_assign(w.row0 + n), p) : w.row0 + n;
+        const float* bsp = srow >= 0 ? p.b_scale + static_cast<size_t>(srow) * KB : nullptr;
+        const size_t wblk = static_cast<size_t>(w.e) * (p.M >> 7);
+        const float* wsg = p.w_scale +
+            (wblk + (BSRC == kGather ? (w.mt * 64) >> 7 : w.mt)) * KB;   // gate (or only)
+        const float* wsu = p.w_scale +
+            (wblk + (BSRC == kGather ? (p.I + w.mt * 64) >> 7 : w.mt)) * KB;   // up
+        auto sx_at = [&](int kt) { return (bsp && kt < w.kt1) ? __ldg(bsp + kt) : 0.f; };
+        auto sg_at = [&](int kt) { return kt < w.kt1 ? __ldg(wsg + kt) : 0.f; };
+        auto su_at = [&](int kt) { return kt < w.kt1 ? __ldg(wsu + kt) : 0.f; };
+        float sx0 = sx_at(w.kt0), sx1 = sx_at(w.kt0 + 1), sx2 = sx_at(w.kt0 + 2);
+        float sg0 = sg_at(w.kt0), sg1 = sg_at(w.kt0 + 1), sg2 = sg_at(w.kt0 + 2);
+        float su0 = su_at(w.kt0), su1 = su_at(w.kt0 + 1), su2 = su_at(w.kt0 + 2);
+        uint64_t acc2[kWarpCols / 2];
+#pragma unroll
+        for (int j = 0; j < kWarpCols / 2; ++j) acc2[j] = 0ull;
+        bool ok = true;
+        for (int kt = w.kt0; kt < w.kt1; ++kt) {
+          const float sg = sx0 * sg0, su = sx0 * su0;
+          sx0 = sx1, sx1 = sx2, sx2 = sx_at(kt + 3);
+          sg0 = sg1, sg1 = sg2, sg2 = sg_at(kt + 3);
+          su0 = su1, su1 = su2, su2 = su_at(kt + 3);
+          if (!mbar_wait(bar_accf + 8 * ab, aph)) {
+            report_timeout(p, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (live) {
+            uint32_t v[kWarpCols / 16][16];
+#pragma unroll
+            for (int g = 0; g < kWarpCols / 16; ++g)
+              tmem_ld16(t_lane + static_cast<uint32_t>(ab * BN + c_base + g * 16), v[g]);
+            tmem_ld_wait();
+            const uint64_t s_g = pack_f32x2(sg, sg), s_u = pack_f32x2(su, su);
+#pragma unroll
+            for (int g = 0; g < kWarpCols / 16; ++g) {
+              tmem_ld_bind(v[g]);
+              const bool gate = BSRC != kGather || (((c_base + g * 16) & 31) < 16);
+              const uint64_t sc = gate ? s_g : s_u;
+#pragma unroll
+              for (int h = 0; h < 8; ++h)
+                acc2[g * 8 + h] = fma_f32x2(pack_u32x2(v[g][2 * h], v[g][2 * h + 1]), sc,
+                                            acc2[g * 8 + h]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acce + 8 * ab);
+          if (++ab == S::kAccBufs) {
+            ab = 0;
+            aph ^= 1u;
+          }
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        if (n < w.rows) {
+          float* orow = p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0 + n) * p.M;
+#pragma unroll
+          for (int g = 0; g < kWarpCols / 16; ++g) {
+            const int j0 = c_base + g * 16;
+            int col0 = w.mt * kTileM + j0;
+            if (BSRC == kGather) {
+              const int feat = w.mt * 64 + 16 * (j0 >> 5);
+              col0 = (j0 & 31) < 16 ? feat : p.I + feat;
+            }
+            if (col0 + 16 <= p.M) {
+              float4* dst = reinterpret_cast<float4*>(orow + col0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                float4 o;
+                unpack_f32x2(acc2[g * 8 + 2 * q], o.x, o.y);
+                unpack_f32x2(acc2[g * 8 + 2 * q + 1], o.z, o.w);
+                dst[q] = o;
+              }
+            }
+          }
         }
       } else {
         const int feat = w.mt * 64 + qd * 16 + (lane & 15);  // Gate-Up: this lane's channel
