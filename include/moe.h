@@ -154,6 +154,15 @@ typedef struct {
    * Qwen3-shaped FP8 layer at T=64 (its last CTA builds the index alone after
    * every token's top-k), so off by default. */
   int32_t fuse_routing;
+  /* Order in which each persistent GEMM walks its work units (weight tile x
+   * split x token tile).  0: planner.  1: weight-tile-major (the units of
+   * one weight tile over all token tiles are consecutive).  2: token-tile-
+   * major (the units of one token tile are consecutive, so an expert's few
+   * token tiles read each weight tile at about the same time and the second
+   * read hits L2).  The planner takes 2 when an expert's expected token
+   * tiles times its units per token tile fit one wave of CTAs, else 1.
+   * Results do not depend on it. */
+  int32_t unit_order;
 } moe_forward_opts;
 
 /* Options of moe_align_ex: the same shared-expert and expert-parallel mapping
@@ -175,6 +184,7 @@ typedef struct {
                           Gate-Up writes it out (no separate index kernel) */
   int32_t weight_tiles_per_unit;  /* Gate-Up | Down << 8 (1 or 2 each) */
   int32_t route_fused;  /* moe_forward_routed: router top-k, x-quant and index in one grid */
+  int32_t unit_order;   /* Gate-Up | Down << 8: 1 weight-tile-major, 2 token-tile-major */
   size_t off_counts, off_offsets, off_sorted_ids, off_tile_expert, off_tiles,
       off_inv_pos, off_num_tiles;
   size_t off_index_scratch; /* per-chunk histograms of the split index build */

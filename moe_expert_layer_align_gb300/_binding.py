@@ -47,7 +47,8 @@ class moe_forward_opts(ctypes.Structure):
                 ("grid_ctas", _i32), ("stage_events", _vp * 8), ("separate_act", _i32),
                 ("smem_index", _i32), ("single_weight_tile", _i32),
                 ("num_shared_experts", _i32), ("shared_expert_weight", ctypes.c_float),
-                ("ep_first_expert", _i32), ("ep_num_experts", _i32), ("fuse_routing", _i32)]
+                ("ep_first_expert", _i32), ("ep_num_experts", _i32), ("fuse_routing", _i32),
+                ("unit_order", _i32)]
 
 
 class moe_align_opts(ctypes.Structure):
@@ -58,7 +59,7 @@ class moe_workspace_layout(ctypes.Structure):
     _fields_ = [("block_m", _i32), ("tiles_cap", _i32), ("rows_cap", _i32),
                 ("split_gateup", _i32), ("split_down", _i32), ("grid_gateup", _i32),
                 ("grid_down", _i32), ("fused_act", _i32), ("smem_index", _i32),
-                ("weight_tiles_per_unit", _i32), ("route_fused", _i32)] + [
+                ("weight_tiles_per_unit", _i32), ("route_fused", _i32), ("unit_order", _i32)] + [
         (n, _sz) for n in ("off_counts", "off_offsets", "off_sorted_ids", "off_tile_expert",
                            "off_tiles", "off_inv_pos", "off_num_tiles", "off_index_scratch", "off_xq", "off_xs",
                            "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "off_router",
@@ -158,8 +159,10 @@ def moe_index_tiles_cap(T, k, E, block_m) -> int:
 def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
               stage_events=None, separate_act=False, smem_index=False,
               single_weight_tile=False, num_shared_experts=0, shared_expert_weight=0.0,
-              ep_first_expert=0, ep_num_experts=0, fuse_routing=False) -> moe_forward_opts:
+              ep_first_expert=0, ep_num_experts=0, fuse_routing=False,
+              unit_order=0) -> moe_forward_opts:
     o = moe_forward_opts()
+    o.unit_order = unit_order
     o.fuse_routing = int(fuse_routing)
     o.num_shared_experts = num_shared_experts
     o.shared_expert_weight = shared_expert_weight

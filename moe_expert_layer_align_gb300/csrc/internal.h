@@ -39,6 +39,7 @@ struct GemmParams {
   int splits;        // split-K count
   int kt_per_split;  // K tiles (128 bytes of K each) per split
   int kt_total;      // K tiles in total
+  int tile_major;    // unit order: 0 weight-tile-major, 1 token-tile-major
   const int32_t* tiles;      // [tiles_cap][4] task map (gather / direct)
   const int32_t* num_tiles;  // device scalar (gather / direct)
   const int32_t* sorted_ids; // gather: row -> assignment

@@ -151,9 +151,13 @@ struct WorkUnit {
   int mt, ks, e, row0, rows, kt0, kt1;
 };
 
-// Unit u = ((mt * splits + ks) * num_tiles + q): consecutive units share a
-// weight tile.  The task-map entry is the only memory read, so roles load
-// the next unit's entry while they work on the current one.
+// Unit u = ((mt * splits + ks) * num_tiles + q), weight-tile-major:
+// consecutive units share a weight tile; or, token-tile-major,
+// u = (q * m_tiles + mt) * splits + ks: consecutive units share a token tile,
+// and the few token tiles of an expert reach each of its weight tiles within
+// one wave of CTAs (the later reads hit L2).  The task-map entry is the only
+// memory read, so roles load the next unit's entry while they work on the
+// current one.
 template <int BN, int BSRC>
 __device__ __forceinline__ int4 load_tile(int q, const GemmParams& p, const int4* smem_tiles) {
   if (BSRC == kDense) return make_int4(0, q * BN, min(BN, p.dense_rows - q * BN), 0);
@@ -173,9 +177,13 @@ __device__ __forceinline__ int assignment_token(int a, const GemmParams& p) {
   return static_cast<unsigned>(a) < static_cast<unsigned>(p.T * p.topk) ? a / p.topk : -1;
 }
 
+__device__ __forceinline__ int unit_tile(int u, int num_tiles, const GemmParams& p) {
+  return p.tile_major ? u / (p.m_tiles * p.splits) : u % num_tiles;
+}
+
 __device__ __forceinline__ WorkUnit make_unit(int u, int num_tiles, int4 t, const GemmParams& p) {
   WorkUnit w;
-  const int r = u / num_tiles;
+  const int r = p.tile_major ? u % (p.m_tiles * p.splits) : u / num_tiles;
   w.ks = r % p.splits;
   w.mt = r / p.splits;
   w.e = t.x;
@@ -195,14 +203,14 @@ struct UnitIter {
   __device__ __forceinline__ UnitIter(int units_, int num_tiles_, const GemmParams& p,
                                       const int4* st)
       : u(blockIdx.x), units(units_), num_tiles(num_tiles_), smem_tiles(st) {
-    if (u < units) next = load_tile<BN, BSRC>(u % num_tiles, p, smem_tiles);
+    if (u < units) next = load_tile<BN, BSRC>(unit_tile(u, num_tiles, p), p, smem_tiles);
   }
   __device__ __forceinline__ bool valid() const { return u < units; }
   // The current unit; starts the load of the one after it.
   __device__ __forceinline__ WorkUnit take(const GemmParams& p) {
     const int4 t = next;
     const int un = u + gridDim.x;
-    if (un < units) next = load_tile<BN, BSRC>(un % num_tiles, p, smem_tiles);
+    if (un < units) next = load_tile<BN, BSRC>(unit_tile(un, num_tiles, p), p, smem_tiles);
     return make_unit(u, num_tiles, t, p);
   }
   __device__ __forceinline__ void advance() { u += gridDim.x; }

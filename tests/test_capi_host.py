@@ -170,3 +170,22 @@ def test_routed_plan():
             moe.moe_plan_routed(s, o)
     with pytest.raises(moe.MoeError):           # router E must be a multiple of 64
         moe.moe_plan_routed(moe.make_shape(64, 2048, 768, 100, 8))
+
+
+def test_unit_order_plan():
+    """Token-tile-major where an expert's token tiles x units per tile fit one
+    wave of CTAs; weight-tile-major for the Mixtral-shaped prefill Gate-Up
+    (four token tiles per expert, 112 units each); forced orders are kept;
+    anything else is rejected."""
+    mix = moe.make_shape(2048, 4096, 14336, 8, 2, 0)
+    L = moe.moe_plan(mix)
+    assert (L.unit_order & 255, L.unit_order >> 8) == (1, 2)
+    qwen = moe.make_shape(4096, 2048, 768, 128, 8, 0)
+    assert moe.moe_plan(qwen).unit_order == 2 | (2 << 8)
+    ds = moe.make_shape(4096, 7168, 2048, 256, 8, 0, True)
+    assert moe.moe_plan(ds).unit_order == 2 | (2 << 8)
+    for order in (1, 2):
+        assert moe.moe_plan(mix, moe.make_opts(unit_order=order)).unit_order == order | (order << 8)
+    for bad in (-1, 3):
+        with pytest.raises(moe.MoeError):
+            moe.moe_plan(mix, moe.make_opts(unit_order=bad))

@@ -245,3 +245,21 @@ def test_shape_limits(cfg, T, kw):
     wl = small(cfg, T, **kw)
     got = run_layer(wl).float().cpu().numpy()
     assert_layer_close(got, oracle_layer(wl), wl.mode, f"cfg{cfg} T={T} {kw}")
+
+
+@pytest.mark.parametrize("cfg,T,bm,s2", [(2, 300, 64, 0), (2, 700, 128, 2), (4, 600, 128, 0),
+                                         (4, 200, 16, 3), (3, 900, 32, 0)])
+def test_unit_orders_are_bitwise_equal(cfg, T, bm, s2):
+    """Both walks over the work units (weight-tile-major, token-tile-major)
+    compute every output element in the same unit with the same arithmetic,
+    so the layer outputs are bitwise equal, and equal to the oracle's within
+    tolerance.  Several token tiles per expert, ragged tails, forced split."""
+    import moe_expert_layer_align_gb300 as moe
+    kw = dict(H=512, I=256, E=8) if cfg != 3 else dict(H=256, I=128, E=16)
+    wl = small(cfg, T, **kw)
+    outs = []
+    for order in (1, 2):
+        opts = moe.make_opts(split_down=s2, unit_order=order)
+        outs.append(run_layer(wl, block_m=bm, opts=opts).float().cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])
+    assert_layer_close(outs[1], oracle_layer(wl), wl.mode, f"cfg{cfg} T={T} bm={bm}")
