@@ -11,46 +11,79 @@
 namespace moe {
 
 // ---------------------------------------------------------------- x quant
-// x bf16 [T][H] -> xq e4m3 [T][H], xs [T][H/128]; one warp per group.  The
-// scales are also written to the index rows that hold the token's
-// assignments (xs_rows[inv_pos[t*k+j]]), so the Gate-Up epilogue reads them
-// by row without going through the index.
-__global__ void __launch_bounds__(128) moe_quant_x_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          int T, int H, int k,
-                                                          const int32_t* __restrict__ inv_pos,
-                                                          uint8_t* __restrict__ xq,
-                                                          float* __restrict__ xs,
-                                                          float* __restrict__ xs_rows,
-                                                          int rows_cap) {
+// x bf16 [T][H] -> xq e4m3 [T][H], xs [T][H/128].  The scales are also
+// written to the index rows that hold the token's assignments
+// (xs_rows[inv_pos[t*k+j]]), so the Gate-Up epilogue reads them by row
+// without going through the index.
+//
+// Block (t, b) quantises eight group pairs of token t, one per warp: each
+// half-warp one 128-channel group with eight channels per lane (one 16-byte
+// load, one 8-byte store); the token's index rows are staged once per block.
+constexpr int kQuantThreads = 256;
+constexpr int kQuantMaxK = 64;   // index rows of a token staged in shared memory
+
+__global__ void __launch_bounds__(kQuantThreads) moe_quant_x_kernel(
+    const __nv_bfloat16* __restrict__ x, int T, int H, int k, const int32_t* __restrict__ inv_pos,
+    uint8_t* __restrict__ xq, float* __restrict__ xs, float* __restrict__ xs_rows, int rows_cap) {
+  __shared__ int s_pos[kQuantMaxK];
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
-  const int g = blockIdx.y * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
   const int G = H / 128;
-  if (g >= G) return;
-  const size_t base = static_cast<size_t>(t) * H + g * 128 + lane * 4;
-  const uint2 raw = *reinterpret_cast<const uint2*>(x + base);
-  const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-  const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-  float v[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
-  float s;
-  const uint32_t q = quant_group4(v, &s);
-  *reinterpret_cast<uint32_t*>(xq + base) = q;
-  if (lane == 0) xs[static_cast<size_t>(t) * G + g] = s;
-  if (inv_pos != nullptr)
-    for (int j = lane; j < k; j += 32) {
-      const int pos = __ldg(inv_pos + static_cast<size_t>(t) * k + j);
-      if (static_cast<unsigned>(pos) < static_cast<unsigned>(rows_cap))
-        xs_rows[static_cast<size_t>(pos) * G + g] = s;
+  const bool staged = inv_pos != nullptr && k <= kQuantMaxK;
+  if (staged) {
+    for (int j = threadIdx.x; j < k; j += kQuantThreads)
+      s_pos[j] = __ldg(inv_pos + static_cast<size_t>(t) * k + j);
+    __syncthreads();
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hl = lane & 15;
+  const int gp = blockIdx.y * (kQuantThreads / 32) + warp;
+  if (2 * gp < G) {
+    const int g = 2 * gp + (lane >> 4);
+    const bool on = g < G;   // an odd G leaves the last pair's upper half idle
+    const size_t base = static_cast<size_t>(t) * H + g * 128 + hl * 8;
+    uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+    if (on) raw = __ldg(reinterpret_cast<const uint4*>(x + base));
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w4[i]);
+      v[2 * i] = __low2float(b);
+      v[2 * i + 1] = __high2float(b);
     }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float sc = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+    uint32_t q[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint16_t lo = cvt_e4m3x2(__fdiv_rn(v[4 * i + 1], sc), __fdiv_rn(v[4 * i], sc));
+      const uint16_t hi = cvt_e4m3x2(__fdiv_rn(v[4 * i + 3], sc), __fdiv_rn(v[4 * i + 2], sc));
+      q[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    if (!on) return;
+    *reinterpret_cast<uint2*>(xq + base) = make_uint2(q[0], q[1]);
+    if (hl == 0) xs[static_cast<size_t>(t) * G + g] = sc;
+    if (inv_pos != nullptr)
+      for (int j = hl; j < k; j += 16) {
+        const int pos = staged ? s_pos[j] : __ldg(inv_pos + static_cast<size_t>(t) * k + j);
+        if (static_cast<unsigned>(pos) < static_cast<unsigned>(rows_cap))
+          xs_rows[static_cast<size_t>(pos) * G + g] = sc;
+      }
+  }
 }
 
 cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* inv_pos,
                            uint8_t* xq, float* xs, float* xs_rows, int rows_cap, cudaStream_t st,
                            bool pdl) {
-  const dim3 grid(T, (H / 128 + 3) / 4);
-  return launch_kernel(moe_quant_x_kernel, grid, dim3(128), 0, st, pdl,
+  const int pairs = (H / 128 + 1) / 2;
+  const dim3 grid(T, (pairs + kQuantThreads / 32 - 1) / (kQuantThreads / 32));
+  return launch_kernel(moe_quant_x_kernel, grid, dim3(kQuantThreads), 0, st, pdl,
                        static_cast<const __nv_bfloat16*>(x), T, H, k, inv_pos, xq, xs, xs_rows,
                        rows_cap);
 }
