@@ -605,12 +605,18 @@ def run_ncu(args):
     import moe_expert_layer_align_gb300 as moe  # noqa: F401
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
-    wl = make_workload(args.config, args.T, "cuda")
+    if args.experts:
+        # a small case of the same recipe for multi-pass captures: E experts,
+        # the same rows per expert at T * E / E_config tokens
+        from moe_expert_layer_align_gb300 import workloads
+        wl = workloads.make(args.config, args.T, "cuda", E=args.experts)
+    else:
+        wl = make_workload(args.config, args.T, "cuda")
     layer = Layer(wl, stream, graph=False, w8a16=args.w8a16)
     for _ in range(args.warmup + args.steps):
         layer.run()
     stream.synchronize()
-    print(json.dumps({"ncu_mode": True, "config": args.config, "T": args.T,
+    print(json.dumps({"ncu_mode": True, "config": args.config, "T": args.T, "E": wl.E,
                       "calls": args.warmup + args.steps, "dev_status": int(layer.status.item())}))
 
 
@@ -626,6 +632,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ncu", action="store_true", help="profiler mode (no bench line)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiler mode: draw the workload with this many experts (small case)")
     ap.add_argument("--w8a16", action="store_true",
                     help="e4m3-weight workloads (4, 5) with bf16 activations (MOE_W8A16)")
     ap.add_argument("--record-traffic", metavar="CSV",
