@@ -99,8 +99,14 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 
 constexpr int kActThreads = 256;
 
+// Each block iteration takes R = max(1, 256 / (I/8)) index rows; thread t
+// owns channels 8c..8c+7 of row t / (I/8), c = t % (I/8) (more chunks than
+// threads: c = t, t + 256, ...), and loads its eight gate and eight up
+// values of every split as four 16-byte loads.  Padding rows are skipped
+// with one load.  In FP8 mode a half-warp covers one 128-channel group of
+// one row (I % 128 == 0, so 16 aligned lanes share row and group).
 template <int FP8>
-__global__ void __launch_bounds__(kActThreads)
+__global__ void __launch_bounds__(kActThreads, 4)
     moe_act_kernel(const float* __restrict__ G, int splits, int rows_cap, int I,
                    const int32_t* __restrict__ sorted_ids, int sentinel, void* __restrict__ A,
                    float* __restrict__ As) {
@@ -108,38 +114,65 @@ __global__ void __launch_bounds__(kActThreads)
   pdl_launch_dependents();
   const size_t two_i = 2 * static_cast<size_t>(I);
   const size_t slice = static_cast<size_t>(rows_cap) * two_i;
-  // Block-strided over index rows, thread-strided over 4-channel groups.  In
-  // FP8 mode a warp covers one whole 128-channel group per iteration (the
-  // loop bound is warp-uniform because I % 128 == 0).
-  for (int p = blockIdx.x; p < rows_cap; p += gridDim.x) {
-    if (__ldg(sorted_ids + p) >= sentinel) continue;  // padding row (block-uniform)
+  const int chunks = I / 8;
+  const bool wide = chunks >= kActThreads;
+  const int rows_per = wide ? 1 : kActThreads / chunks;
+  const int my_row = wide ? 0 : threadIdx.x / chunks;
+  const int c_first = wide ? threadIdx.x : threadIdx.x % chunks;
+  const int c_step = wide ? kActThreads : chunks;
+  const int lane = threadIdx.x & 31;
+  const uint32_t half_mask = lane < 16 ? 0x0000ffffu : 0xffff0000u;
+  if (my_row >= rows_per) return;   // threads past rows_per whole rows
+  for (int pb = blockIdx.x * rows_per; pb < rows_cap; pb += gridDim.x * rows_per) {
+    const int p = pb + my_row;
+    if (p >= rows_cap || __ldg(sorted_ids + p) >= sentinel) continue;   // padding row
     const float* row = G + static_cast<size_t>(p) * two_i;
-    for (int i = threadIdx.x * 4; i < I; i += kActThreads * 4) {
-      float4 g = __ldg(reinterpret_cast<const float4*>(row + i));
-      float4 u = __ldg(reinterpret_cast<const float4*>(row + I + i));
+    for (int c = c_first; c < chunks; c += c_step) {
+      const int i = 8 * c;
+      float g[8], u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = u[j] = 0.f;
 #pragma unroll 4
-      for (int s = 1; s < splits; ++s) {
-        const float4 gs = __ldg(reinterpret_cast<const float4*>(row + s * slice + i));
-        const float4 us = __ldg(reinterpret_cast<const float4*>(row + s * slice + I + i));
-        g.x += gs.x; g.y += gs.y; g.z += gs.z; g.w += gs.w;
-        u.x += us.x; u.y += us.y; u.z += us.z; u.w += us.w;
+      for (int sp = 0; sp < splits; ++sp) {
+        const float* r = row + sp * slice + i;
+        const float4 g0 = __ldg(reinterpret_cast<const float4*>(r));
+        const float4 g1 = __ldg(reinterpret_cast<const float4*>(r + 4));
+        const float4 u0 = __ldg(reinterpret_cast<const float4*>(r + I));
+        const float4 u1 = __ldg(reinterpret_cast<const float4*>(r + I + 4));
+        g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
+        g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
+        u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
+        u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
       }
-      float v[4] = {silu_mul(g.x, u.x), silu_mul(g.y, u.y), silu_mul(g.z, u.z),
-                    silu_mul(g.w, u.w)};
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = silu_mul(g[j], u[j]);
       if (FP8) {
-        float sc;
-        const uint32_t q = quant_group4(v, &sc);
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+#pragma unroll
+        for (int d = 8; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, d));
+        const float sc = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+        uint32_t q[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint16_t lo = cvt_e4m3x2(__fdiv_rn(v[4 * h + 1], sc), __fdiv_rn(v[4 * h], sc));
+          const uint16_t hi = cvt_e4m3x2(__fdiv_rn(v[4 * h + 3], sc), __fdiv_rn(v[4 * h + 2], sc));
+          q[h] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
         uint8_t* Aq = static_cast<uint8_t*>(A);
-        *reinterpret_cast<uint32_t*>(Aq + static_cast<size_t>(p) * I + i) = q;
-        if ((threadIdx.x & 31) == 0) As[static_cast<size_t>(p) * (I / 128) + i / 128] = sc;
+        *reinterpret_cast<uint2*>(Aq + static_cast<size_t>(p) * I + i) = make_uint2(q[0], q[1]);
+        if ((lane & 15) == 0) As[static_cast<size_t>(p) * (I / 128) + i / 128] = sc;
       } else {
-        __nv_bfloat16* Ab = static_cast<__nv_bfloat16*>(A) + static_cast<size_t>(p) * I + i;
-        __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(Ab) = packed;
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * h], v[2 * h + 1]);
+          w[h] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(A) + static_cast<size_t>(p) * I + i) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   }
@@ -148,12 +181,16 @@ __global__ void __launch_bounds__(kActThreads)
 cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
                        const int32_t* sorted_ids, int sentinel, void* A, float* As,
                        cudaStream_t st, bool pdl) {
-  // A few resident blocks per SM walk all rows: launching one block per
-  // (row, column chunk) spent most of the stage scheduling blocks of padding.
+  // Up to eight resident blocks of 256 threads per SM walk all index rows:
+  // one block per (row, column chunk) spent most of the stage scheduling
+  // blocks of padding.
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = rows_cap < 4 * sms ? rows_cap : 4 * sms;
+  const int chunks = I / 8;
+  const int rows_per = chunks >= kActThreads ? 1 : kActThreads / chunks;
+  const int want = (rows_cap + rows_per - 1) / rows_per;
+  const int grid = want < 8 * sms ? want : 8 * sms;
   if (fp8)
     return launch_kernel(moe_act_kernel<1>, dim3(grid), dim3(kActThreads), 0, st, pdl, G, splits,
                          rows_cap, I, sorted_ids, sentinel, A, As);
@@ -166,9 +203,14 @@ cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
 // weighted reduction restores expert outputs to token order.
 //   out[t][h] = sum_{j ascending} w[t][j] * sum_{s ascending} Y[s][inv_pos[t*k+j]][h]
 // fp32, fixed order, no atomics.
-constexpr int kCombineBatch = 8;   // assignments whose rows are loaded together
+// kCols output columns per thread (one or two 16-byte loads a row) and kBatch
+// assignments whose rows are loaded together: wide (8, 4) where the blocks
+// fill the GPU, narrow (4, 8) for few tokens, where more, shorter blocks
+// and all of a token's rows in flight at once cut the latency.
+constexpr int kCombineThreads = 256;
 
-__global__ void __launch_bounds__(128)
+template <int kCols, int kBatch>
+__global__ void __launch_bounds__(kCombineThreads)
     moe_combine_kernel(const float* __restrict__ Y, int splits, int rows_cap, int H,
                        const int32_t* __restrict__ inv_pos, const float* __restrict__ topk_w,
                        int T, int k, int k_routed, float w_shared, void* __restrict__ out,
@@ -176,18 +218,21 @@ __global__ void __launch_bounds__(128)
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
-  const int h = (blockIdx.y * 128 + threadIdx.x) * 4;
+  constexpr int kQ = kCols / 4;
+  const int h = (blockIdx.y * kCombineThreads + threadIdx.x) * kCols;
   if (h >= H) return;
   const size_t slice = static_cast<size_t>(rows_cap) * H;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < k; j0 += kCombineBatch) {
+  // H % 4 == 0: the second four columns exist unless this is a 4-column tail
+  const bool q1 = kQ > 1 && h + 4 < H;
+  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  for (int j0 = 0; j0 < k; j0 += kBatch) {
     // Issue every row load of the batch before reducing: the reduction order
     // (splits ascending, then j ascending) is unchanged.
-    int pos[kCombineBatch];
-    float w[kCombineBatch];
-    float4 y[kCombineBatch];
+    int pos[kBatch];
+    float w[kBatch];
+    float4 y[kBatch][kQ];
 #pragma unroll
-    for (int b = 0; b < kCombineBatch; ++b) {
+    for (int b = 0; b < kBatch; ++b) {
       const int j = j0 + b;
       pos[b] = j < k ? __ldg(inv_pos + static_cast<size_t>(t) * k + j) : -1;
       if (pos[b] >= rows_cap) pos[b] = -1;   // only rows of the index are read
@@ -196,38 +241,53 @@ __global__ void __launch_bounds__(128)
                           : (j < k ? w_shared : 0.f);
     }
 #pragma unroll
-    for (int b = 0; b < kCombineBatch; ++b)
-      y[b] = pos[b] >= 0 ? __ldg(reinterpret_cast<const float4*>(Y + static_cast<size_t>(pos[b]) * H + h))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+      for (int q = 0; q < kQ; ++q)
+        y[b][q] = (pos[b] >= 0 && (q == 0 || q1))
+                      ? __ldg(reinterpret_cast<const float4*>(Y + static_cast<size_t>(pos[b]) * H +
+                                                              h + 4 * q))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2
     for (int s = 1; s < splits; ++s) {
 #pragma unroll
-      for (int b = 0; b < kCombineBatch; ++b) {
+      for (int b = 0; b < kBatch; ++b) {
         if (pos[b] < 0) continue;
-        const float4 ys = __ldg(reinterpret_cast<const float4*>(
-            Y + s * slice + static_cast<size_t>(pos[b]) * H + h));
-        y[b].x += ys.x; y[b].y += ys.y; y[b].z += ys.z; y[b].w += ys.w;
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+          if (q == 1 && !q1) continue;
+          const float4 ys = __ldg(reinterpret_cast<const float4*>(
+              Y + s * slice + static_cast<size_t>(pos[b]) * H + h + 4 * q));
+          y[b][q].x += ys.x; y[b][q].y += ys.y; y[b][q].z += ys.z; y[b][q].w += ys.w;
+        }
       }
     }
 #pragma unroll
-    for (int b = 0; b < kCombineBatch; ++b) {
+    for (int b = 0; b < kBatch; ++b) {
       if (pos[b] < 0) continue;   // dropped assignment contributes 0
-      acc.x = fmaf(w[b], y[b].x, acc.x);
-      acc.y = fmaf(w[b], y[b].y, acc.y);
-      acc.z = fmaf(w[b], y[b].z, acc.z);
-      acc.w = fmaf(w[b], y[b].w, acc.w);
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        acc[q].x = fmaf(w[b], y[b][q].x, acc[q].x);
+        acc[q].y = fmaf(w[b], y[b][q].y, acc[q].y);
+        acc[q].z = fmaf(w[b], y[b][q].z, acc[q].z);
+        acc[q].w = fmaf(w[b], y[b][q].w, acc[q].w);
+      }
     }
   }
+  // 8-byte (bf16) or 16-byte (fp32) stores per four columns: t * H is only a
+  // multiple of 4
   const size_t o = static_cast<size_t>(t) * H + h;
-  if (out_bf16) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + o) = packed;
-  } else {
-    *reinterpret_cast<float4*>(static_cast<float*>(out) + o) = acc;
+#pragma unroll
+  for (int q = 0; q < kQ; ++q) {
+    if (q == 1 && !q1) break;
+    if (out_bf16) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[q].x, acc[q].y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[q].z, acc[q].w);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + o + 4 * q) =
+          make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + o + 4 * q) = acc[q];
+    }
   }
 }
 
@@ -235,9 +295,20 @@ cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H, cons
                            const float* topk_w, int T, int k,
                            int k_routed, float w_shared, void* out, int out_bf16,
                            cudaStream_t st, bool pdl) {
-  const dim3 grid(T, (H / 4 + 127) / 128);
-  return launch_kernel(moe_combine_kernel, grid, dim3(128), 0, st, pdl, Y, splits, rows_cap, H,
-                       inv_pos, topk_w, T, k, k_routed, w_shared, out, out_bf16);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int wide_blocks = T * ((H + 8 * kCombineThreads - 1) / (8 * kCombineThreads));
+  if (wide_blocks >= 4 * sms) {
+    const dim3 grid(T, (H + 8 * kCombineThreads - 1) / (8 * kCombineThreads));
+    return launch_kernel(moe_combine_kernel<8, 4>, grid, dim3(kCombineThreads), 0, st, pdl, Y,
+                         splits, rows_cap, H, inv_pos, topk_w, T, k, k_routed, w_shared, out,
+                         out_bf16);
+  }
+  const dim3 grid(T, (H + 4 * kCombineThreads - 1) / (4 * kCombineThreads));
+  return launch_kernel(moe_combine_kernel<4, 8>, grid, dim3(kCombineThreads), 0, st, pdl, Y,
+                       splits, rows_cap, H, inv_pos, topk_w, T, k, k_routed, w_shared, out,
+                       out_bf16);
 }
 
 // ---------------------------------------------------------------- router
