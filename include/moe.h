@@ -126,9 +126,12 @@ typedef struct {
   /* 1: run SiLU-and-mul as its own stage even where the plan fuses it into
    * the Gate-Up epilogue (BF16 layer with an unsplit Gate-Up). */
   int32_t separate_act;
-  /* 1: every GEMM CTA rebuilds the routing index from the top-k ids in its
+  /* Every GEMM CTA rebuilds the routing index from the top-k ids in its
    * shared memory (T*k <= 4096 and room next to the pipeline), instead of
-   * the separate index kernel; the Gate-Up writes the index out. */
+   * the separate index kernel; the Gate-Up writes the index out.
+   * 1: on where it fits; -1: off; 0: planner (on where it fits for BF16
+   * layers with at most 16 experts, index and weight experts counted;
+   * never with moe_forward_routed).  Other values: MOE_ERR_ARG. */
   int32_t smem_index;
   /* 1: one 128-row weight tile per GEMM work unit even for large token tiles
    * (where the plan pairs two to halve the token-tile traffic per MMA). */

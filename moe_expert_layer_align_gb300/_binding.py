@@ -157,7 +157,7 @@ def moe_index_tiles_cap(T, k, E, block_m) -> int:
 
 
 def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
-              stage_events=None, separate_act=False, smem_index=False,
+              stage_events=None, separate_act=False, smem_index=None,
               single_weight_tile=False, num_shared_experts=0, shared_expert_weight=0.0,
               ep_first_expert=0, ep_num_experts=0, fuse_routing=False,
               unit_order=0) -> moe_forward_opts:
@@ -170,7 +170,8 @@ def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
     o.ep_num_experts = ep_num_experts
     o.disable_pdl = int(disable_pdl)
     o.separate_act = int(separate_act)
-    o.smem_index = int(smem_index)
+    # None: planner; True / False: on / off
+    o.smem_index = 0 if smem_index is None else (1 if smem_index else -1)
     o.single_weight_tile = int(single_weight_tile)
     o.split_gateup = split_gateup
     o.split_down = split_down

@@ -90,6 +90,16 @@ struct IndexScratch {
   }
 };
 
+// Warps that take part in counting and scattering: one per 32 assignments,
+// at most the block's.  A small batch then zeroes and scans a short count
+// table instead of the whole block's (the segments, and with them the
+// result, are the same function of tk and this count in both passes).
+__device__ __forceinline__ int index_warps(int tk) {
+  const int nwarps = blockDim.x >> 5;
+  const int need = (tk + 31) / 32;
+  return need < 1 ? 1 : (need < nwarps ? need : nwarps);
+}
+
 // offs[0..E] = exclusive prefix of tot[] rounded up to multiples of bm (warp
 // 0; each lane a run of experts).  Ends with a block barrier.
 __device__ __forceinline__ void index_scan_offsets(int E, int bm, const IndexScratch& sc) {
@@ -119,7 +129,7 @@ __device__ __forceinline__ void index_scan_offsets(int E, int bm, const IndexScr
 // holds the T*k ids (shared or global memory).  Ends with a block barrier.
 __device__ __forceinline__ void index_count_and_scan(const int32_t* src, int tk, int E, int bm,
                                                      const IndexScratch& sc) {
-  const int tid = threadIdx.x, nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int tid = threadIdx.x, nthreads = blockDim.x, nwarps = index_warps(tk);
   const int warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < nwarps * E; i += nthreads) sc.cnt[i] = 0;
   if (tid == 0) *sc.flag = 0;
@@ -158,7 +168,7 @@ template <class RowFn, class InvalidFn>
 __device__ __forceinline__ void index_scatter(const int32_t* src, int tk, int E,
                                               const IndexScratch& sc, RowFn row,
                                               InvalidFn invalid) {
-  const int tid = threadIdx.x, nwarps = blockDim.x >> 5;
+  const int tid = threadIdx.x, nwarps = index_warps(tk);
   const int warp = tid >> 5, lane = tid & 31;
   const int seg = (tk + nwarps - 1) / nwarps;
   const int beg = min(tk, warp * seg);

@@ -199,7 +199,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     // variants are not combined with the in-path router
     RouterPlan r;
     if (!router_plan(s->T, s->H, s->E, &r) || s->k > 32) return MOE_ERR_SHAPE;
-    if (o && (o->smem_index || o->num_shared_experts || o->ep_num_experts)) return MOE_ERR_SHAPE;
+    if (o && (o->smem_index == 1 || o->num_shared_experts || o->ep_num_experts)) return MOE_ERR_SHAPE;
     p->routed = 1;
     p->rp_bn = r.bn, p->rp_rows_cap = r.rows_cap, p->rp_splits = r.splits, p->rp_kts = r.kts;
     p->rp_kt = r.kt, p->rp_mt = r.mt, p->rp_bytes = r.bytes;
@@ -259,12 +259,17 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     p->ord1 = unit_order(p->T, p->k, p->E, p->bm, p->mt1 / p->me1 * p->s1);
     p->ord2 = unit_order(p->T, p->k, p->E, p->bm, p->mt2 / p->me2 * p->s2);
   }
-  // On request (small batches): every GEMM CTA rebuilds the index from the
-  // top-k ids in shared memory when it fits next to the pipeline (no index
-  // kernel).  Measured no faster than the index kernel, so not the default.
+  // Every GEMM CTA rebuilds the index from the top-k ids in shared memory
+  // (no index kernel) on request, or by default for bf16 layers with at most
+  // 16 experts, where the per-CTA build is short (tiny 8-expert layer at
+  // T=8: 23.1 -> 21.0 us; with 128 experts it measured slower), when it fits
+  // next to the pipeline.
   {
+    if (o && (o->smem_index < -1 || o->smem_index > 1)) return MOE_ERR_ARG;
+    const int want = o ? o->smem_index : 0;
+    const bool auto_on = want == 0 && !routed && !p->fp8 && !p->w8 && p->E <= 16;
     const int tk = p->T * p->k;
-    bool fits = tk <= kSmemIndexMaxAssignments && o && o->smem_index && !p->w8;
+    bool fits = tk <= kSmemIndexMaxAssignments && (want == 1 || auto_on) && !p->w8;
     for (int bsrc : {static_cast<int>(kGather), static_cast<int>(kDirect)}) {
       const size_t need = gemm_smem_bytes(p->fp8, p->bm, bsrc) +
                           gemm_index_smem_bytes(gemm_warps(p->fp8, p->bm, bsrc), p->E, tk, p->rows_cap,

@@ -189,3 +189,21 @@ def test_unit_order_plan():
     for bad in (-1, 3):
         with pytest.raises(moe.MoeError):
             moe.moe_plan(mix, moe.make_opts(unit_order=bad))
+
+
+def test_smem_index_plan():
+    """The in-GEMM index is the default for bf16 layers with at most 16
+    experts (where it fits), never for FP8 or larger expert counts; it can be
+    forced on or off; other values are rejected."""
+    tiny = moe.make_shape(8, 256, 512, 8, 2, 0)
+    assert moe.moe_plan(tiny).smem_index == 1
+    assert moe.moe_plan(tiny, moe.make_opts(smem_index=False)).smem_index == 0
+    assert moe.moe_plan(moe.make_shape(1, 2048, 768, 128, 8, 0)).smem_index == 0
+    assert moe.moe_plan(moe.make_shape(1, 2048, 768, 128, 8, 0),
+                        moe.make_opts(smem_index=True)).smem_index == 1
+    assert moe.moe_plan(moe.make_shape(8, 256, 512, 8, 2, 0, True)).smem_index == 0
+    assert moe.moe_plan(moe.make_shape(2048, 4096, 14336, 8, 2, 0)).smem_index == 0   # T*k > 4096
+    o = moe.make_opts()
+    o.smem_index = 2
+    with pytest.raises(moe.MoeError):
+        moe.moe_plan(tiny, o)

@@ -37,7 +37,7 @@ def test_layer_matches_oracle(cfg, T, kw, smem_index):
     import moe_expert_layer_align_gb300 as moe
     wl = small(cfg, T, **kw)
     # the index kernel (default) or every GEMM CTA rebuilding the index
-    opts = moe.make_opts(smem_index=True) if smem_index else None
+    opts = moe.make_opts(smem_index=smem_index)   # both index paths, explicitly
     got = run_layer(wl, opts=opts).float().cpu().numpy()
     ref = oracle_layer(wl)
     assert_layer_close(got, ref, wl.mode, f"cfg{cfg} T={T}")
