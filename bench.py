@@ -38,7 +38,7 @@ import torch  # noqa: E402
 METRIC = "MoE layer µs & HBM GB/s vs 8 TB/s at T=1–64; TFLOP/s vs peak at T≥1024"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_SOURCES = ("k_gemm.cuh", "k_gemm_bf16.cu", "k_gemm_bf16_direct.cu", "k_gemm_fp8.cu",
-                "ptx.cuh")
+                "ptx.cuh", "index_build.cuh")
 
 
 def peaks():
