@@ -9,13 +9,18 @@
 // bf16 (round to nearest even) — and the MMA, the epilogue (with the fused
 // SiLU-and-mul) and the token operand are those of the bf16 layer.
 //
-// Two rings: R raw slots (the e4m3 weight stage, 128 rows x 64 bytes, plus
-// for the Down GEMM its token rows) filled by TMA, and C converted slots
-// (128 rows x 128 bytes bf16, 128-byte swizzle, plus for the Gate-Up GEMM the
-// gathered token rows).  A raw slot is released when the MMA that read its
-// converted tile (and, Down, its token rows) completes; a converted slot
-// likewise.  The raw ring is deep (up to 16 stages) because in the decode
-// regime the weight stream is what the kernel waits on.
+// A stage is one 128-wide K block (one block scale).  Two rings: R raw slots
+// (the e4m3 weight stage as two 64-wide halves of 128 rows x 64 bytes, one TMA
+// box each, plus for the Down GEMM its token rows as two 64-wide bf16
+// sub-tiles) filled by TMA, and C converted
+// slots (two 128-row x 64-wide bf16 sub-tiles, 128-byte swizzle, plus for the
+// Gate-Up GEMM the gathered token rows as two sub-tiles).  The MMA issues
+// eight instructions per stage.  (64-wide stages cost the MMA thread the same
+// waits, fence and commits per stage for half the bytes, and it was the
+// kernel's limit: issuing 65 % of the time.)  A raw slot is released when the
+// MMA that read its converted tile (and, Down, its token rows) completes; a
+// converted slot likewise.  The raw ring is as deep as shared memory allows
+// because in the decode regime the weight stream is what the kernel waits on.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -24,25 +29,31 @@
 
 namespace moe {
 
-constexpr int kW8RawA = kTileM * 64;    // e4m3 weight stage: 128 rows x 64 K
+constexpr int kW8RawHalf = kTileM * 64;  // one 64-wide K half of a stage, 64-byte rows
+constexpr int kW8RawA = 2 * kW8RawHalf;  // e4m3 weight stage: 128 rows x 128 K
+constexpr int kW8Budget = 214 * 1024;    // both rings
 
-// Converted slots (6 for narrow tiles measured no faster than 3).
-__host__ __device__ constexpr int w8_conv_slots(int) { return 3; }
-
+__host__ __device__ constexpr int w8_conv_slots(int) { return 2; }
+__host__ __device__ constexpr int w8_conv_slot_bytes(int bn, int bsrc) {
+  return 2 * kABytes + (bsrc == kGather ? 2 * bn * kKBytes : 0);
+}
+__host__ __device__ constexpr int w8_raw_slot_bytes(int bn, int bsrc) {
+  return kW8RawA + (bsrc == kDirect ? 2 * bn * kKBytes : 0);
+}
 __host__ __device__ constexpr int w8_raw_slots(int bn, int bsrc) {
-  return ((196608 - w8_conv_slots(bn) * (kABytes + bn * kKBytes)) /
-              (kW8RawA + (bsrc == kDirect ? bn * kKBytes : 0)) < 16)
-             ? (196608 - w8_conv_slots(bn) * (kABytes + bn * kKBytes)) /
-                   (kW8RawA + (bsrc == kDirect ? bn * kKBytes : 0))
+  return ((kW8Budget - w8_conv_slots(bn) * w8_conv_slot_bytes(bn, bsrc)) /
+              w8_raw_slot_bytes(bn, bsrc) < 16)
+             ? (kW8Budget - w8_conv_slots(bn) * w8_conv_slot_bytes(bn, bsrc)) /
+                   w8_raw_slot_bytes(bn, bsrc)
              : 16;
 }
 
 template <int BN, int BSRC>
 struct W8Shape {
-  static constexpr int kRawB = BSRC == kDirect ? BN * kKBytes : 0;   // token rows (Down)
-  static constexpr int kRawSlot = kW8RawA + kRawB;
-  static constexpr int kBBytes = BN * kKBytes;
-  static constexpr int kConvSlot = kABytes + kBBytes;    // bf16 weight tile + gathered rows
+  static constexpr int kBBytes = BN * kKBytes;            // one 64-wide token sub-tile
+  static constexpr int kRawB = BSRC == kDirect ? 2 * kBBytes : 0;   // token rows (Down)
+  static constexpr int kRawSlot = w8_raw_slot_bytes(BN, BSRC);
+  static constexpr int kConvSlot = w8_conv_slot_bytes(BN, BSRC);   // 2 bf16 sub-tiles (+ rows)
   static constexpr int kRawSlots = w8_raw_slots(BN, BSRC);
   static constexpr int kConvSlots = w8_conv_slots(BN);
   static constexpr int kEpiWarps = 4;
@@ -66,7 +77,7 @@ struct W8Shape {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr size_t kSmemBytes = 1024 + ((kOffMisc + 16 + 15) & ~15);
   static_assert(kRawSlot % 1024 == 0 && kConvSlot % 1024 == 0, "slots keep 1024-byte alignment");
-  static_assert(kRawSlots >= 4, "raw ring too shallow");
+  static_assert(kRawSlots >= 3, "raw ring too shallow");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "tcgen05.alloc takes a power of two from 32 to 512 columns");
@@ -174,13 +185,17 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
         if (lane == 0) {
           const uint32_t full = bar_rfull + 8 * slot;
           const uint32_t dst = sRaw + slot * S::kRawSlot;
-          const int kc = kt * 64;
+          const int kc = kt * 128;   // e4m3: elements are bytes
           mbar_arrive_expect_tx(full, bytes);
-          if (BSRC == kGather)
-            tma_load_5d(dst, &tmA, full, kc, 0, 0, w.mt * 4, w.e);
-          else
-            tma_load_3d(dst, &tmA, full, kc, w.mt * kTileM, w.e);
-          if (BSRC != kGather) tma_load_2d(dst + kW8RawA, &tmB, full, kc, w.row0);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (BSRC == kGather)
+              tma_load_5d(dst + h * kW8RawHalf, &tmA, full, kc + 64 * h, 0, 0, w.mt * 4, w.e);
+            else
+              tma_load_3d(dst + h * kW8RawHalf, &tmA, full, kc + 64 * h, w.mt * kTileM, w.e);
+            if (BSRC != kGather)
+              tma_load_2d(dst + kW8RawA + h * S::kBBytes, &tmB, full, kc + 64 * h, w.row0);
+          }
         }
         __syncwarp();
         ++issued;
@@ -223,13 +238,18 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
           tc_fence_after();
           fence_proxy_async_smem();   // converted tile and gathered rows: generic-proxy writes
           const uint32_t conv = sConv + cs * S::kConvSlot;
-          const uint64_t adesc = smem_desc_sw128(conv);
-          const uint64_t bdesc = smem_desc_sw128(BSRC == kGather ? conv + kABytes
-                                                                 : sRaw + rs * S::kRawSlot + kW8RawA);
           const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kt > w.kt0 || k > 0) ? 1u : 0u);
+          for (int h = 0; h < 2; ++h) {   // the stage's two 64-wide sub-tiles
+            const uint64_t adesc = smem_desc_sw128(conv + h * kABytes);
+            const uint64_t bdesc = smem_desc_sw128(
+                BSRC == kGather ? conv + 2 * kABytes + h * S::kBBytes
+                                : sRaw + rs * S::kRawSlot + kW8RawA + h * S::kBBytes);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc,
+                       (kt > w.kt0 || h > 0 || k > 0) ? 1u : 0u);
+          }
           tc_commit(bar_cempty + 8 * cs);
           tc_commit(bar_rempty + 8 * rs);
           if (++cs == S::kConvSlots) {
@@ -320,29 +340,30 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
     }
   } else if (warp < S::kGatherBase / 32) {
     // ------------------------------------------------------------ converters
-    // Converter thread t handles items t + NT i (NT converter threads, i <
-    // 512 / NT) of a stage, item = (row, 16-byte chunk) = (item / 4, item %
-    // 4): a warp instruction covers 8 whole rows (512 contiguous bytes) of
-    // the raw tile.  All of a thread's rows are at the same place in their
-    // quadrant (NT is a multiple of 128), so they share one block scale
-    // (Gate-Up: gate or up rows).
-    constexpr int kItems = 512 / S::kConvThreads;
+    // A stage has 1024 items (half h, row, 16-byte chunk c of the 64-byte
+    // half-row): item j = t + NT i (NT converter threads) is c = j % 4, row
+    // (j / 4) % 128, h = j / 512.  Eight consecutive threads read two whole
+    // 64-byte rows of one half (128 contiguous bytes) and write two swizzled
+    // bf16 rows whose chunks fall in disjoint banks.  All of a thread's rows
+    // sit at the same place in their 32-row quadrant (NT / 4 is a multiple of
+    // 32), so they share one block scale: Down's, or the gate or up scale.
+    constexpr int kItems = 1024 / S::kConvThreads;
     const int t = threadIdx.x - S::kRoleThreads;
-    const int rq = (t >> 2) & 31;   // row within its quadrant
-    const int ch = t & 3;           // raw chunk
-    const int KB = p.kt_total / 2;  // 128-wide K blocks (two 64-wide stages each)
+    const int c4 = t & 3;
+    const bool up_rows = BSRC == kGather && ((t >> 2) & 31) >= 16;
+    const int KB = p.kt_total;      // 128-wide K blocks = stages
     int rs = 0, cs = 0;
     uint32_t rph = 0, cph = 0;
     bool ok = true;
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, nullptr); ok && it.valid(); it.advance()) {
       if (*abort_flag) break;
       const WorkUnit w = it.take(p);
-      const int row = BSRC == kGather ? (rq < 16 ? w.mt * 64 : p.I + w.mt * 64) : w.mt * kTileM;
+      const int row = BSRC == kGather ? (up_rows ? p.I + w.mt * 64 : w.mt * 64) : w.mt * kTileM;
       const float* wsp = p.w_scale + (static_cast<size_t>(w.e) * (p.M >> 7) + (row >> 7)) * KB;
-      float sc_next = __ldg(wsp + (w.kt0 >> 1));
+      float sc_next = __ldg(wsp + w.kt0);
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         const float sc = sc_next;
-        if (kt + 1 < w.kt1) sc_next = __ldg(wsp + ((kt + 1) >> 1));
+        if (kt + 1 < w.kt1) sc_next = __ldg(wsp + kt + 1);
         if (!mbar_wait(bar_rfull + 8 * rs, rph) || !mbar_wait(bar_cempty + 8 * cs, cph ^ 1u)) {
           report_timeout(p, abort_flag);
           ok = false;
@@ -352,13 +373,16 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
         uint8_t* conv = smem + S::kOffConv + cs * S::kConvSlot;
 #pragma unroll
         for (int i = 0; i < kItems; ++i) {
-          const int rr = (t >> 2) + (S::kConvThreads / 4) * i;   // tile row
-          const uint4 q = *reinterpret_cast<const uint4*>(raw + rr * 64 + ch * 16);
+          const int j = t + S::kConvThreads * i;
+          const int rr = (j >> 2) & 127;   // tile row
+          const int h = j >> 9;            // K half
+          const uint4 q = *reinterpret_cast<const uint4*>(raw + h * kW8RawHalf + rr * 64 + c4 * 16);
           uint4 lo, hi;
           dequant16_bf16(q, sc, lo, hi);
-          const int c0 = 2 * ch, sw = rr & 7;
-          *reinterpret_cast<uint4*>(conv + rr * kKBytes + ((c0 ^ sw) << 4)) = lo;
-          *reinterpret_cast<uint4*>(conv + rr * kKBytes + (((c0 + 1) ^ sw) << 4)) = hi;
+          const int c0 = 2 * c4, sw = rr & 7;
+          uint8_t* sub = conv + h * kABytes + rr * kKBytes;
+          *reinterpret_cast<uint4*>(sub + ((c0 ^ sw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(sub + (((c0 + 1) ^ sw) << 4)) = hi;
         }
         fence_proxy_async_smem();
         mbar_arrive(bar_cfull + 8 * cs);
@@ -399,15 +423,18 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t b_dst = sConv + cs * S::kConvSlot + kABytes;
-        const uint8_t* src = rows + static_cast<size_t>(kt) * kKBytes;
+        // the stage's 128 K of each row: two 128-byte halves, one per sub-tile
+        const uint32_t b_dst = sConv + cs * S::kConvSlot + 2 * kABytes;
+        const uint8_t* src = rows + static_cast<size_t>(kt) * 2 * kKBytes;
 #pragma unroll
-        for (int i = 0; i < kR; ++i) {
-          const int n = r0 + kRowStep * i;
-          if (tok[i] >= 0)
-            cp_async_16(b_dst + n * kKBytes + ((c ^ (n & 7)) << 4),
-                        src + static_cast<size_t>(tok[i]) * p.b_row_bytes);
-        }
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < kR; ++i) {
+            const int n = r0 + kRowStep * i;
+            if (tok[i] >= 0)
+              cp_async_16(b_dst + h * S::kBBytes + n * kKBytes + ((c ^ (n & 7)) << 4),
+                          src + h * kKBytes + static_cast<size_t>(tok[i]) * p.b_row_bytes);
+          }
         cp_async_arrive_noinc(bar_cfull + 8 * cs);
         if (++cs == S::kConvSlots) {
           cs = 0;

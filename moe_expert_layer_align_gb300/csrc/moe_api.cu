@@ -221,7 +221,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   if (tc * p->bm >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
   p->tiles_cap = static_cast<int>(tc);
   p->rows_cap = static_cast<int>(tc * p->bm);
-  const int kstage = p->fp8 ? 128 : 64;
+  const int kstage = (p->fp8 || p->w8) ? 128 : 64;   // K elements per pipeline stage
   p->kt1 = s->H / kstage;
   p->mt1 = s->I / 64;
   p->kt2 = s->I / kstage;
