@@ -17,9 +17,10 @@
 // Gate-Up GEMM the gathered token rows as two sub-tiles).  The MMA issues
 // eight instructions per stage.  (64-wide stages cost the MMA thread the same
 // waits, fence and commits per stage for half the bytes, and it was the
-// kernel's limit: issuing 65 % of the time.)  A raw slot is released when the
-// MMA that read its converted tile (and, Down, its token rows) completes; a
-// converted slot likewise.  The raw ring is as deep as shared memory allows
+// kernel's limit: issuing 65 % of the time.)  A Gate-Up raw slot is released
+// by the converter warps once they have read it; a Down raw slot, whose token
+// rows the MMA reads, when that MMA completes; a converted slot likewise.
+// The raw ring is as deep as shared memory allows
 // because in the decode regime the weight stream is what the kernel waits on.
 #pragma once
 #include <cuda_bf16.h>
@@ -135,7 +136,9 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kRawSlots; ++s) {
       mbar_init(bar_rfull + 8 * s, 1);      // the TMA thread's expect-tx arrival
-      mbar_init(bar_rempty + 8 * s, 1);     // the MMA's commit
+      // Gate-Up: each converter warp once it has read the slot; Down (whose
+      // token rows the MMA reads from it): the MMA's commit
+      mbar_init(bar_rempty + 8 * s, BSRC == kGather ? S::kConvWarps : 1);
     }
     for (int s = 0; s < S::kConvSlots; ++s) {
       mbar_init(bar_cfull + 8 * s, S::kConvThreads + S::kGatherThreads);
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
                        (kt > w.kt0 || h > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(bar_cempty + 8 * cs);
-          tc_commit(bar_rempty + 8 * rs);
+          if (BSRC != kGather) tc_commit(bar_rempty + 8 * rs);
           if (++cs == S::kConvSlots) {
             cs = 0;
             cph ^= 1u;
@@ -386,6 +389,11 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(bar_cfull + 8 * cs);
+        if (BSRC == kGather) {
+          // this warp's reads of the raw slot are done (their values were used)
+          __syncwarp();
+          if ((t & 31) == 0) mbar_arrive(bar_rempty + 8 * rs);
+        }
         if (++rs == S::kRawSlots) {
           rs = 0;
           rph ^= 1u;
