@@ -9,9 +9,11 @@
 // SiLU-and-mul of section "MoE", "Gate-Up and activation" and writes the
 // activation Down reads, so no separate activation stage runs.
 //
-// Orientation ("swap-AB"): the MMA's M side is always 128 weight rows, the N
-// side (BN = block_m) is the token tile.  A decode-sized expert group of a
-// few tokens then costs a narrow N, not a padded 128-row M.
+// Orientation ("swap-AB"): the MMA's M side is 128 weight rows, the N side
+// (BN = block_m) is the token tile.  A decode-sized expert group of a few
+// tokens then costs a narrow N, not a padded 128-row M.  FP8 with 128-row
+// token tiles is the exception: it runs token-major (kTokM below), which
+// makes the block-scale promotion per-thread constant.
 //
 // For weight tile mt, split ks and row tile q (one work unit), with e the
 // tile's expert:
@@ -28,7 +30,8 @@
 // one of up to 8 TMEM buffers; the epilogue warps read it and add
 // partial * w_scale[e][row/128][kb] * b_scale[row or token][kb] into fp32
 // registers (block scales are fp32, so the product cannot be folded into the
-// MMA).
+// MMA).  Work units are walked weight-tile-major or token-tile-major, as the
+// planner chooses (make_unit).
 //
 // Index modes.  With few assignments every CTA rebuilds the routing index in
 // its own shared memory from the top-k ids (index_build.cuh) — an input of
