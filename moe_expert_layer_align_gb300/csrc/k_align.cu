@@ -150,12 +150,22 @@ __global__ void __launch_bounds__(kAlignThreads)
   const int tid = threadIdx.x;
   pdl_wait();
   pdl_launch_dependents();
+  // Per expert, the exclusive prefix over the chunks.  Each batch's counts
+  // are all loaded before its bases are stored: a load-store-load walk put
+  // one L2 round trip per chunk on the critical path (13.9 us at 32 chunks).
+  constexpr int kScanBatch = 16;
   for (int e = tid; e < E; e += kAlignThreads) {
     int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      const int c = hist[static_cast<size_t>(b) * E + e];
-      hist[static_cast<size_t>(b) * E + e] = run;
-      run += c;
+    for (int b0 = 0; b0 < nb; b0 += kScanBatch) {
+      int c[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j)
+        c[j] = b0 + j < nb ? hist[static_cast<size_t>(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) {
+        if (b0 + j < nb) hist[static_cast<size_t>(b0 + j) * E + e] = run;
+        run += c[j];
+      }
     }
     sc.tot[e] = run;
     idx.counts[e] = run;
