@@ -104,10 +104,16 @@ def test_intermediates_bf16(fused, smem_index):
         np.testing.assert_allclose(A[p], act, rtol=1e-2, atol=1e-2 * np.abs(act).max())
 
 
-@pytest.mark.parametrize("smem_index", [False, True])
-def test_intermediates_fp8_codes(smem_index):
+@pytest.mark.parametrize("smem_index,H,I", [(False, 512, 256), (True, 512, 256),
+                                            (False, 384, 256), (False, 2304, 256),
+                                            (False, 512, 2304)])
+def test_intermediates_fp8_codes(smem_index, H, I):
+    """x codes and scales bit-exact (an odd number of 128-channel groups,
+    several blocks of group pairs per token), the index bit-exact, and the
+    activation codes (rows of more than 256 eight-channel chunks) within a
+    few rounding-edge flips of the oracle's."""
     import moe_expert_layer_align_gb300 as moe
-    wl = small(4, 20, H=512, I=256, E=6, k=3)
+    wl = small(4, 20, H=H, I=I, E=6, k=3)
     opts = moe.make_opts(smem_index=smem_index)
     shape = moe.layer_shape(wl.x, wl.w13q, wl.topk_ids, 0, torch.bfloat16)
     ws = torch.zeros(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
