@@ -67,10 +67,12 @@ def test_forced_splits_and_no_pdl(s1, s2, sep, mode_cfg):
     assert_layer_close(got, oracle_layer(wl), wl.mode, f"splits {s1},{s2}")
 
 
-@pytest.mark.parametrize("fused,smem_index", [(True, False), (False, False), (True, True)])
-def test_intermediates_bf16(fused, smem_index):
+@pytest.mark.parametrize("fused,smem_index,I", [(True, False, 128), (False, False, 128),
+                                               (True, True, 128), (False, False, 2112)])
+def test_intermediates_bf16(fused, smem_index, I):
     import moe_expert_layer_align_gb300 as moe
-    wl = small(2, 33, H=256, I=128, E=4)
+    # I = 2112: activation rows of 264 eight-channel chunks (more than a block's threads)
+    wl = small(2, 33, H=256, I=I, E=4)
     # unsplit Gate-Up fuses SiLU-and-mul into its epilogue; a split one
     # leaves fp32 partials for the separate stage.  The index comes from the
     # Gate-Up's CTA 0 (shared-memory mode) or from the index kernel.
