@@ -126,9 +126,10 @@ struct GemmShape {
   static constexpr int kOffBar = kOffB + kStages * kBBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;  // + drain
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  // FP8: the token-operand scales of one K block, double-buffered [2][BN]
+  // FP8: the token-operand scales of one K block, double-buffered per
+  // epilogue warp: [kEpiWarps][2][its BN * 4 / kEpiWarps columns]
   static constexpr int kOffScale = (kOffMisc + 16 + 15) & ~15;
-  static constexpr int kOffIdx = kOffScale + (FP8 ? 2 * BN * 4 : 0);  // shared-memory index
+  static constexpr int kOffIdx = kOffScale + (FP8 ? 8 * BN * 4 : 0);  // shared-memory index
   static constexpr size_t kSmemBytes = 1024 + kOffIdx;             // without the index
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N % 16 == 0");
   static_assert(ME == 1 || !FP8, "FP8 promotion keeps one weight tile per unit");
@@ -697,15 +698,18 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
         }
         float* outp = p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0) * p.M + col;
         // The token-operand scale of column n is the same for every row, so
-        // the four epilogue warps stage it in shared memory once per K block
-        // (epilogue thread et loads column et) and read it back as broadcast
-        // 16-byte loads.  One named barrier per K block publishes the next
-        // block's scales; the buffer written is never the one being read.
-        const int et = threadIdx.x - 64;
+        // each epilogue warp stages its own columns' scales in its own
+        // shared-memory slots once per K block (lane j loads column
+        // c_base + j) and reads them back as broadcast 16-byte loads; a
+        // __syncwarp publishes them, so the warps never wait on one another
+        // (a block-wide barrier per K block cost 4-8 % of the FP8 decode
+        // GEMMs).  The slot written is never the one being read.
         const int KB = p.kt_total;
+        float* sxw = sx_buf + (warp - 2) * 2 * kWarpCols;
+        const int jc = c_base + lane;   // this lane's column
         int srow = -1;
-        if (et < BN && et < w.rows)
-          srow = p.scale_by_token ? assignment_token(row_assign(w.row0 + et), p) : w.row0 + et;
+        if (lane < kWarpCols && jc < w.rows)
+          srow = p.scale_by_token ? assignment_token(row_assign(w.row0 + jc), p) : w.row0 + jc;
         const float* bsp = srow >= 0 ? p.b_scale + static_cast<size_t>(srow) * KB : nullptr;
         const int blk = (BSRC == kGather) ? ((lane < 16 ? w.mt * 64 : p.I + w.mt * 64) >> 7) : w.mt;
         const float* wsp = p.w_scale + (static_cast<size_t>(w.e) * (p.M >> 7) + blk) * KB;
@@ -714,10 +718,10 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
         // would put its latency on the critical path.
         auto sx_at = [&](int kt) { return (bsp && kt < w.kt1) ? __ldg(bsp + kt) : 0.f; };
         auto sw_at = [&](int kt) { return kt < w.kt1 ? __ldg(wsp + kt) : 0.f; };
-        if (et < BN) sx_buf[et] = sx_at(w.kt0);
+        if (lane < kWarpCols) sxw[lane] = sx_at(w.kt0);
         float sx_n1 = sx_at(w.kt0 + 1), sx_n2 = sx_at(w.kt0 + 2);
         float sw_0 = sw_at(w.kt0), sw_1 = sw_at(w.kt0 + 1), sw_2 = sw_at(w.kt0 + 2);
-        named_barrier_sync(1, S::kEpiThreads);
+        __syncwarp();
         // this warp's columns c_base.. in packed pairs (fma.rn.f32x2: two
         // fp32 FMAs, each rounded as fmaf)
         uint64_t acc2[kWarpCols / 2];
@@ -740,7 +744,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           }
           if (ok) {
             tc_fence_after();
-            const float* sxb = sx_buf + cur * BN;
+            const float* sxb = sxw + cur * kWarpCols;   // this warp's columns
             const uint64_t sw2 = pack_f32x2(sw, sw);
             // TMEM reads two 16-column chunks at a time, one wait per pair
             constexpr int kLdBatch = kWarpCols / 16 < 2 ? kWarpCols / 16 : 2;
@@ -762,7 +766,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
 #pragma unroll
                   for (int q4 = 0; q4 < 4; ++q4) {
                     const float4 s4 =
-                        *reinterpret_cast<const float4*>(sxb + c_base + c * 16 + 4 * q4);
+                        *reinterpret_cast<const float4*>(sxb + c * 16 + 4 * q4);
                     const int h = (c * 16 + 4 * q4) / 2;
                     const uint64_t s01 = mul_f32x2(pack_f32x2(s4.x, s4.y), sw2);
                     const uint64_t s23 = mul_f32x2(pack_f32x2(s4.z, s4.w), sw2);
@@ -782,11 +786,9 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
             }
           }
           cur ^= 1;
-          if (et < BN) sx_buf[cur * BN + et] = sx_stage;
-          // Every epilogue warp reaches this barrier once per K block, also
-          // after a timeout; the OR of the abort state it returns ends all
-          // four loops at the same K block.
-          if (named_barrier_or(1, S::kEpiThreads, !ok || *abort_flag)) {
+          if (lane < kWarpCols) sxw[cur * kWarpCols + lane] = sx_stage;
+          __syncwarp();
+          if (!ok || *abort_flag) {
             ok = false;
             break;
           }
