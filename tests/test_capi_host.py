@@ -207,3 +207,16 @@ def test_smem_index_plan():
     o.smem_index = 2
     with pytest.raises(moe.MoeError):
         moe.moe_plan(tiny, o)
+
+
+def test_fp8_row_tile_rule():
+    """FP8 takes 128-row (token-major) tiles where the mean-rows rule gives
+    64; bf16 keeps 64 there; w8a16 follows the bf16 rule."""
+    # DeepSeek-shaped at T=1024: 32 rows per active expert -> 64 by the rule
+    assert moe.moe_plan(moe.make_shape(1024, 7168, 2048, 256, 8, 0, True)).block_m == 128
+    assert moe.moe_plan(moe.make_shape(1024, 7168, 2048, 256, 8, 0)).block_m == 64
+    assert moe.moe_plan(moe.make_shape(1024, 7168, 2048, 256, 8, 0,
+                                       mode=B.MOE_W8A16)).block_m == 64
+    # decode sizes keep their narrow tiles
+    assert moe.moe_plan(moe.make_shape(64, 7168, 2048, 256, 8, 0, True)).block_m == 16
+    assert moe.moe_plan(moe.make_shape(512, 7168, 2048, 256, 8, 0, True)).block_m == 32
