@@ -166,6 +166,16 @@ typedef struct {
    * tiles times its units per token tile fit one wave of CTAs, else 1.
    * Results do not depend on it. */
   int32_t unit_order;
+  /* Testing aid for the timeout path.  0 (default): the pipeline waits of the
+   * expert GEMMs (operands landed, stage free, accumulator ready) give up
+   * after 2 s.  A positive value sets that limit in nanoseconds (and those
+   * waits then poll without blocking), so that a test can make them give up;
+   * 1 makes a wait give up unless its barrier is already complete when first
+   * tested.  The kernel then flags MOE_ERR_TIMEOUT in dev_status, lets its
+   * own copies and MMAs finish, frees its tensor memory and returns, and the
+   * call's output is undefined.  The waits for the kernel's own copies and
+   * MMAs before it exits keep the 2-s limit. */
+  int32_t pipeline_wait_ns;
 } moe_forward_opts;
 
 /* Options of moe_align_ex: the same shared-expert and expert-parallel mapping
@@ -327,24 +337,27 @@ MOE_API moe_status moe_router_topk(const void* x, const void* hi_lo, int32_t T,
                            float* topk_w, void* workspace, size_t ws_bytes,
                            void* stream);
 
-/* Largest workspace moe_forward_static can serve (128 MiB): for example the
- * Mixtral-shaped bf16 layer up to T=64 or the Qwen3-30B-A3B-shaped layer up
- * to T=256. */
+/* Largest workspace moe_forward_static can serve (128 MiB).  With the plans
+ * of this version that covers, for example, the Mixtral-shaped bf16 layer up
+ * to T=256, the Qwen3-30B-A3B-shaped layer up to T=512 and the
+ * DeepSeek-V3-shaped FP8 layer up to T=8; moe_workspace_bytes(shape, NULL)
+ * tells for any shape. */
 #define MOE_STATIC_SCRATCH_BYTES ((size_t)128 << 20)
 
 /* moe_forward without a workspace argument, for callers that cannot allocate
- * device memory: code running while a stream is captured into a CUDA graph in
- * the global capture mode (cudaMalloc is rejected there), serving engines
- * that reserve all device memory at start-up and forbid later allocation, and
- * plain-C hosts with no device allocator of their own.  No counterpart on the
- * pages: it is an interface convenience of this library.
+ * device memory: serving engines that reserve all device memory at start-up
+ * and forbid later allocation, and plain-C hosts with no device allocator of
+ * their own.  No counterpart on the pages: it is an interface convenience of
+ * this library.
  *   The intermediates live in one file-scope device array of
- *   MOE_STATIC_SCRATCH_BYTES that the CUDA loader reserves on every GPU that
- *   loads this library and that stays reserved until the process exits.  The
- *   call itself allocates nothing (no cudaMalloc / cudaFree, no allocating
- *   library routine).
- *   The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ *   MOE_STATIC_SCRATCH_BYTES.  The call itself allocates nothing (no
+ *   cudaMalloc / cudaFree, no allocating library routine), but under the CUDA
+ *   runtime's lazy module loading (its default) the array is reserved on a
+ *   device by the first moe_forward_static call there, and then held until
+ *   the process exits.  Make that first call on each device before reserving
+ *   the rest of device memory, and before any stream capture: it looks up the
+ *   array's device address with that device current.  A failed lookup returns
+ *   MOE_ERR_CUDA and is retried by the next call.
  *   All calls share the array and it keeps the last call's contents (nothing
  *   in it needs to start at zero): calls that overlap on the GPU race and must
  *   be serialised by the caller.

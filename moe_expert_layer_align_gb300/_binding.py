@@ -48,7 +48,7 @@ class moe_forward_opts(ctypes.Structure):
                 ("smem_index", _i32), ("single_weight_tile", _i32),
                 ("num_shared_experts", _i32), ("shared_expert_weight", ctypes.c_float),
                 ("ep_first_expert", _i32), ("ep_num_experts", _i32), ("fuse_routing", _i32),
-                ("unit_order", _i32)]
+                ("unit_order", _i32), ("pipeline_wait_ns", _i32)]
 
 
 class moe_align_opts(ctypes.Structure):
@@ -160,8 +160,9 @@ def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
               stage_events=None, separate_act=False, smem_index=None,
               single_weight_tile=False, num_shared_experts=0, shared_expert_weight=0.0,
               ep_first_expert=0, ep_num_experts=0, fuse_routing=False,
-              unit_order=0) -> moe_forward_opts:
+              unit_order=0, pipeline_wait_ns=0) -> moe_forward_opts:
     o = moe_forward_opts()
+    o.pipeline_wait_ns = pipeline_wait_ns
     o.unit_order = unit_order
     o.fuse_routing = int(fuse_routing)
     o.num_shared_experts = num_shared_experts

@@ -66,7 +66,10 @@ struct GemmParams {
     int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
   } index_out;
   unsigned int* zero_word;   // if set, CTA 0 zeroes it at start (the next kernel's ticket counter)
+  int clear_status;          // first kernel of the call: CTA 0 zeroes dev_status at start
   int early_weights;         // contiguous token operand: stream weights before the wait
+  uint64_t pipe_wait_ns;     // limit of the pipeline waits (0: kWaitLimitNs); drains keep
+                             // the full limit
   int scale_by_token;        // FP8 gathered operand: b_scale rows are tokens
 };
 
@@ -99,15 +102,17 @@ struct IndexPtrs {
 };
 // k and E below count assignments per token and experts of the index (map.kk
 // and map.E + shared experts); `map` turns topk_ids into index experts.
+// `clear`: the kernel is the call's first and zeroes dev_status before any
+// kernel of the call can set a bit (later kernels only OR bits in).
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                          const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st,
-                         bool pdl, const IdMap& map);
+                         bool pdl, const IdMap& map, bool clear);
 // The same index built by three kernels over chunks of assignments (count,
 // scan, scatter); `scratch` holds align_split_scratch_words(T, k, E) ints.
 size_t align_split_scratch_words(int T, int k, int E);
 cudaError_t launch_align_split(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                                const IndexPtrs& idx, int32_t* scratch, int32_t* dev_status,
-                               cudaStream_t st, bool pdl, const IdMap& map);
+                               cudaStream_t st, bool pdl, const IdMap& map, bool clear);
 cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* inv_pos,
                            uint8_t* xq, float* xs, float* xs_rows, int rows_cap, cudaStream_t st,
                            bool pdl);

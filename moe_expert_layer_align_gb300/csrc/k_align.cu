@@ -20,7 +20,8 @@ constexpr int kAlignMaxStagedIds = 32768;  // ids staged in shared memory up to 
 
 __global__ void __launch_bounds__(kAlignThreads)
     moe_align_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int tiles_cap,
-                     IndexPtrs idx, int32_t* dev_status, int stage_ids, IdMap map) {
+                     IndexPtrs idx, int32_t* dev_status, int stage_ids, IdMap map,
+                     int clear_status) {
   extern __shared__ int32_t sm[];
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
   IndexScratch sc;
@@ -34,7 +35,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   pdl_wait();
   pdl_launch_dependents();
 
-  if (tid == 0 && dev_status) *dev_status = 0;
+  if (tid == 0 && dev_status && clear_status) *dev_status = 0;
   if (stage_ids && !map.plain()) {
     // shared experts / expert parallelism: stage the index experts
     for (int i = tid; i < tk; i += nthreads) sids[i] = mapped_id(ids, i, map);
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(kAlignThreads)
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                          const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st, bool pdl,
-                         const IdMap& map) {
+                         const IdMap& map, bool clear) {
   const int tk = T * k;
   const int stage_ids = tk <= kAlignMaxStagedIds ? 1 : 0;
   if (!stage_ids && !map.plain()) return cudaErrorInvalidValue;   // mapped ids are staged
@@ -92,7 +93,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int ti
     configured[dev] = 1;
   }
   return launch_kernel(moe_align_kernel, dim3(1), dim3(threads), smem, st, pdl, ids, T, k, E,
-                       bm, tiles_cap, idx, dev_status, stage_ids, map);
+                       bm, tiles_cap, idx, dev_status, stage_ids, map, clear ? 1 : 0);
 }
 
 // ---------------------------------------------------------------- split build
@@ -126,13 +127,15 @@ __device__ __forceinline__ int stage_chunk(const int32_t* ids, int tk, int32_t* 
 
 __global__ void __launch_bounds__(kSplitThreads)
     moe_align_count_kernel(const int32_t* __restrict__ ids, int tk, int E, int bm,
-                           int32_t* __restrict__ hist, int32_t* __restrict__ flags, IdMap map) {
+                           int32_t* __restrict__ hist, int32_t* __restrict__ flags, IdMap map,
+                           int32_t* dev_status, int clear_status) {
   extern __shared__ int32_t sm[];
   IndexScratch sc;
   sc.carve(sm, kSplitWarps, E, map.Eg != 0);
   int32_t* chunk = sm + (chunk_smem_words(E) - kChunk);
   pdl_wait();
   pdl_launch_dependents();
+  if (clear_status && dev_status && blockIdx.x == 0 && threadIdx.x == 0) *dev_status = 0;
   const int n = stage_chunk(ids, tk, chunk, map);
   index_count_and_scan(chunk, n, E, bm, sc);
   for (int e = threadIdx.x; e < E; e += kSplitThreads)
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   if (tid == 0 && dev_status) {
     int any = 0;
     for (int b = 0; b < nb; ++b) any |= flags[b];
-    *dev_status = any ? kStatusExpertId : 0;
+    if (any) atomicOr(dev_status, kStatusExpertId);
   }
 }
 
@@ -218,14 +221,15 @@ size_t align_split_scratch_words(int T, int k, int E) {
 
 cudaError_t launch_align_split(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                                const IndexPtrs& idx, int32_t* scratch, int32_t* dev_status,
-                               cudaStream_t st, bool pdl, const IdMap& map) {
+                               cudaStream_t st, bool pdl, const IdMap& map, bool clear) {
   const int tk = T * k;
   const int nb = (tk + kChunk - 1) / kChunk;
   int32_t* hist = scratch;
   int32_t* flags = scratch + static_cast<size_t>(nb) * E;
   const size_t chunk_smem = 4 * chunk_smem_words(E);
   cudaError_t e = launch_kernel(moe_align_count_kernel, dim3(nb), dim3(kSplitThreads), chunk_smem,
-                                st, pdl, ids, tk, E, bm, hist, flags, map);
+                                st, pdl, ids, tk, E, bm, hist, flags, map, dev_status,
+                                clear ? 1 : 0);
   if (e != cudaSuccess) return e;
   e = launch_kernel(moe_align_scan_kernel, dim3(1), dim3(kAlignThreads),
                     4 * IndexScratch::words(1, E), st, true, hist,

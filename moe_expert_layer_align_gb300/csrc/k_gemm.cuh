@@ -54,8 +54,13 @@
 // instead of registers this split costs no registers, so the Hopper argument
 // for one warp group doing everything ("occupancy first, no warp
 // specialisation") does not carry over.  Every wait is bounded
-// (kWaitLimitNs); on a timeout the kernel ORs kStatusTimeout into dev_status,
-// drains its own copies and MMAs, frees TMEM and returns.
+// (GemmParams::pipe_wait_ns, kWaitLimitNs by default); on a timeout the
+// kernel ORs kStatusTimeout into dev_status and raises a CTA-wide abort flag
+// that every other wait also watches, so all roles leave their loops; then
+// the TMA warp waits for its own copies to land, the gather threads for
+// theirs, the MMA thread for its MMAs, and TMEM is freed.  Waits of warps
+// that go on to warp-collective instructions (tcgen05.ld, __syncwarp) are
+// voted across the warp, so its lanes never part ways.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -124,7 +129,12 @@ struct GemmShape {
   static constexpr uint32_t kIdesc = mma_idesc(FP8 ? 0u : 1u, kTileM, BN);
   static constexpr int kOffB = kStages * kAStage;
   static constexpr int kOffBar = kOffB + kStages * kBBytes;
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;  // + drain
+  // full (TMA bytes), empty, accumulator full / empty, drain, and for a
+  // gathered token operand one more ring that the gather threads arrive on
+  // (kept apart from the TMA's so that the TMA warp can wait for its own
+  // copies alone after an abort)
+  static constexpr int kNumBars =
+      2 * kStages + 2 * kAccBufs + 1 + (kGatherThreads > 0 ? kStages : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // FP8: the token-operand scales of one K block, double-buffered per
   // epilogue warp: [kEpiWarps][2][its BN * 4 / kEpiWarps columns]
@@ -248,6 +258,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
   const uint32_t bar_accf = bar_empty + 8 * S::kStages;
   const uint32_t bar_acce = bar_accf + 8 * S::kAccBufs;
   const uint32_t bar_drain = bar_acce + 8 * S::kAccBufs;
+  const uint32_t bar_gfull = bar_drain + 8;   // gathered rows of stage s landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 4);
   float* sx_buf = reinterpret_cast<float*>(smem + S::kOffScale);
@@ -255,13 +266,28 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tk = p.T * p.topk;
+  // Pipeline waits: bounded by pipe_wait_ns and left early once another role
+  // raised the abort flag.  warp_wait votes the outcome across the warp.
+  const uint64_t wait_ns = p.pipe_wait_ns ? p.pipe_wait_ns : kWaitLimitNs;
+  auto thread_wait = [&](uint32_t bar, uint32_t par) {
+    return mbar_wait(bar, par, wait_ns, abort_flag);
+  };
+  auto warp_wait = [&](uint32_t bar, uint32_t par) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, par, wait_ns, abort_flag));
+  };
+  auto warp_aborted = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0); };
 
   if (threadIdx.x == 0) {
     if (p.zero_word && blockIdx.x == 0) *p.zero_word = 0u;
+    // First kernel of the call: clear the status word before any bit is set.
+    // (A timeout bit of another CTA comes at least kWaitLimitNs after the
+    // grid started; CTA 0's own expert-id bit is ORed in after the prologue
+    // barrier, which orders it after this store.)
+    if (p.clear_status && p.dev_status && blockIdx.x == 0) *p.dev_status = 0;
     for (int s = 0; s < S::kStages; ++s) {
-      // the TMA thread's expect-tx arrival, plus one per gather thread
-      mbar_init(bar_full + 8 * s, 1 + S::kGatherThreads);
+      mbar_init(bar_full + 8 * s, 1);   // the TMA thread's expect-tx arrival
       mbar_init(bar_empty + 8 * s, 1);
+      if (S::kGatherThreads > 0) mbar_init(bar_gfull + 8 * s, S::kGatherThreads);
     }
     for (int b = 0; b < S::kAccBufs; ++b) {
       mbar_init(bar_accf + 8 * b, 1);
@@ -350,7 +376,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       b_now = true;
     };
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); ok && it.valid(); it.advance()) {
-      if (*abort_flag) break;
+      if (warp_aborted()) break;
       const WorkUnit w = it.take(p);
       if constexpr (S::kTmaRows > 0) {
         // lane l looks up row l's token; padding rows read token 0 (their
@@ -361,7 +387,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
         for (int j = 0; j < S::kTmaRows; ++j) tma_tok[j] = __shfl_sync(0xffffffffu, tok, j);
       }
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
-        if (!mbar_wait((S::kShareRel ? bar_accf : bar_empty) + 8 * stage, phase ^ 1u)) {
+        if (!warp_wait((S::kShareRel ? bar_accf : bar_empty) + 8 * stage, phase ^ 1u)) {
           report_timeout(p, abort_flag);
           ok = false;
           break;
@@ -401,8 +427,10 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       }
     }
     if (!b_now) flush_deferred();   // fewer stages than the ring holds
-    if (*abort_flag && lane == 0) {
-      // Let our own copies land before the CTA can exit.
+    if (lane == 0) {
+      // Let our own copies land before the CTA can exit (after a normal run
+      // every one of them has already been waited for by the MMA thread).
+      // Long limit and no abort check: this is the drain.
       const long first = issued > S::kStages ? issued - S::kStages : 0;
       for (long i = first; i < issued; ++i)
         mbar_wait(bar_full + 8 * static_cast<int>(i % S::kStages),
@@ -427,7 +455,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
         const int n_eff = S::kTokM ? BN : min(BN, max(16, (w.rows + 15) & ~15));
         const uint32_t idesc = (S::kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(n_eff >> 3) << 17);
         if (!FP8) {
-          if (!mbar_wait(bar_acce + 8 * ab, aph ^ 1u)) {
+          if (!thread_wait(bar_acce + 8 * ab, aph ^ 1u)) {
             report_timeout(p, abort_flag);
             break;
           }
@@ -435,14 +463,15 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
         }
         for (int kt = w.kt0; kt < w.kt1; ++kt) {
           if (FP8) {
-            if (!mbar_wait(bar_acce + 8 * ab, aph ^ 1u)) {
+            if (!thread_wait(bar_acce + 8 * ab, aph ^ 1u)) {
               report_timeout(p, abort_flag);
               ok = false;
               break;
             }
             tc_fence_after();
           }
-          if (!mbar_wait(bar_full + 8 * stage, phase)) {
+          if (!thread_wait(bar_full + 8 * stage, phase) ||
+              (BSRC == kGather && !thread_wait(bar_gfull + 8 * stage, phase))) {
             report_timeout(p, abort_flag);
             ok = false;
             break;
@@ -488,10 +517,10 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           }
         }
       }
-      if (*abort_flag) {
-        tc_commit(bar_drain);  // wait for our own MMAs before TMEM is freed
-        mbar_wait(bar_drain, 0);
-      }
+      // Wait for our own MMAs before TMEM is freed (always: another role may
+      // have given up after this thread issued its last MMA).  Long limit.
+      tc_commit(bar_drain);
+      mbar_wait(bar_drain, 0);
     }
     __syncwarp();
   } else if (warp < S::kRoleThreads / 32) {
@@ -519,7 +548,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       }
       if (et == 0) {
         *p.index_out.num_tiles = num_tiles;
-        if (p.dev_status) *p.dev_status = *si.sc.flag ? kStatusExpertId : 0;
+        if (p.dev_status && *si.sc.flag) atomicOr(p.dev_status, kStatusExpertId);
       }
     }
     const int qd = warp & 3;          // TMEM lane quadrant this warp may read
@@ -534,7 +563,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); it.valid(); it.advance()) {
       const WorkUnit w = it.take(p);
       if (!FP8) {
-        if (!mbar_wait(bar_accf + 8 * ab, aph)) {
+        if (!warp_wait(bar_accf + 8 * ab, aph)) {
           report_timeout(p, abort_flag);
           break;
         }
@@ -627,7 +656,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           sx0 = sx1, sx1 = sx2, sx2 = sx_at(kt + 3);
           sg0 = sg1, sg1 = sg2, sg2 = sg_at(kt + 3);
           su0 = su1, su1 = su2, su2 = su_at(kt + 3);
-          if (!mbar_wait(bar_accf + 8 * ab, aph)) {
+          if (!warp_wait(bar_accf + 8 * ab, aph)) {
             report_timeout(p, abort_flag);
             ok = false;
             break;
@@ -658,7 +687,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
             ab = 0;
             aph ^= 1u;
           }
-          if (*abort_flag) {
+          if (warp_aborted()) {
             ok = false;
             break;
           }
@@ -738,7 +767,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           const float sx_stage = sx_n1;   // published below for kt + 1
           sx_n1 = sx_n2;
           sx_n2 = sx_at(kt + 3);
-          if (!mbar_wait(bar_accf + 8 * ab, aph)) {
+          if (!warp_wait(bar_accf + 8 * ab, aph)) {
             report_timeout(p, abort_flag);
             ok = false;
           }
@@ -788,7 +817,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           cur ^= 1;
           if (lane < kWarpCols) sxw[cur * kWarpCols + lane] = sx_stage;
           __syncwarp();
-          if (!ok || *abort_flag) {
+          if (!ok || warp_aborted()) {
             ok = false;
             break;
           }
@@ -840,7 +869,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       const int step_a = nk > 1 ? 1 : 0;           // sorted-row loads issued
       const int step_b = nk > 2 ? 2 : nk - 1;      // turned into token rows
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
-        if (!mbar_wait((S::kShareRel ? bar_accf : bar_empty) + 8 * stage, phase ^ 1u)) {
+        if (!thread_wait((S::kShareRel ? bar_accf : bar_empty) + 8 * stage, phase ^ 1u)) {
           report_timeout(p, abort_flag);
           ok = false;
           break;
@@ -854,7 +883,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
             cp_async_16(b_dst + n * kKBytes + ((c ^ (n & 7)) << 4),
                         src + static_cast<size_t>(tok[i]) * p.b_row_bytes);
         }
-        cp_async_arrive_noinc(bar_full + 8 * stage);
+        cp_async_arrive_noinc(bar_gfull + 8 * stage);
         if (++stage == S::kStages) {
           stage = 0;
           phase ^= 1u;

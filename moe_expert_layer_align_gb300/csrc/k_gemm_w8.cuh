@@ -132,6 +132,17 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Pipeline waits as in moe_gemm_kernel: bounded, left early once another
+  // role gave up, and voted across the warp where warp-collective
+  // instructions follow.
+  const uint64_t wait_ns = p.pipe_wait_ns ? p.pipe_wait_ns : kWaitLimitNs;
+  auto thread_wait = [&](uint32_t bar, uint32_t par) {
+    return mbar_wait(bar, par, wait_ns, abort_flag);
+  };
+  auto warp_wait = [&](uint32_t bar, uint32_t par) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, par, wait_ns, abort_flag));
+  };
+  auto warp_aborted = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kRawSlots; ++s) {
@@ -177,10 +188,10 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
     bool ok = true;
     constexpr uint32_t bytes = kW8RawA + S::kRawB;
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, nullptr); ok && it.valid(); it.advance()) {
-      if (*abort_flag) break;
+      if (warp_aborted()) break;
       const WorkUnit w = it.take(p);
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
-        if (!mbar_wait(bar_rempty + 8 * slot, phase ^ 1u)) {
+        if (!warp_wait(bar_rempty + 8 * slot, phase ^ 1u)) {
           report_timeout(p, abort_flag);
           ok = false;
           break;
@@ -208,7 +219,8 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
         }
       }
     }
-    if (*abort_flag && lane == 0) {
+    if (lane == 0) {
+      // drain: our own copies land before the CTA can exit (long limit)
       const long first = issued > S::kRawSlots ? issued - S::kRawSlots : 0;
       for (long i = first; i < issued; ++i)
         mbar_wait(bar_rfull + 8 * static_cast<int>(i % S::kRawSlots),
@@ -227,13 +239,13 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
         const int n_eff = min(BN, max(16, (w.rows + 15) & ~15));
         const uint32_t idesc =
             (S::kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(n_eff >> 3) << 17);
-        if (!mbar_wait(bar_acce + 8 * ab, aph ^ 1u)) {
+        if (!thread_wait(bar_acce + 8 * ab, aph ^ 1u)) {
           report_timeout(p, abort_flag);
           break;
         }
         tc_fence_after();
         for (int kt = w.kt0; kt < w.kt1; ++kt) {
-          if (!mbar_wait(bar_cfull + 8 * cs, cph)) {
+          if (!thread_wait(bar_cfull + 8 * cs, cph)) {
             report_timeout(p, abort_flag);
             ok = false;
             break;
@@ -269,10 +281,9 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
           }
         }
       }
-      if (*abort_flag) {
-        tc_commit(bar_drain);
-        mbar_wait(bar_drain, 0);
-      }
+      // always: another role may give up after our last MMA (long limit)
+      tc_commit(bar_drain);
+      mbar_wait(bar_drain, 0);
     }
     __syncwarp();
   } else if (warp < S::kRoleThreads / 32) {
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
     uint32_t aph = 0;
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, nullptr); it.valid(); it.advance()) {
       const WorkUnit w = it.take(p);
-      if (!mbar_wait(bar_accf + 8 * ab, aph)) {
+      if (!warp_wait(bar_accf + 8 * ab, aph)) {
         report_timeout(p, abort_flag);
         break;
       }
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
     uint32_t rph = 0, cph = 0;
     bool ok = true;
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, nullptr); ok && it.valid(); it.advance()) {
-      if (*abort_flag) break;
+      if (warp_aborted()) break;
       const WorkUnit w = it.take(p);
       const int row = BSRC == kGather ? (up_rows ? p.I + w.mt * 64 : w.mt * 64) : w.mt * kTileM;
       const float* wsp = p.w_scale + (static_cast<size_t>(w.e) * (p.M >> 7) + (row >> 7)) * KB;
@@ -367,7 +378,7 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         const float sc = sc_next;
         if (kt + 1 < w.kt1) sc_next = __ldg(wsp + kt + 1);
-        if (!mbar_wait(bar_rfull + 8 * rs, rph) || !mbar_wait(bar_cempty + 8 * cs, cph ^ 1u)) {
+        if (!warp_wait(bar_rfull + 8 * rs, rph) || !warp_wait(bar_cempty + 8 * cs, cph ^ 1u)) {
           report_timeout(p, abort_flag);
           ok = false;
           break;
@@ -426,7 +437,7 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
         tok[i] = n < w.rows ? assignment_token(row_assign(w.row0 + n), p) : -1;
       }
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
-        if (!mbar_wait(bar_cempty + 8 * cs, cph ^ 1u)) {
+        if (!thread_wait(bar_cempty + 8 * cs, cph ^ 1u)) {
           report_timeout(p, abort_flag);
           ok = false;
           break;

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_index_kernel(RouteInd
     reinterpret_cast<int4*>(idx.tiles)[i] = tile;
   }
   __syncthreads();
-  if (tid == 0 && q.dev_status) *q.dev_status = *sc.flag ? kStatusExpertId : 0;
+  if (tid == 0 && q.dev_status && *sc.flag) atomicOr(q.dev_status, kStatusExpertId);
 }
 
 size_t route_index_smem_bytes(int T, int k, int Ei) {

@@ -253,6 +253,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   }
   p->fused_act = !p->fp8 && p->s1 == 1 && !(o && o->separate_act);
   if (o && (o->unit_order < 0 || o->unit_order > 2)) return MOE_ERR_ARG;
+  if (o && o->pipeline_wait_ns < 0) return MOE_ERR_ARG;
   if (o && o->unit_order) {
     p->ord1 = p->ord2 = o->unit_order;
   } else {
@@ -505,7 +506,7 @@ moe_status moe_align(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E, i
   const int tc = static_cast<int>(tiles_cap_of(T, k, E, block_m));
   IdMap plain{k, k, E, 0, 0};
   return cuda_status(launch_align(topk_ids, T, k, E, block_m, tc, ip, dev_status,
-                                  static_cast<cudaStream_t>(stream), false, plain));
+                                  static_cast<cudaStream_t>(stream), false, plain, true));
 }
 
 moe_status moe_align_ex(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E, int32_t block_m,
@@ -530,7 +531,7 @@ moe_status moe_align_ex(const int32_t* topk_ids, int32_t T, int32_t k, int32_t E
   const int Ei = E + opts->num_shared_experts;
   const int tc = static_cast<int>(tiles_cap_of(T, m.kk, Ei, block_m));
   return cuda_status(launch_align(topk_ids, T, m.kk, Ei, block_m, tc, ip, dev_status,
-                                  static_cast<cudaStream_t>(stream), false, m));
+                                  static_cast<cudaStream_t>(stream), false, m, true));
 }
 
 }  // extern "C"
@@ -561,6 +562,8 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool pdl = !(opts && opts->disable_pdl);
+  const uint64_t wait_ns =
+      (opts && opts->pipeline_wait_ns > 0) ? static_cast<uint64_t>(opts->pipeline_wait_ns) : 0;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto at = [&](int i) { return ws + p.off[i]; };
   IndexPtrs ip{reinterpret_cast<int32_t*>(at(kOffCounts)),     reinterpret_cast<int32_t*>(at(kOffOffsets)),
@@ -617,6 +620,9 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
     gr.out = reinterpret_cast<float*>(at(kOffRouterP));
     gr.rows_cap = p.rp_rows_cap;
     gr.zero_word = p.route_fused ? reinterpret_cast<unsigned int*>(at(kOffCounter)) : nullptr;
+    gr.dev_status = dev_status;
+    gr.clear_status = 1;   // the call's first kernel
+    gr.pipe_wait_ns = wait_ns;
     const int units_r = p.rp_mt * p.rp_splits * (p.rp_rows_cap / p.rp_bn);
     e = launch_gemm_bf16(p.rp_bn, kDense, std::min(sms, units_r), s, chain(), tmR, tmXr, gr);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -661,11 +667,11 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   } else if (p.split_index) {
     e = launch_align_split(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip,
                            reinterpret_cast<int32_t*>(at(kOffIdxScratch)), dev_status, s, chain(),
-                           p.map);
+                           p.map, rc == nullptr);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else if (!p.smem_index) {
     e = launch_align(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s, chain(),
-                     p.map);
+                     p.map, rc == nullptr);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
 
@@ -707,12 +713,14 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.idmap = p.map;
   g1.tiles_cap = p.tiles_cap;
   g1.write_index = p.smem_index;
+  g1.clear_status = p.smem_index && rc == nullptr;   // the Gate-Up is the call's first kernel
   g1.index_out = {ip.counts, ip.offsets, ip.sorted_ids, ip.tile_expert, ip.tiles, ip.inv_pos,
                   ip.num_tiles};
   g1.out = G;
   g1.act_out = p.fused_act ? A : nullptr;
   g1.rows_cap = p.rows_cap;
   g1.dev_status = dev_status;
+  g1.pipe_wait_ns = wait_ns;
   const int units1 = g1.m_tiles * p.s1 * p.tiles_cap;
   e = p.w8 ? launch_gemm_w8(p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13, tmX, g1)
            : launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13,
@@ -752,6 +760,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g2.out = Y;
   g2.rows_cap = p.rows_cap;
   g2.dev_status = dev_status;
+  g2.pipe_wait_ns = wait_ns;
   const int units2 = g2.m_tiles * p.s2 * p.tiles_cap;
   e = p.w8 ? launch_gemm_w8(p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2)
            : launch_gemm(p.fp8, p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2,

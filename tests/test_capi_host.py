@@ -220,3 +220,10 @@ def test_fp8_row_tile_rule():
     # decode sizes keep their narrow tiles
     assert moe.moe_plan(moe.make_shape(64, 7168, 2048, 256, 8, 0, True)).block_m == 16
     assert moe.moe_plan(moe.make_shape(512, 7168, 2048, 256, 8, 0, True)).block_m == 32
+
+
+def test_wait_limit_option_changes_no_plan_and_rejects_negatives():
+    s = moe.make_shape(8, 256, 512, 8, 2)
+    assert moe.moe_workspace_bytes(s, moe.make_opts(pipeline_wait_ns=1)) == moe.moe_workspace_bytes(s)
+    with pytest.raises(moe.MoeError):
+        moe.moe_plan(s, moe.make_opts(pipeline_wait_ns=-5))
