@@ -85,3 +85,58 @@ def test_full_size_layer(cfg, T, n, bases):
     got = layer.out.float().cpu().numpy()[sel]
     want = oracle_layer_sampled(wl, ids, w, sel)
     assert_layer_close(got, want, wl.mode, f"cfg{cfg} T={T} bm={L.block_m}")
+
+
+# Prefill sizes: whole token tiles of the Down output (every row of the tile,
+# so every TMEM lane quadrant and every epilogue warp of both GEMMs is read),
+# for the fullest tile (a full one in the middle of the index where there is
+# one) and the most ragged one.
+TILE_CASES = [(2, 2048), (3, 4096), (4, 4096), (4, 512)]
+
+
+def expert_rows_oracle(wl, e, tokens):
+    """The expert-e output y = W2[e] (SiLU(x W1[e]^T) * x W3[e]^T) of each token
+    (the oracle's layer over expert e alone, k = 1, weight 1; a selection of
+    inputs, no arithmetic)."""
+    n = len(tokens)
+    ids = np.zeros((n, 1), np.int32)
+    w = np.ones((n, 1), np.float32)
+    rows = torch.from_numpy(np.asarray(tokens)).long().to(wl.x.device)
+    x = bits16(wl.x[rows])
+    sl = slice(e, e + 1)
+    if wl.mode == "bf16":
+        return oracle.moe_bf16(x, bits16(wl.w13[sl]), bits16(wl.w2[sl]), ids, w)
+    from helpers import u8
+    xq, xs = oracle.quant_x(x)
+    return oracle.moe_fp8(xq, xs, u8(wl.w13q[sl]), wl.w13s[sl].cpu().numpy(), u8(wl.w2q[sl]),
+                          wl.w2s[sl].cpu().numpy(), ids, w)
+
+
+@pytest.mark.parametrize("cfg,T", TILE_CASES)
+def test_full_size_whole_tiles(cfg, T, bases):
+    import bench
+    import moe_expert_layer_align_gb300 as moe
+    wl = bench.make_workload(cfg, T, "cuda", base=bases(cfg))
+    stream = torch.cuda.Stream()
+    layer = bench.Layer(wl, stream)
+    layer.run()
+    stream.synchronize()
+    assert layer.status.item() == 0
+    v = moe.workspace_views(layer.ws, layer.shape, routed=wl.wr is not None)
+    L = v["layout"]
+    tiles = v["tiles"].cpu().numpy()
+    nt = int(v["num_tiles"].item())
+    sorted_ids = v["sorted_ids"].cpu().numpy()
+    valid = tiles[:nt, 2]
+    full = np.nonzero(valid == L.block_m)[0]
+    fullest = int(full[len(full) // 2]) if len(full) else int(np.argmax(valid))
+    picks = {fullest, int(np.argmin(np.where(valid > 0, valid, 1 << 30)))}
+    Y = v["Y"]
+    for q in sorted(picks):
+        e, r0, nv = int(tiles[q, 0]), int(tiles[q, 1]), int(tiles[q, 2])
+        a = sorted_ids[r0:r0 + nv]
+        assert np.all(a < T * wl.k)
+        got = Y[:, r0:r0 + nv, :].double().sum(0).cpu().numpy()
+        want = expert_rows_oracle(wl, e, a // wl.k)
+        assert_layer_close(got, want, wl.mode,
+                           f"cfg{cfg} T={T} tile {q} (expert {e}, {nv} rows, bm={L.block_m})")
