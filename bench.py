@@ -12,12 +12,14 @@ moe_forward so that host launch cost is not measured.
 
 The JSON line reports the layer latency (us), the roofline fractions, the
 dominant kernel's achieved HBM bandwidth (per-stage CUDA events), the sweep
-over the workload's other token counts, an end-to-end number through host
-buffers, the oracle timed on the host cores, and the SM clocks sampled during
-the timed region.
+over the workload's other token counts, the other workloads at their first
+decode size and largest token count ("workloads": latency, roofline
+fraction, Gate-Up bandwidth, oracle baseline each), an end-to-end number
+through host buffers, the oracle timed on the host cores, and the SM clocks
+sampled during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--T 64]
-                  [--impl reference] [--no-sweep] [--no-cpu] [--ncu]
+                  [--impl reference] [--no-sweep] [--no-workloads] [--no-cpu] [--ncu]
 """
 from __future__ import annotations
 
@@ -204,9 +206,24 @@ def layer_numbers(wl, topk_ids):
                 gateup_bytes=w13_bytes + T * H * bw, down_bytes=w2_bytes)
 
 
-def make_workload(cfg, T, device, base=None):
-    from moe_expert_layer_align_gb300 import workloads
-    return workloads.make(cfg, T, device, base=base)
+def workloads_module():
+    """moe_expert_layer_align_gb300/workloads.py (the seeded input generators)
+    loaded by path, without importing the package, whose __init__ loads the
+    CUDA library: the reference arm draws its inputs with it and runs the
+    oracle alone."""
+    import importlib.util
+    name = "_moe_workloads"
+    if name not in sys.modules:
+        path = os.path.join(ROOT, "moe_expert_layer_align_gb300", "workloads.py")
+        spec = importlib.util.spec_from_file_location(name, path)
+        mod = importlib.util.module_from_spec(spec)
+        sys.modules[name] = mod
+        spec.loader.exec_module(mod)
+    return sys.modules[name]
+
+
+def make_workload(cfg, T, device, base=None, **kw):
+    return workloads_module().make(cfg, T, device, base=base, **kw)
 
 
 class Layer:
@@ -214,9 +231,10 @@ class Layer:
     moe_forward — captured in a CUDA graph.  Router weights are split into
     their two bf16 parts once, before any timing."""
 
-    def __init__(self, wl, stream, opts=None, graph=True, w8a16=False):
+    def __init__(self, wl, stream, opts=None, graph=True, w8a16=False, block_m=0):
         import moe_expert_layer_align_gb300 as moe
         self.moe, self.wl, self.stream, self.opts = moe, wl, stream, opts
+        self.block_m = block_m      # 0: the planner's row tile
         self.w8a16 = w8a16          # FP8 workload's weights with bf16 activations
         dev = wl.x.device
         # The inputs were drawn on the current stream, whose freed blocks the
@@ -237,7 +255,7 @@ class Layer:
             self.hi_lo = None
             self.ids, self.w = wl.topk_ids, wl.topk_w
         out_dtype = torch.float32 if wl.out == "f32" else torch.bfloat16
-        shape = moe.layer_shape(wl.x, self.w13, self.ids, 0, out_dtype, 0, w8a16)
+        shape = moe.layer_shape(wl.x, self.w13, self.ids, block_m, out_dtype, 0, w8a16)
         self.shape = shape
         if self.hi_lo is not None:
             self.plan = moe.moe_plan_routed(shape, opts)
@@ -279,12 +297,13 @@ class Layer:
                                         score_fn=wl.router_fn, scale=wl.router_scale,
                                         scales=self.scales, out=self.out, scores=self.scores,
                                         topk_ids=self.ids, topk_w=self.w, workspace=self.ws,
-                                        dev_status=self.status, stream=self.stream,
-                                        opts=self.opts)
+                                        block_m=self.block_m, dev_status=self.status,
+                                        stream=self.stream, opts=self.opts)
             return
         self.moe.moe_forward(wl.x, self.w13, self.w2, self.ids, self.w, scales=self.scales,
-                             out=self.out, workspace=self.ws, dev_status=self.status,
-                             stream=self.stream, opts=self.opts, w8a16=self.w8a16)
+                             out=self.out, workspace=self.ws, block_m=self.block_m,
+                             dev_status=self.status, stream=self.stream, opts=self.opts,
+                             w8a16=self.w8a16)
 
     def run(self):
         # replay() launches on the current stream: make it ours
@@ -400,35 +419,58 @@ def e2e_time(wl, stream, steps, warmup, w8a16=False):
             "d2h_bytes_per_step": hout.numel() * hout.element_size()}
 
 
-def oracle_baseline(wl, topk_ids, topk_w, budget_s=15.0, max_tokens=None, w8a16=False):
-    """The oracle on the host cores over a bounded sample of the batch's
-    tokens; latency scaled to the whole batch.  (In-path router: its fp64
-    scores over the whole batch are timed and added.)"""
+def _oracle_call(wl, ids, w, sel, w8a16=False):
+    """The oracle's layer over the tokens `sel`: it is fed the sampled x rows
+    and only the experts they route to, ids renumbered into that subset (a
+    selection of inputs, no arithmetic; a token's output depends on nothing
+    else).  Returns a thunk that runs it."""
     import oracle
     from tests.helpers import bits16, u8
+    sel = np.asarray(sel)
+    ids_s = ids[sel]
+    used, inv = np.unique(ids_s, return_inverse=True)
+    ids_c = inv.reshape(ids_s.shape).astype(np.int32)
+    w_s = np.ascontiguousarray(w[sel])
+    dev = wl.x.device
+    rows = torch.from_numpy(sel).long().to(dev)
+    ex = torch.from_numpy(used).long().to(dev)
+    x = bits16(wl.x[rows])
+    if w8a16:
+        args = (x, u8(wl.w13q[ex]), wl.w13s[ex].cpu().numpy(), u8(wl.w2q[ex]),
+                wl.w2s[ex].cpu().numpy(), ids_c, w_s)
+        return lambda: oracle.moe_w8a16(*args)
+    if wl.mode == "bf16":
+        args = (x, bits16(wl.w13[ex]), bits16(wl.w2[ex]), ids_c, w_s)
+        return lambda: oracle.moe_bf16(*args)
+    wq = (u8(wl.w13q[ex]), wl.w13s[ex].cpu().numpy(), u8(wl.w2q[ex]), wl.w2s[ex].cpu().numpy())
+
+    def run():
+        xq, xs = oracle.quant_x(x)          # the layer's own x quantisation, timed
+        return oracle.moe_fp8(xq, xs, *wq, ids_c, w_s)
+    return run
+
+
+def oracle_baseline(wl, topk_ids, topk_w, budget_s=15.0, max_tokens=None, w8a16=False):
+    """The oracle on the host cores over a bounded sample of the batch's
+    tokens (evenly spaced), fed those tokens' rows and experts; latency scaled
+    to the whole batch.  (In-path router: its fp64 scores over the whole batch
+    are timed and added.)"""
+    import oracle
+    from tests.helpers import bits16
     ids = topk_ids.cpu().numpy()
     w = topk_w.cpu().numpy()
-    if w8a16:
-        args = (bits16(wl.x), u8(wl.w13q), wl.w13s.cpu().numpy(), u8(wl.w2q),
-                wl.w2s.cpu().numpy(), ids, w)
-        fn = oracle.moe_w8a16
-    elif wl.mode == "bf16":
-        args = (bits16(wl.x), bits16(wl.w13), bits16(wl.w2), ids, w)
-        fn = oracle.moe_bf16
-    else:
-        xq, xs = oracle.quant_x(bits16(wl.x))
-        args = (xq, xs, u8(wl.w13q), wl.w13s.cpu().numpy(), u8(wl.w2q), wl.w2s.cpu().numpy(),
-                ids, w)
-        fn = oracle.moe_fp8
+    run = _oracle_call(wl, ids, w, [0], w8a16)
     t0 = time.perf_counter()
-    fn(*args, np.array([0], np.int32))
+    run()
     one = time.perf_counter() - t0
     n = int(max(1, min(wl.T, budget_s // max(one, 1e-6))))
     if max_tokens:
         n = min(n, max_tokens)
-    sel = np.linspace(0, wl.T - 1, n).astype(np.int32)
+    sel = np.unique(np.linspace(0, wl.T - 1, n).astype(np.int64))
+    n = len(sel)
+    run = _oracle_call(wl, ids, w, sel, w8a16)
     t0 = time.perf_counter()
-    fn(*args, sel)
+    run()
     dt = time.perf_counter() - t0
     us = dt / n * wl.T * 1e6
     extra = ""
@@ -439,15 +481,15 @@ def oracle_baseline(wl, topk_ids, topk_w, budget_s=15.0, max_tokens=None, w8a16=
         us += r * 1e6
         extra = f"; fp64 router scores of all {wl.T} tokens {r:.3f} s added"
     return {"value": us, "unit": "us", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} of {wl.T} tokens of the T={wl.T} batch (fp64 C oracle, OpenMP); "
-                      f"measured {dt:.2f} s, scaled x{wl.T}/{n}{extra}"}
+            "sample": f"{n} of {wl.T} tokens of the T={wl.T} batch (fp64 C oracle, OpenMP, fed "
+                      f"those tokens' rows and experts); measured {dt:.2f} s, scaled "
+                      f"x{wl.T}/{n}{extra}"}
 
 
 # ---------------------------------------------------------------- arms
 
 def workload_config(cfg, T, wl, nums, extra=None):
-    from moe_expert_layer_align_gb300 import workloads
-    c = workloads.CONFIGS[cfg]
+    c = workloads_module().CONFIGS[cfg]
     d = {"workload": f"{c['name']} MoE layer T={T}", "T": T, "H": wl.H, "I": wl.I, "E": wl.E,
          "k": wl.k, "weights": "e4m3 + fp32 128x128 block scales" if wl.mode == "fp8" else "bf16",
          "routing": "in-path router (two-bf16 split), Zipf(1.2) bias" if wl.wr is not None
@@ -470,7 +512,13 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    wl = make_workload(args.config, args.T, "cpu")
+    # The inputs are drawn exactly as the CUDA arm draws them (the same seeded
+    # generators on the same device, so the same values), then moved to the
+    # host; nothing of the CUDA library is loaded.
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = make_workload(args.config, args.T, gen_dev).to("cpu")
+    if gen_dev == "cuda":
+        torch.cuda.empty_cache()
     if wl.wr is not None:
         ids, w = oracle_routing(wl)
     else:
@@ -504,9 +552,63 @@ def roofline_times(nums, pk, fp8):
     return t_bytes, t_flops
 
 
+# The other workloads, each at its first decode size and its largest token
+# count (workload 4 also with bf16 activations, w8a16), reported beside the
+# headline line.
+WORKLOAD_POINTS = [(1, 8, False), (3, 1, False), (3, 4096, False), (4, 1, False),
+                   (4, 4096, False), (4, 1, True), (4, 4096, True), (5, 4, False),
+                   (5, 256, False)]
+
+
+def workload_points(stream, flush, pk, points, steps=20, warmup=3, cpu_budget_s=2.0):
+    """One entry per (workload, T, w8a16): layer latency, its roofline
+    fraction, the Gate-Up GEMM's event-timed duration and bandwidth (the
+    dominant kernel), and the oracle on the host cores over a bounded token
+    sample.  One full-size weight set is held on the device at a time."""
+    import moe_expert_layer_align_gb300 as moe
+    out = []
+    base_cfg, base = None, None
+    for cfg, T, w8 in points:
+        if cfg != base_cfg:
+            base = None
+            torch.cuda.empty_cache()
+            base = make_workload(cfg, T, "cuda")
+            base_cfg = cfg
+        wl = make_workload(cfg, T, "cuda", base=base)
+        fp8 = wl.mode == "fp8" and not w8
+        L = Layer(wl, stream, w8a16=w8)
+        stream.synchronize()
+        nums = layer_numbers(wl, L.ids)
+        tt, _ = time_layer(L, stream, flush, steps, warmup)
+        us = float(np.mean(tt))
+        tb, tf = roofline_times(nums, pk, fp8)
+        stg = stage_times(wl, stream, flush, 3, w8)
+        gu = stg["gateup"]
+        gu_gbs = nums["gateup_bytes"] / (gu * 1e-6) / 1e9
+        plan = moe.moe_plan(L.shape)
+        cpu = oracle_baseline(wl, L.ids, L.w, budget_s=cpu_budget_s, w8a16=w8)
+        c = workloads_module().CONFIGS[cfg]
+        out.append({
+            "workload": f"{c['name']}{' w8a16' if w8 else ''} MoE layer T={T}", "config": cfg,
+            "T": T, "dtype": "e4m3" if fp8 else ("w8a16" if w8 else "bf16"),
+            "us": us, "us_median": float(np.median(tt)), "active_experts": nums["U"],
+            "block_m": int(plan.block_m), "split_k": [plan.split_gateup, plan.split_down],
+            "hbm_gbs": nums["bytes"] / (us * 1e-6) / 1e9,
+            "tflops": nums["flops"] / (us * 1e-6) / 1e12,
+            "bound": "hbm" if tb >= tf else "tensor", "roofline_us": max(tb, tf),
+            "roofline_frac": max(tb, tf) / us,
+            "gateup_us": gu, "gateup_gbs": gu_gbs, "gateup_frac_of_hbm": gu_gbs / pk["hbm_gbs"],
+            "stages_us": stg, "dev_status": int(L.status.item()),
+            "cpu_baseline": cpu})
+        del L, wl
+    del base
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_cuda(args):
     import moe_expert_layer_align_gb300 as moe  # noqa: F401  (loads the CUDA library)
-    from moe_expert_layer_align_gb300 import workloads
+    workloads = workloads_module()
     ws_, rank, local = dist_env()
     torch.cuda.set_device(local)
     if ws_ > 1:
@@ -570,11 +672,14 @@ def run_cuda(args):
                               "roofline_frac": max(tb, tf) / u})
                 del L2, w2l
         e2e = e2e_time(wl, stream, max(args.steps, 5), args.warmup, w8)
+        others = []
+        if not args.no_workloads:
+            points = [pt for pt in WORKLOAD_POINTS if (pt[0], pt[1], pt[2]) != (cfg, args.T, w8)]
+            others = workload_points(stream, flush, pk, points)
         clk.__exit__()
         clocks = clk.summary()
-        clocks["window"] = "timed region, stage pass, sweep and e2e pass"
-        cpu = None if args.no_cpu else oracle_baseline(wl.to("cpu"), layer.ids, layer.w,
-                                                       w8a16=w8)
+        clocks["window"] = "timed region, stage pass, sweep, e2e pass and other workloads"
+        cpu = None if args.no_cpu else oracle_baseline(wl, layer.ids, layer.w, w8a16=w8)
         plan = moe.moe_plan(layer.shape)
         result = {
             "metric": METRIC, "value": us, "unit": "us", "n_gpus": ws_, "steps": args.steps,
@@ -599,6 +704,7 @@ def run_cuda(args):
             "stages_us": stg,
             "roofline": roof,
             "sweep": sweep,
+            "workloads": others,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,
@@ -623,8 +729,7 @@ def run_ncu(args):
     if args.experts:
         # a small case of the same recipe for multi-pass captures: E experts,
         # the same rows per expert at T * E / E_config tokens
-        from moe_expert_layer_align_gb300 import workloads
-        wl = workloads.make(args.config, args.T, "cuda", E=args.experts)
+        wl = make_workload(args.config, args.T, "cuda", E=args.experts)
     else:
         wl = make_workload(args.config, args.T, "cuda")
     layer = Layer(wl, stream, graph=False, w8a16=args.w8a16)
@@ -645,6 +750,8 @@ def main():
     ap.add_argument("--T", type=int, default=64)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads' lines (the 'workloads' key)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ncu", action="store_true", help="profiler mode (no bench line)")
     ap.add_argument("--experts", type=int, default=0,
