@@ -90,7 +90,17 @@ struct GemmShape {
   // with wide token tiles, where the per-K-block promotion is the busiest
   // role; the second warp of a quadrant then takes the upper half of the
   // columns.
-  static constexpr int kEpiWarps = (FP8 && BN >= 64) ? 8 : 4;   // 16 measured slower (spills)
+  // bf16 with 256-row token tiles and two weight tiles per unit runs token-
+  // major as well: the two 128-row halves of the token tile are the M sides
+  // of two MMAs against one N = 256 operand made of both weight tiles, i.e. a
+  // 256 x 256 tile per CTA staging 64 MACs per operand byte (the 128-row
+  // tiles' 2 x 128 x 128 stage holds 43, and their rate is what the L2-to-SM
+  // bandwidth allows).  The halves' fp32 accumulators fill the 512 TMEM
+  // columns, so there is one set, drained and released per half by four
+  // epilogue warps each; a TMEM lane is a token, so each thread writes its
+  // token's output row with 16-byte stores.
+  static constexpr bool kTok2 = !FP8 && BN == 256 && ME == 2 && BSRC != kDense;
+  static constexpr int kEpiWarps = ((FP8 && BN >= 64) || kTok2) ? 8 : 4;   // 16 measured slower (spills)
   // FP8 with 128-row token tiles runs token-major: the token tile is the
   // MMA's M side and the weight tile its N side.  A TMEM lane is then one
   // token, and both block scales of its K-block partial are per-thread
@@ -107,7 +117,7 @@ struct GemmShape {
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kRoleThreads = 64 + kEpiThreads;   // + TMA and MMA warps
   // token-row gather warps (gathered operand only) and block size
-  static constexpr int kGatherWarps = BSRC == kGather ? (BN >= 64 ? 2 : 1) : 0;
+  static constexpr int kGatherWarps = BSRC == kGather ? (BN >= 256 ? 4 : BN >= 64 ? 2 : 1) : 0;
   static constexpr int kGatherThreads = 32 * kGatherWarps;
   static constexpr int kThreads = kRoleThreads + kGatherThreads;
   static constexpr int kWarps = kThreads / 32;
@@ -122,19 +132,17 @@ struct GemmShape {
   // for bf16 where they fit; for FP8 every 128-wide K block is its own
   // buffer, so keep up to 8 in flight (the MMA would otherwise wait on the
   // epilogue's promotion every other K block).
+  // (kTok2: the two token halves, each with its own full / empty barriers.)
   static constexpr int kAccBufs =
-      FP8 ? (512 / BN < 8 ? 512 / BN : 8) : (512 / (ME * BN) < 2 ? 1 : 2);
-  static constexpr int kTmemCols = (kAccBufs * ME * BN < 32) ? 32 : kAccBufs * ME * BN;
+      kTok2 ? 2 : FP8 ? (512 / BN < 8 ? 512 / BN : 8) : (512 / (ME * BN) < 2 ? 1 : 2);
+  static constexpr int kTmemCols =
+      kTok2 ? 512 : (kAccBufs * ME * BN < 32) ? 32 : kAccBufs * ME * BN;
   static constexpr int kElemsPerStage = FP8 ? 128 : 64;
-  static constexpr uint32_t kIdesc = mma_idesc(FP8 ? 0u : 1u, kTileM, BN);
+  static constexpr uint32_t kIdesc =
+      kTok2 ? mma_idesc(1u, kTileM, ME * kTileM) : mma_idesc(FP8 ? 0u : 1u, kTileM, BN);
   static constexpr int kOffB = kStages * kAStage;
   static constexpr int kOffBar = kOffB + kStages * kBBytes;
-  // full (TMA bytes), empty, accumulator full / empty, drain, and for a
-  // gathered token operand one more ring that the gather threads arrive on
-  // (kept apart from the TMA's so that the TMA warp can wait for its own
-  // copies alone after an abort)
-  static constexpr int kNumBars =
-      2 * kStages + 2 * kAccBufs + 1 + (kGatherThreads > 0 ? kStages : 0);
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 1;  // + drain
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // FP8: the token-operand scales of one K block, double-buffered per
   // epilogue warp: [kEpiWarps][2][its BN * 4 / kEpiWarps columns]
@@ -258,22 +266,24 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
   const uint32_t bar_accf = bar_empty + 8 * S::kStages;
   const uint32_t bar_acce = bar_accf + 8 * S::kAccBufs;
   const uint32_t bar_drain = bar_acce + 8 * S::kAccBufs;
-  const uint32_t bar_gfull = bar_drain + 8;   // gathered rows of stage s landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 4);
+  volatile int* issued_slot = reinterpret_cast<volatile int*>(smem + S::kOffMisc + 8);
   float* sx_buf = reinterpret_cast<float*>(smem + S::kOffScale);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tk = p.T * p.topk;
   // Pipeline waits: bounded by pipe_wait_ns and left early once another role
-  // raised the abort flag.  warp_wait votes the outcome across the warp.
+  // raised the abort flag.  warp_wait votes across the warp (a lane that saw
+  // the abort flag counts as failed), so all its lanes take the same branch.
   const uint64_t wait_ns = p.pipe_wait_ns ? p.pipe_wait_ns : kWaitLimitNs;
   auto thread_wait = [&](uint32_t bar, uint32_t par) {
-    return mbar_wait(bar, par, wait_ns, abort_flag);
+    return mbar_wait_pipe(bar, par, wait_ns, abort_flag);
   };
   auto warp_wait = [&](uint32_t bar, uint32_t par) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, par, wait_ns, abort_flag));
+    const bool r = mbar_wait_pipe(bar, par, wait_ns, abort_flag) && *abort_flag == 0;
+    return __all_sync(0xffffffffu, r);
   };
   auto warp_aborted = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0); };
 
@@ -285,13 +295,14 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     // barrier, which orders it after this store.)
     if (p.clear_status && p.dev_status && blockIdx.x == 0) *p.dev_status = 0;
     for (int s = 0; s < S::kStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);   // the TMA thread's expect-tx arrival
+      // the TMA thread's expect-tx arrival, plus one per gather thread
+      mbar_init(bar_full + 8 * s, 1 + S::kGatherThreads);
       mbar_init(bar_empty + 8 * s, 1);
-      if (S::kGatherThreads > 0) mbar_init(bar_gfull + 8 * s, S::kGatherThreads);
     }
     for (int b = 0; b < S::kAccBufs; ++b) {
       mbar_init(bar_accf + 8 * b, 1);
-      mbar_init(bar_acce + 8 * b, S::kEpiWarps);  // one arrival per epilogue warp
+      // one arrival per epilogue warp (kTok2: per warp of that token half)
+      mbar_init(bar_acce + 8 * b, S::kTok2 ? S::kEpiWarps / 2 : S::kEpiWarps);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -427,6 +438,12 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       }
     }
     if (!b_now) flush_deferred();   // fewer stages than the ring holds
+    if constexpr (S::kGatherThreads > 0) {
+      // The gather threads make up the arrivals they skipped on stages we
+      // issued (after an abort), so that the drain below can complete.
+      if (lane == 0) *issued_slot = static_cast<int>(issued);
+      named_barrier_sync(1, 32 + S::kGatherThreads);
+    }
     if (lane == 0) {
       // Let our own copies land before the CTA can exit (after a normal run
       // every one of them has already been waited for by the MMA thread).
@@ -448,6 +465,49 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); ok && it.valid(); it.advance()) {
         if (*abort_flag) break;
         const WorkUnit w = it.take(p);
+        if constexpr (S::kTok2) {
+          // Both token halves of the previous unit drained, then per stage
+          // the 4 K steps of each half that holds valid rows (a half of
+          // padding rows only is not computed).
+          if (!thread_wait(bar_acce, aph ^ 1u) || !thread_wait(bar_acce + 8, aph ^ 1u)) {
+            report_timeout(p, abort_flag);
+            break;
+          }
+          tc_fence_after();
+          const int halves = w.rows > kTileM ? 2 : 1;
+          for (int kt = w.kt0; kt < w.kt1; ++kt) {
+            if (!thread_wait(bar_full + 8 * stage, phase)) {
+              report_timeout(p, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (BSRC == kGather) fence_proxy_async_smem();
+            const uint64_t wdesc = smem_desc_sw128(sA + stage * S::kAStage);  // 2 x 128 weight rows
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (h < halves) {
+                const uint64_t tdesc =
+                    smem_desc_sw128(sB + stage * S::kBBytes + h * kTileM * kKBytes);
+                const uint32_t d = tmem_base + static_cast<uint32_t>(h * ME * kTileM);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mma_bf16(d, tdesc + 2 * k, wdesc + 2 * k, S::kIdesc, (kt > w.kt0 || k > 0));
+              }
+            }
+            tc_commit(bar_empty + 8 * stage);
+            if (++stage == S::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) {
+            tc_commit(bar_accf);
+            tc_commit(bar_accf + 8);
+            aph ^= 1u;
+          }
+          continue;
+        }
         // The MMA's N is the tile's valid rows rounded up to 16: columns of
         // padding rows are never computed (nor stored), so a wide token tile
         // costs a narrow one's MMA time when few of its rows are valid.
@@ -470,8 +530,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
             }
             tc_fence_after();
           }
-          if (!thread_wait(bar_full + 8 * stage, phase) ||
-              (BSRC == kGather && !thread_wait(bar_gfull + 8 * stage, phase))) {
+          if (!thread_wait(bar_full + 8 * stage, phase)) {
             report_timeout(p, abort_flag);
             ok = false;
             break;
@@ -562,6 +621,81 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     uint32_t aph = 0;
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); it.valid(); it.advance()) {
       const WorkUnit w = it.take(p);
+      if constexpr (S::kTok2) {
+        // Token half h, lanes qd*32.. of it: lane n of the accumulator is row
+        // h*128 + n of the token tile; column j is weight row j of the unit's
+        // two tiles (tile j/128; Gate-Up: rows 32q..32q+15 of a tile gate,
+        // 32q+16.. up, as the weight map stages them).
+        const int h = (warp - 2) >> 2;
+        const int n = h * kTileM + qd * 32 + lane;
+        if (!warp_wait(bar_accf + 8 * h, aph)) {
+          report_timeout(p, abort_flag);
+          break;
+        }
+        tc_fence_after();
+        if (h * kTileM + qd * 32 < w.rows) {   // warp-uniform: the warp holds a valid row
+          const uint32_t tb = t_lane + static_cast<uint32_t>(h * ME * kTileM);
+          const bool live = n < w.rows;
+          if (BSRC == kGather && p.act_out != nullptr) {
+            // SiLU(gate) * up of 16 channels per (tile, quadrant group), as
+            // two 16-byte stores of bf16 into the token's activation row
+            __nv_bfloat16* arow = static_cast<__nv_bfloat16*>(p.act_out) +
+                                  static_cast<size_t>(w.row0 + n) * p.I;
+#pragma unroll 1
+            for (int g = 0; g < ME * 4; ++g) {
+              const int me = g >> 2, q = g & 3;
+              uint32_t gv[16], uv[16];
+              tmem_ld16(tb + static_cast<uint32_t>(me * kTileM + 32 * q), gv);
+              tmem_ld16(tb + static_cast<uint32_t>(me * kTileM + 32 * q + 16), uv);
+              tmem_ld_wait();
+              tmem_ld_bind(gv);
+              tmem_ld_bind(uv);
+              uint32_t pk[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
+                const float a0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(uv[2 * i]);
+                const float a1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(uv[2 * i + 1]);
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+                pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              if (live) {
+                uint4* dst = reinterpret_cast<uint4*>(arow + (w.mt * ME + me) * 64 + 16 * q);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              }
+            }
+          } else {
+            float* orow =
+                p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0 + n) * p.M;
+#pragma unroll 1
+            for (int c = 0; c < ME * kTileM / 16; ++c) {
+              uint32_t v[16];
+              tmem_ld16(tb + static_cast<uint32_t>(c * 16), v);
+              tmem_ld_wait();
+              tmem_ld_bind(v);
+              const int me = c >> 3, j0 = (c & 7) * 16;
+              int col0 = (w.mt * ME + me) * kTileM + j0;
+              if (BSRC == kGather) {
+                const int feat = (w.mt * ME + me) * 64 + 16 * (j0 >> 5);
+                col0 = (j0 & 31) < 16 ? feat : p.I + feat;
+              }
+              if (live && col0 + 16 <= p.M) {
+                float4* dst = reinterpret_cast<float4*>(orow + col0);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                  dst[q4] = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
+                                        __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_acce + 8 * h);
+        aph ^= 1u;
+        continue;
+      }
       if (!FP8) {
         if (!warp_wait(bar_accf + 8 * ab, aph)) {
           report_timeout(p, abort_flag);
@@ -686,10 +820,6 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           if (++ab == S::kAccBufs) {
             ab = 0;
             aph ^= 1u;
-          }
-          if (warp_aborted()) {
-            ok = false;
-            break;
           }
         }
         if (!ok) break;
@@ -817,10 +947,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           cur ^= 1;
           if (lane < kWarpCols) sxw[cur * kWarpCols + lane] = sx_stage;
           __syncwarp();
-          if (!ok || warp_aborted()) {
-            ok = false;
-            break;
-          }
+          if (!ok) break;
         }
         if (!ok) break;
 #pragma unroll
@@ -850,6 +977,7 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     bool ok = true;
     int tok[kR];
     bool tok_ready = false;       // tok[] already holds the current unit's rows
+    long garr = 0;                // stages this thread has arrived on
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); ok && it.valid(); it.advance()) {
       if (*abort_flag) break;
       const WorkUnit w = it.take(p);
@@ -883,7 +1011,8 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
             cp_async_16(b_dst + n * kKBytes + ((c ^ (n & 7)) << 4),
                         src + static_cast<size_t>(tok[i]) * p.b_row_bytes);
         }
-        cp_async_arrive_noinc(bar_gfull + 8 * stage);
+        cp_async_arrive_noinc(bar_full + 8 * stage);
+        ++garr;
         if (++stage == S::kStages) {
           stage = 0;
           phase ^= 1u;
@@ -912,6 +1041,19 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the CTA
+    // Stages the TMA warp issued but this thread skipped (it gave up first):
+    // arrive on them so that their phases, and the TMA warp's drain, can
+    // complete.  Stage i's previous phase (i - kStages) needs no arrival of
+    // ours any more (every thread arrived on it before the TMA warp could
+    // reissue the stage), so wait for it to complete before arriving.
+    named_barrier_sync(1, 32 + S::kGatherThreads);
+    const long issued_total = *issued_slot;
+    for (long i = garr; i < issued_total; ++i) {
+      const int s = static_cast<int>(i % S::kStages);
+      if (i >= S::kStages)
+        mbar_wait(bar_full + 8 * s, static_cast<uint32_t>(((i - S::kStages) / S::kStages) & 1));
+      mbar_arrive(bar_full + 8 * s);
+    }
   }
 
   tc_fence_before();

@@ -137,10 +137,11 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
   // instructions follow.
   const uint64_t wait_ns = p.pipe_wait_ns ? p.pipe_wait_ns : kWaitLimitNs;
   auto thread_wait = [&](uint32_t bar, uint32_t par) {
-    return mbar_wait(bar, par, wait_ns, abort_flag);
+    return mbar_wait_pipe(bar, par, wait_ns, abort_flag);
   };
   auto warp_wait = [&](uint32_t bar, uint32_t par) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, par, wait_ns, abort_flag));
+    const bool r = mbar_wait_pipe(bar, par, wait_ns, abort_flag) && *abort_flag == 0;
+    return __all_sync(0xffffffffu, r);
   };
   auto warp_aborted = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0); };
 
@@ -378,7 +379,11 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
       for (int kt = w.kt0; kt < w.kt1; ++kt) {
         const float sc = sc_next;
         if (kt + 1 < w.kt1) sc_next = __ldg(wsp + kt + 1);
-        if (!warp_wait(bar_rfull + 8 * rs, rph) || !warp_wait(bar_cempty + 8 * cs, cph ^ 1u)) {
+        // both slots ready, one vote for the two waits
+        const bool ready = mbar_wait_pipe(bar_rfull + 8 * rs, rph, wait_ns, abort_flag) &&
+                           mbar_wait_pipe(bar_cempty + 8 * cs, cph ^ 1u, wait_ns, abort_flag) &&
+                           *abort_flag == 0;
+        if (!__all_sync(0xffffffffu, ready)) {
           report_timeout(p, abort_flag);
           ok = false;
           break;

@@ -68,15 +68,21 @@ int64_t tiles_cap_of(int64_t T, int64_t k, int64_t E, int64_t bm) {
 }
 
 // Row tile: the smallest of 16..128 that holds 1.5x the mean rows of an
-// active expert, so that most experts occupy one tile.  (256-row tiles are
-// accepted when asked for, but measured slower than 128 for every workload.)
+// active expert, so that most experts occupy one tile.
 // FP8 takes 128 where this gives 64: 128-row FP8 tiles run token-major with
 // per-thread block scales, cheaper to promote than the swap-AB 64-row tile
 // (DeepSeek-shaped layer at T=1024: 2.23 ms against 2.47 ms).
-int auto_bm(int T, int k, int E, int fp8) {
+// bf16 takes 256 where an active expert holds 384 rows or more on average and
+// both GEMMs pair two weight tiles per unit (`pair`): the 256 x 256 token-major
+// tile then stages 64 MACs per operand byte against the 128-row tiles' 43
+// (Mixtral-shaped layer at T=2048: 1366 -> 1248 us).  With fewer rows per
+// expert its half-empty tiles cost more than it saves (Mixtral-shaped T=512:
+// 572 -> 610 us; Qwen3-shaped T=4096, 256 rows per expert: 495 -> 543 us).
+int auto_bm(int T, int k, int E, int fp8, bool pair) {
   const double tk = static_cast<double>(T) * k;
   const double active = E * (1.0 - std::pow(1.0 - static_cast<double>(k) / E, T));
   const double mean = tk / std::max(1.0, std::min(active, tk));
+  if (!fp8 && pair && mean >= 384) return 256;
   const int cap = 128;
   int bm = 16;
   while (bm < cap && bm < 1.5 * mean) bm *= 2;
@@ -216,7 +222,9 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   p->fp8 = s->mode == MOE_FP8_W8A8;
   p->w8 = s->mode == MOE_W8A16;
   p->out_bf16 = s->out_dtype == MOE_OUT_BF16;
-  p->bm = s->block_m ? s->block_m : auto_bm(p->T, p->k, p->E, p->fp8);
+  const bool pair = !p->fp8 && !p->w8 && !(o && o->single_weight_tile) &&
+                    (s->I / 64) % 2 == 0 && (s->H / 128) % 2 == 0;
+  p->bm = s->block_m ? s->block_m : auto_bm(p->T, p->k, p->E, p->fp8, pair);
   const int64_t tc = tiles_cap_of(p->T, p->k, p->E, p->bm);
   if (tc * p->bm >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
   p->tiles_cap = static_cast<int>(tc);

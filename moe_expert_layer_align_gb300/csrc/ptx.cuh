@@ -44,48 +44,44 @@ MOE_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Non-blocking test of the same phase.
-MOE_DEV bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 MOE_DEV uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase of `parity` to complete; false if `limit_ns` passed or,
-// when `abort` is given, once *abort is nonzero (another role of the CTA gave
-// up: every role then leaves its loop instead of waiting out its own limit).
-// Limits shorter than kWaitLimitNs (a testing aid) poll without blocking and
-// read the clock at every poll; a limit of 1 ns gives up unless the phase is
-// already complete when first tested.
-MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs,
-                       const volatile int* abort = nullptr) {
-  if (limit_ns < kWaitLimitNs) {
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-      if (mbar_test_wait(bar, parity)) return true;
-      if (limit_ns <= 1 || global_timer_ns() - t0 > limit_ns ||
-          (abort != nullptr && *abort != 0))
-        return false;
-    }
-  }
+// Wait for the phase of `parity` to complete; false if kWaitLimitNs passed.
+// (Drains: the waits for a CTA's own copies and MMAs before it exits.)
+MOE_DEV bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u &&
-        (global_timer_ns() - t0 > limit_ns || (abort != nullptr && *abort != 0)))
-      return false;
+    if ((i & 63u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// The slow path of a pipeline wait, out of line: the first try_wait failed.
+// False once `limit_ns` passed or *abort is nonzero (another role of the CTA
+// gave up: every role then leaves its loop instead of waiting out its own
+// limit).  Limits shorter than kWaitLimitNs (a testing aid) read the clock at
+// every poll, and a limit of 1 ns gives up at once.
+static __device__ __noinline__ bool mbar_wait_pipe_slow(uint32_t bar, uint32_t parity,
+                                                 uint64_t limit_ns,
+                                                 const volatile int* abort) {
+  const uint64_t t0 = global_timer_ns();
+  const uint32_t mask = limit_ns < kWaitLimitNs ? 0u : 63u;
+  for (uint32_t i = 1;; ++i) {
+    if (limit_ns <= 1) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & mask) == 0u && (global_timer_ns() - t0 > limit_ns || *abort != 0)) return false;
+  }
+}
+// A pipeline wait (operands landed, stage free, accumulator ready): one
+// try_wait on the fast path, the bounded, abort-watching loop behind it.
+MOE_DEV bool mbar_wait_pipe(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                            const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_pipe_slow(bar, parity, limit_ns, abort);
 }
 
 // ------------------------------------------------------------------ TMA

@@ -277,3 +277,24 @@ def test_unit_orders_are_bitwise_equal(cfg, T, bm, s2):
         outs.append(run_layer(wl, block_m=bm, opts=opts).float().cpu().numpy())
     np.testing.assert_array_equal(outs[0], outs[1])
     assert_layer_close(outs[1], oracle_layer(wl), wl.mode, f"cfg{cfg} T={T} bm={bm}")
+
+
+@pytest.mark.parametrize("T,E,kw", [
+    (300, 4, dict(H=512, I=256)),     # one 256-row tile per expert, its second half ragged
+    (700, 3, dict(H=256, I=384)),     # a full 256-row tile and a ragged one per expert
+    (100, 4, dict(H=384, I=128)),     # at most 128 valid rows: second half never computed
+])
+@pytest.mark.parametrize("split", [False, True])
+def test_token_major_256_row_tiles(T, E, kw, split):
+    """bf16 with 256-row token tiles and two weight tiles per unit: the
+    token-major 256 x 256 tile (two M = 128 halves against one N = 256
+    weight operand), fused SiLU-and-mul or, with a split Gate-Up, fp32
+    partial rows."""
+    import moe_expert_layer_align_gb300 as moe
+    wl = small(2, T, E=E, **kw)
+    opts = moe.make_opts(split_gateup=2, separate_act=True) if split else None
+    shape = moe.layer_shape(wl.x, wl.w13, wl.topk_ids, 256, torch.bfloat16)
+    L = moe.moe_plan(shape, opts)
+    assert L.block_m == 256 and (L.weight_tiles_per_unit & 0xff) == 2
+    got = run_layer(wl, block_m=256, opts=opts).float().cpu().numpy()
+    assert_layer_close(got, oracle_layer(wl), "bf16", f"T={T} E={E} {kw} split={split}")
