@@ -271,7 +271,7 @@ class Layer:
         # or align[, x-quant]; Gate-Up; [act]; Down; combine
         L = self.plan
         quant = 1 if (self.fp8 and not w8a16) else 0
-        front = (2 if L.route_fused else 3 + quant) if self.hi_lo is not None \
+        front = (1 if L.route_fused else 3 + quant) if self.hi_lo is not None \
             else (0 if L.smem_index else 1) + quant
         self.kernels_per_step = front + 3 + (0 if L.fused_act else 1)
         if graph:
@@ -338,8 +338,9 @@ def stage_times(wl, stream, flush, steps, w8a16=False):
     """Per-stage device time (us) from events recorded between the stages,
     captured with the layer in a CUDA graph (recording events between stages
     serialises them: PDL overlap is lost in this pass).  With the router in
-    the path, "router" is its GEMM and "align" the fused routing kernel (top-k,
-    x-quant and index) where the plan fuses them."""
+    the path, "router" is the fused routing launch (router GEMM, top-k, x-quant
+    and index; "align" and "quant_x" are then empty) or, with separate
+    kernels, the router GEMM alone ("align" then holds the top-k too)."""
     import moe_expert_layer_align_gb300 as moe
     n = len(moe.STAGES) + 1
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
@@ -606,6 +607,66 @@ def workload_points(stream, flush, pk, points, steps=20, warmup=3, cpu_budget_s=
     return out
 
 
+# The router-GEMM table of the "HPC-Ops × SGLang" post (section "Router GEMM",
+# Table 2: H20, K = 4096, N = 192, BF16 x FP32 -> FP32, their kernel), us per
+# call: context for the router line, measured on other hardware.
+ROUTER_TABLE_H20_US = {1: 11.200, 16: 11.744, 48: 12.144, 96: 13.904, 208: 17.088,
+                       512: 26.992, 1024: 50.640, 2048: 76.688, 4096: 141.120}
+
+
+class _Replay:
+    """A captured CUDA graph of one call, replayed on `stream` (time_layer's
+    step)."""
+
+    def __init__(self, fn, stream):
+        self.stream = stream
+        with torch.cuda.stream(stream):
+            fn()                                  # warm the launch path before capture
+        stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            fn()
+        stream.synchronize()
+
+    def run(self):
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
+
+
+def router_points(stream, flush, pk, steps=20, warmup=3):
+    """The router alone (moe_router_topk: the two-bf16 GEMM on the tensor cores
+    and the softmax top-k) at the router-GEMM table shape over its token
+    counts: latency, roofline fraction, the pages' H20 figure for context."""
+    import moe_expert_layer_align_gb300 as moe
+    W = workloads_module()
+    H, E, k = W.ROUTER_SHAPE["H"], W.ROUTER_SHAPE["E"], W.ROUTER_SHAPE["k"]
+    _, wr = W.router_inputs(1, "cuda")
+    hi_lo = moe.moe_router_prepare(wr, stream=stream)
+    stream.synchronize()
+    out = []
+    for M in W.ROUTER_SHAPE["sweep"]:
+        x, _ = W.router_inputs(M, "cuda")
+        stream.wait_stream(torch.cuda.current_stream())
+        sc = torch.empty((M, E), dtype=torch.float32, device="cuda")
+        ids = torch.empty((M, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((M, k), dtype=torch.float32, device="cuda")
+        ws = torch.empty(max(16, moe.moe_router_workspace_bytes(M, H, E)), dtype=torch.uint8,
+                         device="cuda")
+        r = _Replay(lambda: moe.moe_router_topk(x, hi_lo, k, scores=sc, topk_ids=ids, topk_w=w,
+                                                workspace=ws, stream=stream), stream)
+        tt, _ = time_layer(r, stream, flush, steps, warmup)
+        us = float(np.median(tt))
+        nbytes = 2 * E * H * 2 + M * H * 2 + M * E * 4 + M * k * 8
+        flops = 2 * M * 2 * E * H
+        tb = nbytes / (pk["hbm_gbs"] * 1e9) * 1e6
+        tf = flops / (pk["bf16_tflops"] * 1e12) * 1e6
+        out.append({"M": M, "K": H, "N": E, "k": k, "us": us,
+                    "tflops": flops / (us * 1e-6) / 1e12, "hbm_gbs": nbytes / (us * 1e-6) / 1e9,
+                    "roofline_frac": max(tb, tf) / us, "page_table_h20_us": ROUTER_TABLE_H20_US[M]})
+        del r, x, sc, ids, w, ws
+    return out
+
+
 def run_cuda(args):
     import moe_expert_layer_align_gb300 as moe  # noqa: F401  (loads the CUDA library)
     workloads = workloads_module()
@@ -672,10 +733,11 @@ def run_cuda(args):
                               "roofline_frac": max(tb, tf) / u})
                 del L2, w2l
         e2e = e2e_time(wl, stream, max(args.steps, 5), args.warmup, w8)
-        others = []
+        others, router = [], []
         if not args.no_workloads:
             points = [pt for pt in WORKLOAD_POINTS if (pt[0], pt[1], pt[2]) != (cfg, args.T, w8)]
             others = workload_points(stream, flush, pk, points)
+            router = router_points(stream, flush, pk)
         clk.__exit__()
         clocks = clk.summary()
         clocks["window"] = "timed region, stage pass, sweep, e2e pass and other workloads"
@@ -705,6 +767,10 @@ def run_cuda(args):
             "roofline": roof,
             "sweep": sweep,
             "workloads": others,
+            "router": {"what": "moe_router_topk (two-bf16 router GEMM + softmax top-8) at the "
+                               "router-GEMM table shape K=4096, N=192; page_table_h20_us: the "
+                               "pages' H20 figure (GEMM alone), context only",
+                       "points": router},
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,

@@ -151,11 +151,15 @@ typedef struct {
    * and flagged).  The output is this rank's partial sum.  0 = off. */
   int32_t ep_first_expert;
   int32_t ep_num_experts;
-  /* moe_forward_routed: 1 = run the router's top-k, the FP8 quantisation of x
-   * and the routing index as one grid (up to 2048 assignments) instead of
-   * three kernels.  Bit-identical results; measured slower on the Zipf-routed
-   * Qwen3-shaped FP8 layer at T=64 (its last CTA builds the index alone after
-   * every token's top-k), so off by default. */
+  /* moe_forward_routed: how the router's GEMM, top-k, the FP8 quantisation
+   * of x and the routing index run.  1: as one cooperative launch (the
+   * router GEMM on the tensor cores, then, after a grid barrier, each CTA's
+   * block of tokens: top-k and per-expert counts, with x-quant on the CTAs
+   * the GEMM leaves free, then, after a second barrier, its block's rows of
+   * the index), preceded by an 8-byte memset of its barrier counters.
+   * 0 (default) or -1: as separate PDL-chained kernels (router GEMM, top-k,
+   * index, x-quant), measured faster on the Zipf-routed Qwen3-shaped FP8
+   * layer at every token count tried.  Bit-identical results. */
   int32_t fuse_routing;
   /* Order in which each persistent GEMM walks its work units (weight tile x
    * split x token tile).  0: planner.  1: weight-tile-major (the units of
@@ -209,8 +213,9 @@ typedef struct {
   size_t off_as;   /* FP8: fp32 act scales   [rows_cap][I/128]              */
   size_t off_y;    /* fp32 Down partials     [S2][rows_cap][H] (sorted rows)*/
   size_t off_router;        /* moe_forward_routed: router GEMM partial sums   */
-  size_t off_route_counter; /* moe_forward_routed: ticket counter (4 bytes)   */
+  size_t off_route_counter; /* fused routing: two grid-barrier counters (8 bytes) */
   size_t total_bytes;
+  size_t off_route_hist;    /* fused routing: per-CTA expert counts           */
 } moe_workspace_layout;
 
 /* tiles_cap of the index for these sizes (0 on invalid arguments). */
@@ -293,16 +298,17 @@ MOE_API moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t r
 /* The layer with its router in the path (HPC-Ops × SGLang, section "Router
  * GEMM" feeding section "MoE"): the two-bf16 router GEMM over hi_lo (from
  * moe_router_prepare) scores x, its top-k becomes the layer's routing, and the
- * layer runs as in moe_forward — one chain of launches on `stream`.  With
- * opts->fuse_routing and up to 2048 assignments the router's top-k, the FP8
- * quantisation of x and the routing index run as one grid (whose last CTA to
- * finish builds the index) instead of three launches.  Outputs besides `out`: scores fp32 [T][E],
+ * layer runs as in moe_forward — one chain of launches on `stream`, whose
+ * front (router GEMM, top-k, FP8 quantisation of x, routing index) is four
+ * PDL-chained kernels or, on request, one cooperative grid
+ * (moe_forward_opts.fuse_routing).  Outputs besides `out`: scores fp32 [T][E],
  * topk_ids int32 [T][k], topk_w fp32 [T][k] (caller-owned).  score_fn and
  * scale as in moe_router_topk; router shapes as moe_router_workspace_bytes
  * accepts (E a multiple of 64, k <= 32).  Not combined with shared experts,
  * expert parallelism or the shared-memory index (MOE_ERR_SHAPE).  The
  * workspace is sized by moe_routed_workspace_bytes / moe_plan_routed (the
- * router's partial sums and a 4-byte ticket counter are added). */
+ * router's partial sums and, fused, the barrier counters and per-CTA expert
+ * counts are added). */
 MOE_API moe_status moe_plan_routed(const moe_shape* shape, const moe_forward_opts* opts,
                            moe_workspace_layout* layout);
 MOE_API size_t moe_routed_workspace_bytes(const moe_shape* shape, const moe_forward_opts* opts);

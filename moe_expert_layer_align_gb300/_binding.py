@@ -63,7 +63,7 @@ class moe_workspace_layout(ctypes.Structure):
         (n, _sz) for n in ("off_counts", "off_offsets", "off_sorted_ids", "off_tile_expert",
                            "off_tiles", "off_inv_pos", "off_num_tiles", "off_index_scratch", "off_xq", "off_xs",
                            "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "off_router",
-                           "off_route_counter", "total_bytes")]
+                           "off_route_counter", "total_bytes", "off_route_hist")]
 
 
 def _load() -> ctypes.CDLL:
@@ -159,12 +159,13 @@ def moe_index_tiles_cap(T, k, E, block_m) -> int:
 def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
               stage_events=None, separate_act=False, smem_index=None,
               single_weight_tile=False, num_shared_experts=0, shared_expert_weight=0.0,
-              ep_first_expert=0, ep_num_experts=0, fuse_routing=False,
+              ep_first_expert=0, ep_num_experts=0, fuse_routing=None,
               unit_order=0, pipeline_wait_ns=0) -> moe_forward_opts:
     o = moe_forward_opts()
     o.pipeline_wait_ns = pipeline_wait_ns
     o.unit_order = unit_order
-    o.fuse_routing = int(fuse_routing)
+    # None: planner (separate kernels); True / False: one cooperative launch / separate
+    o.fuse_routing = 0 if fuse_routing is None else (1 if fuse_routing else -1)
     o.num_shared_experts = num_shared_experts
     o.shared_expert_weight = shared_expert_weight
     o.ep_first_expert = ep_first_expert

@@ -77,9 +77,10 @@ struct IndexScratch {
   int32_t* offs;   // [E + 1]: padded offsets
   int32_t* tot;    // [E]: per-expert counts
   int32_t* flag;   // [1]: an invalid id was seen
+  int32_t* wsum;   // [33]: per-warp sums of the offset scan, then its total
   int remote_ok;   // kRemoteId entries are another rank's: dropped, not flagged
   static __host__ __device__ constexpr size_t words(int nwarps, int E) {
-    return static_cast<size_t>(nwarps) * E + (E + 1) + E + 1;
+    return static_cast<size_t>(nwarps) * E + (E + 1) + E + 1 + 33;
   }
   __device__ void carve(int32_t* base, int nwarps, int E, int remote = 0) {
     remote_ok = remote;
@@ -87,6 +88,7 @@ struct IndexScratch {
     offs = cnt + nwarps * E;
     tot = offs + E + 1;
     flag = tot + E;
+    wsum = flag + 1;
   }
 };
 
@@ -100,28 +102,44 @@ __device__ __forceinline__ int index_warps(int tk) {
   return need < 1 ? 1 : (need < nwarps ? need : nwarps);
 }
 
-// offs[0..E] = exclusive prefix of tot[] rounded up to multiples of bm (warp
-// 0; each lane a run of experts).  Ends with a block barrier.
+// offs[0..E] = exclusive prefix of tot[] rounded up to multiples of bm (a
+// power of two, as the host checks): one expert per thread, a shuffle scan
+// per warp and one over the warps' sums, blockDim.x experts at a time.  (A
+// single warp walking the experts with divisions took ~2-4 us for 128
+// experts.)  Ends with a block barrier.
 __device__ __forceinline__ void index_scan_offsets(int E, int bm, const IndexScratch& sc) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 0) {
-    const int per = (E + 31) / 32;
-    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int sum = 0;
-    for (int e = e0; e < e1; ++e) sum += (sc.tot[e] + bm - 1) / bm * bm;
-    int incl = sum;
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int warp = tid >> 5, lane = tid & 31, nw = nthreads >> 5;
+  const int mask = bm - 1;
+  int carry = 0;   // padded rows of the experts before this round's
+  for (int e0 = 0; e0 < E; e0 += nthreads) {
+    const int e = e0 + tid;
+    const int v = e < E ? (sc.tot[e] + mask) & ~mask : 0;
+    int incl = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int o = __shfl_up_sync(0xffffffffu, incl, d);
       if (lane >= d) incl += o;
     }
-    int run = incl - sum;
-    for (int e = e0; e < e1; ++e) {
-      sc.offs[e] = run;
-      run += (sc.tot[e] + bm - 1) / bm * bm;
+    if (lane == 31) sc.wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int x = lane < nw ? sc.wsum[lane] : 0;
+      int xi = x;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, xi, d);
+        if (lane >= d) xi += o;
+      }
+      if (lane < nw) sc.wsum[lane] = xi - x;   // exclusive warp bases
+      if (lane == 31) sc.wsum[32] = xi;        // this round's total
     }
-    if (lane == 31) sc.offs[E] = incl;
+    __syncthreads();
+    if (e < E) sc.offs[e] = carry + sc.wsum[warp] + incl - v;
+    carry += sc.wsum[32];
+    __syncthreads();   // wsum is rewritten by the next round
   }
+  if (tid == 0) sc.offs[E] = carry;
   __syncthreads();
 }
 
@@ -190,13 +208,13 @@ __device__ __forceinline__ void index_scatter(const int32_t* src, int tk, int E,
   }
 }
 
-// Padding rows of every expert interval, then the tail [offs[E], rows_end).
+// Padding rows of every expert interval (a thread per expert: fewer than bm
+// rows each), then the tail [offs[E], rows_end).
 template <class PadFn>
 __device__ __forceinline__ void index_pads(int E, int rows_end, const IndexScratch& sc, PadFn pad) {
-  const int tid = threadIdx.x, nthreads = blockDim.x, nwarps = nthreads >> 5;
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int e = warp; e < E; e += nwarps)
-    for (int pos = sc.offs[e] + sc.tot[e] + lane; pos < sc.offs[e + 1]; pos += 32) pad(pos);
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  for (int e = tid; e < E; e += nthreads)
+    for (int pos = sc.offs[e] + sc.tot[e]; pos < sc.offs[e + 1]; ++pos) pad(pos);
   for (int pos = sc.offs[E] + tid; pos < rows_end; pos += nthreads) pad(pos);
 }
 

@@ -65,7 +65,6 @@ struct GemmParams {
   struct {                   // expert-id status bit to dev_status
     int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
   } index_out;
-  unsigned int* zero_word;   // if set, CTA 0 zeroes it at start (the next kernel's ticket counter)
   int clear_status;          // first kernel of the call: CTA 0 zeroes dev_status at start
   int early_weights;         // contiguous token operand: stream weights before the wait
   uint64_t pipe_wait_ns;     // limit of the pipeline waits (0: kWaitLimitNs); drains keep
@@ -129,8 +128,10 @@ cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H,
 cudaError_t launch_router_prepare(const float* wr, int E, int H, void* hi_lo,
                                   cudaStream_t st);
 
-// Router top-k + FP8 x-quant + routing index in one grid (k_route.cu).
-struct RouteIndexParams {
+// The in-path router GEMM, its top-k, the FP8 x-quant and the routing index
+// in one cooperative launch (k_route.cu).  The router GEMM's GemmParams are
+// passed beside these.
+struct RouteFrontParams {
   const float* P;            // router GEMM split-K partials [splits][rows_cap_r][2E]
   int splits, rows_cap_r, T, E, k, score_fn;
   float scale;
@@ -144,10 +145,15 @@ struct RouteIndexParams {
   int Ei, bm, tiles_cap;     // index: experts, row tile, tiles
   IndexPtrs idx;
   int32_t* dev_status;
-  unsigned int* counter;     // ticket counter, zero at launch
+  int owners, tpc;           // CTAs that own tokens, and tokens per owner
+  int gemm_ctas;             // CTAs running router-GEMM units (the others quantise x)
+  int32_t* hist;             // [owners][Ei] per-owner expert counts
+  unsigned int* bar;         // two grid-barrier counters, zero at launch
 };
-size_t route_index_smem_bytes(int T, int k, int Ei);
-cudaError_t launch_route_index(const RouteIndexParams& q, cudaStream_t st, bool pdl);
+size_t route_front_smem_bytes(int bn, int tpc, int k, int Ei);
+cudaError_t launch_route_front(int bn, int grid, cudaStream_t st, const CUtensorMap& tmW,
+                               const CUtensorMap& tmX, const GemmParams& gp,
+                               const RouteFrontParams& q);
 cudaError_t launch_router_topk(const float* P, int splits, int rows_cap, int T, int E,
                                int k, int score_fn, float scale, float* scores,
                                int32_t* ids, float* w, cudaStream_t st, bool pdl);

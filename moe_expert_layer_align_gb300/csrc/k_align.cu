@@ -15,7 +15,6 @@ namespace moe {
 // threads for small batches measured slower: the per-expert loops get longer
 // than the barriers get cheaper.)
 constexpr int kAlignThreads = 1024;
-constexpr int kAlignWarps = kAlignThreads / 32;
 constexpr int kAlignMaxStagedIds = 32768;  // ids staged in shared memory up to this many
 
 __global__ void __launch_bounds__(kAlignThreads)

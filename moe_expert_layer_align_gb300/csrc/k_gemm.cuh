@@ -251,12 +251,14 @@ __device__ __forceinline__ void report_timeout(const GemmParams& p, volatile int
   if (p.dev_status) atomicOr(p.dev_status, kStatusTimeout);
 }
 
+// The persistent GEMM as run by one CTA of S::kThreads threads with the
+// dynamic shared memory at smem_raw: the body of moe_gemm_kernel, and the
+// first phase of the fused routing kernel (k_route.cu), which goes on with
+// the same CTAs after it returns.
 template <int FP8, int BN, int BSRC, int ME>
-__global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+__device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                         const GemmParams& p, uint8_t* smem_raw) {
   using S = GemmShape<FP8, BN, BSRC, ME>;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sA = smem_u32(smem);
@@ -288,7 +290,6 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
   auto warp_aborted = [&]() { return __any_sync(0xffffffffu, *abort_flag != 0); };
 
   if (threadIdx.x == 0) {
-    if (p.zero_word && blockIdx.x == 0) *p.zero_word = 0u;
     // First kernel of the call: clear the status word before any bit is set.
     // (A timeout bit of another CTA comes at least kWaitLimitNs after the
     // grid started; CTA 0's own expert-id bit is ORed in after the prologue
@@ -638,7 +639,13 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
           const bool live = n < w.rows;
           if (BSRC == kGather && p.act_out != nullptr) {
             // SiLU(gate) * up of 16 channels per (tile, quadrant group), as
-            // two 16-byte stores of bf16 into the token's activation row
+            // two 16-byte stores of bf16 into the token's activation row.
+            // This epilogue runs between units (one accumulator set), so
+            // SiLU uses the fast exponential and division intrinsics
+            // (relative error ~1e-6, far below the bf16 rounding of the
+            // result; a very negative gate still gives 0) instead of expf
+            // and an IEEE division: the epilogue's 128 SiLUs per thread and
+            // unit are otherwise ~10 % of the unit's MMA time.
             __nv_bfloat16* arow = static_cast<__nv_bfloat16*>(p.act_out) +
                                   static_cast<size_t>(w.row0 + n) * p.I;
 #pragma unroll 1
@@ -654,8 +661,8 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const float g0 = __uint_as_float(gv[2 * i]), g1 = __uint_as_float(gv[2 * i + 1]);
-                const float a0 = g0 / (1.0f + expf(-g0)) * __uint_as_float(uv[2 * i]);
-                const float a1 = g1 / (1.0f + expf(-g1)) * __uint_as_float(uv[2 * i + 1]);
+                const float a0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(uv[2 * i]);
+                const float a1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(uv[2 * i + 1]);
                 const __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
                 pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
               }
@@ -1062,6 +1069,14 @@ __global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, S::kTmemCols);
   }
+}
+
+template <int FP8, int BN, int BSRC, int ME>
+__global__ void __launch_bounds__(GemmShape<FP8, BN, BSRC, ME>::kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  gemm_cta<FP8, BN, BSRC, ME>(tmA, tmB, p, smem_raw);
 }
 
 template <int FP8, int BN, int BSRC, int ME = 1>

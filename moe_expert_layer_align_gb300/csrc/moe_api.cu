@@ -25,6 +25,14 @@ constexpr int kMaxSplits = 32;
 constexpr int kSmemIndexMaxAssignments = 4096;
 // Above this many assignments the index is built over chunks by several CTAs.
 constexpr int kSplitIndexMinAssignments = 2048;
+// Router GEMM split-K count bound (the top-k sums at most this many partials).
+constexpr int kRouterMaxSplitsHost = 4;
+
+enum {
+  kOffCounts, kOffOffsets, kOffSorted, kOffTileExpert, kOffTiles, kOffInvPos, kOffNumTiles,
+  kOffIdxScratch, kOffXq, kOffXs, kOffXsRows, kOffG, kOffA, kOffAs, kOffY, kOffRouterP,
+  kOffCounter, kOffRouteHist, kNumOff
+};
 
 struct Plan {
   // k, E: assignments per token and experts of the index and the weights
@@ -40,20 +48,15 @@ struct Plan {
   int fused_act;           // SiLU-and-mul in the Gate-Up epilogue
   int ord1, ord2;          // unit order per GEMM: 1 weight-tile-major, 2 token-tile-major
   int smem_index;          // GEMM CTAs rebuild the index in shared memory
-  size_t off[17];
+  size_t off[kNumOff];
   int split_index;         // index built by the count / scan / scatter kernels
   size_t total;
   // in-path router (moe_forward_routed)
   int routed;
-  int route_fused;         // router top-k, x-quant and index in one grid
+  int route_fused;         // router GEMM, top-k, x-quant and index in one launch
   int rp_bn, rp_rows_cap, rp_splits, rp_kts, rp_kt, rp_mt;
   size_t rp_bytes;
-};
-
-enum {
-  kOffCounts, kOffOffsets, kOffSorted, kOffTileExpert, kOffTiles, kOffInvPos, kOffNumTiles,
-  kOffIdxScratch, kOffXq, kOffXs, kOffXsRows, kOffG, kOffA, kOffAs, kOffY, kOffRouterP,
-  kOffCounter, kNumOff
+  int rp_owners_cap;       // fused routing: most token-owning CTAs (histogram rows)
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -289,9 +292,15 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   }
   // many assignments: build the index over chunks, one CTA each
   p->split_index = !p->smem_index && static_cast<int64_t>(p->T) * p->k > kSplitIndexMinAssignments;
-  // in-path router with few assignments: top-k, x-quant and index in one grid
-  p->route_fused = p->routed && o && o->fuse_routing && !p->split_index && p->map.plain() &&
-                   route_index_smem_bytes(p->T, p->k, p->E) <= 128 * 1024;
+  // in-path router: its GEMM, top-k, x-quant and index in one cooperative
+  // launch on request (fuse_routing 1).  The planner (0) and -1 keep the
+  // separate PDL-chained kernels: measured faster on the Zipf-routed layer
+  // (T=4: 54.7 against 62.0 us; T=64: 97.1 against 104.8 us), because PDL
+  // hides each separate kernel's launch behind its predecessor while the
+  // single grid pays its memset, its two grid barriers and a longer tail.
+  if (o && (o->fuse_routing < -1 || o->fuse_routing > 1)) return MOE_ERR_ARG;
+  p->route_fused = p->routed && p->map.plain() && o && o->fuse_routing == 1;
+  p->rp_owners_cap = std::min((p->T + 5) / 6, kPlanCtas);
   // workspace layout
   const size_t tk = static_cast<size_t>(p->T) * p->k;
   const size_t rc = p->rows_cap;
@@ -312,7 +321,8 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
       p->fp8 ? 4 * rc * (s->I / 128) : 0,
       4 * static_cast<size_t>(p->s2) * rc * s->H,
       p->routed ? p->rp_bytes : 0,
-      p->routed ? 4u : 0u,
+      p->route_fused ? 8u : 0u,
+      p->route_fused ? 4 * static_cast<size_t>(p->rp_owners_cap) * p->E : 0,
   };
   size_t cur = 0;
   for (int i = 0; i < kNumOff; ++i) {
@@ -346,6 +356,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->unit_order = p.ord1 | (p.ord2 << 8);
   L->off_router = p.off[kOffRouterP];
   L->off_route_counter = p.off[kOffCounter];
+  L->off_route_hist = p.off[kOffRouteHist];
   L->off_index_scratch = p.off[kOffIdxScratch];
   L->off_xq = p.off[kOffXq];
   L->off_xs = p.off[kOffXs];
@@ -468,7 +479,8 @@ bool router_plan(int T, int H, int E, RouterPlan* r) {
   r->kt = H / 64;
   r->mt = 2 * E / 128;
   // few splits: every score sums its partials in the top-k kernel
-  choose_split(r->mt, r->kt, r->rows_cap / r->bn, r->bn, &r->splits, &r->kts, 4);
+  choose_split(r->mt, r->kt, r->rows_cap / r->bn, r->bn, &r->splits, &r->kts,
+               kRouterMaxSplitsHost);
   r->bytes = 4ull * r->splits * r->rows_cap * 2 * E;
   return true;
 }
@@ -610,8 +622,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   };
 
   if (rc) {
-    // router GEMM over [hi; lo] (dense token rows); it also zeroes the ticket
-    // counter of the fused routing kernel that follows
+    // router GEMM over [hi; lo] (dense token rows)
     record(opts, 7, s);
     CUtensorMap tmR, tmXr;
     if (!make_map_3d(&tmR, rc->hi_lo, 2, p.H, 2ull * p.map.E, 1, 128) ||
@@ -627,17 +638,20 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
     gr.dense_rows = p.T;
     gr.out = reinterpret_cast<float*>(at(kOffRouterP));
     gr.rows_cap = p.rp_rows_cap;
-    gr.zero_word = p.route_fused ? reinterpret_cast<unsigned int*>(at(kOffCounter)) : nullptr;
     gr.dev_status = dev_status;
     gr.clear_status = 1;   // the call's first kernel
     gr.pipe_wait_ns = wait_ns;
     const int units_r = p.rp_mt * p.rp_splits * (p.rp_rows_cap / p.rp_bn);
-    e = launch_gemm_bf16(p.rp_bn, kDense, std::min(sms, units_r), s, chain(), tmR, tmXr, gr);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    record(opts, 0, s);
     if (p.route_fused) {
-      RouteIndexParams q = {};
-      q.P = reinterpret_cast<const float*>(at(kOffRouterP));
+      // one cooperative grid: the router GEMM, then the top-k / x-quant /
+      // index phases on owner CTAs of tpc tokens each
+      // a token per warp of an owner (six warps), more where the owners would
+      // outnumber the SMs; the grid also covers the x-quant at eight
+      // 128-channel groups per warp
+      const int tpc = std::max(6, (p.T + std::min(sms, p.rp_owners_cap) - 1) /
+                                      std::min(sms, p.rp_owners_cap));
+      RouteFrontParams q = {};
+      q.P = gr.out;
       q.splits = p.rp_splits;
       q.rows_cap_r = p.rp_rows_cap;
       q.T = p.T;
@@ -657,10 +671,22 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
       q.tiles_cap = p.tiles_cap;
       q.idx = ip;
       q.dev_status = dev_status;
-      q.counter = reinterpret_cast<unsigned int*>(at(kOffCounter));
-      e = launch_route_index(q, s, chain());
+      q.tpc = tpc;
+      q.owners = (p.T + tpc - 1) / tpc;
+      q.hist = reinterpret_cast<int32_t*>(at(kOffRouteHist));
+      q.bar = reinterpret_cast<unsigned int*>(at(kOffCounter));
+      if (cudaMemsetAsync(q.bar, 0, 8, s) != cudaSuccess) return MOE_ERR_CUDA;
+      first = false;   // the memset orders the grid after earlier work on the stream
+      const int quant_ctas = p.fp8 ? (p.T * (p.H / 128) + 47) / 48 : 0;
+      const int grid = std::min(sms, std::max(units_r + quant_ctas, q.owners));
+      q.gemm_ctas = std::min(units_r, grid);
+      e = launch_route_front(p.rp_bn, grid, s, tmR, tmXr, gr, q);
       if (e != cudaSuccess) return MOE_ERR_CUDA;
+      record(opts, 0, s);
     } else {
+      e = launch_gemm_bf16(p.rp_bn, kDense, std::min(sms, units_r), s, chain(), tmR, tmXr, gr);
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      record(opts, 0, s);
       e = launch_router_topk(reinterpret_cast<const float*>(at(kOffRouterP)), p.rp_splits,
                              p.rp_rows_cap, p.T, p.map.E, p.k, rc->score_fn, rc->scale,
                              rc->scores, const_cast<int32_t*>(topk_ids),

@@ -40,43 +40,108 @@ __device__ __forceinline__ float quant_x_group_warp(const __nv_bfloat16* __restr
   return s;
 }
 
+// x quantisation of up to four (token, group) items by one warp, every row
+// load issued before the first is used (items with t < 0 are skipped).
+__device__ __forceinline__ void quant_x_groups4_warp(const __nv_bfloat16* __restrict__ x,
+                                                     const int (&t)[4], const int (&g)[4],
+                                                     int H, uint8_t* __restrict__ xq,
+                                                     float* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  uint2 raw[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    raw[j] = t[j] >= 0 ? *reinterpret_cast<const uint2*>(
+                             x + static_cast<size_t>(t[j]) * H + g[j] * 128 + lane * 4)
+                       : make_uint2(0u, 0u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (t[j] < 0) continue;
+    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw[j].x);
+    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw[j].y);
+    float v[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
+    float s;
+    const uint32_t q = quant_group4(v, &s);
+    const size_t base = static_cast<size_t>(t[j]) * H + g[j] * 128 + lane * 4;
+    *reinterpret_cast<uint32_t*>(xq + base) = q;
+    if (lane == 0) xs[static_cast<size_t>(t[j]) * (H / 128) + g[j]] = s;
+  }
+}
+
 // Router scores and top-k of token t by one warp (HPC-Ops × SGLang, section
 // "Router GEMM"): the split-K partials of the two GEMMs (P[s][t][0..E) = x.hi,
 // P[s][t][E..2E) = x.lo) give score = acc_hi + acc_lo/256; softmax (or
 // sigmoid); k rounds of warp arg-max over the raw scores (ties to the lower
 // id); weights renormalised over the selected ids, times `scale`.
 constexpr int kRouterMaxE = 512;
+constexpr int kRouterMaxSplits = 4;   // router GEMM split-K partials per score
 
-// kPer score slots per lane (E <= 32 * kPer).
-template <int kPer>
+// kPer score slots per lane (E <= 32 * kPer).  kL2: the partials were written
+// by other CTAs of the same grid, so they are read through L2 (ld.global.cg)
+// rather than the non-coherent path.  ids_out (nullable): the selected ids
+// are also written there, ids_out[j] for j < k.
+template <int kPer, bool kL2>
 __device__ __forceinline__ void router_topk_warp_t(const float* __restrict__ P, int splits,
                                                    int rows_cap, int t, int E, int k,
                                                    int score_fn, float scale,
                                                    float* __restrict__ scores,
                                                    int32_t* __restrict__ ids,
-                                                   float* __restrict__ w) {
+                                                   float* __restrict__ w, int32_t* ids_out) {
   const int lane = threadIdx.x & 31;
+  auto ld = [](const float* a) { return kL2 ? __ldcg(a) : __ldg(a); };
   float s[kPer];
   const size_t slice = static_cast<size_t>(rows_cap) * 2 * E;
   const int per = (E + 31) / 32;   // slots this warp really uses
   float mx = -INFINITY;
   const float* row = P + static_cast<size_t>(t) * 2 * E;
+  if constexpr (kPer <= 8) {
+    // every partial of this lane's slots is loaded before any is summed (one
+    // L2 round trip, not one per slot and split); sums run in split order
+    float ph[kRouterMaxSplits][kPer], pl[kRouterMaxSplits][kPer];
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = lane + 32 * i;
-    float v = -INFINITY;
-    if (i < per && e < E) {
-      float hi = __ldg(row + e), lo = __ldg(row + E + e);
-#pragma unroll 4
-      for (int sp = 1; sp < splits; ++sp) {
-        hi += __ldg(row + sp * slice + e);
-        lo += __ldg(row + sp * slice + E + e);
+    for (int sp = 0; sp < kRouterMaxSplits; ++sp)
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        const bool in = sp < splits && i < per && e < E;
+        ph[sp][i] = in ? ld(row + sp * slice + e) : 0.f;
+        pl[sp][i] = in ? ld(row + sp * slice + E + e) : 0.f;
       }
-      v = hi + lo * (1.0f / 256.0f);
-      scores[static_cast<size_t>(t) * E + e] = v;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      float v = -INFINITY;
+      if (i < per && e < E) {
+        float hi = ph[0][i], lo = pl[0][i];
+#pragma unroll
+        for (int sp = 1; sp < kRouterMaxSplits; ++sp)
+          if (sp < splits) {
+            hi += ph[sp][i];
+            lo += pl[sp][i];
+          }
+        v = hi + lo * (1.0f / 256.0f);
+        scores[static_cast<size_t>(t) * E + e] = v;
+      }
+      s[i] = v;
+      mx = fmaxf(mx, v);
     }
-    s[i] = v;
-    mx = fmaxf(mx, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      float v = -INFINITY;
+      if (i < per && e < E) {
+        float hi = ld(row + e), lo = ld(row + E + e);
+#pragma unroll 4
+        for (int sp = 1; sp < splits; ++sp) {
+          hi += ld(row + sp * slice + e);
+          lo += ld(row + sp * slice + E + e);
+        }
+        v = hi + lo * (1.0f / 256.0f);
+        scores[static_cast<size_t>(t) * E + e] = v;
+      }
+      s[i] = v;
+      mx = fmaxf(mx, v);
+    }
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
@@ -132,22 +197,27 @@ __device__ __forceinline__ void router_topk_warp_t(const float* __restrict__ P, 
   }
   if (lane < k) {
     ids[static_cast<size_t>(t) * k + lane] = my_id;
+    if (ids_out != nullptr) ids_out[lane] = my_id;
     w[static_cast<size_t>(t) * k + lane] = scale * (my_p / psel);
   }
 }
 
+template <bool kL2 = false>
 __device__ __forceinline__ void router_topk_warp(const float* __restrict__ P, int splits,
                                                  int rows_cap, int t, int E, int k, int score_fn,
                                                  float scale, float* __restrict__ scores,
                                                  int32_t* __restrict__ ids,
-                                                 float* __restrict__ w) {
+                                                 float* __restrict__ w,
+                                                 int32_t* ids_out = nullptr) {
   if (E <= 128)
-    router_topk_warp_t<4>(P, splits, rows_cap, t, E, k, score_fn, scale, scores, ids, w);
+    router_topk_warp_t<4, kL2>(P, splits, rows_cap, t, E, k, score_fn, scale, scores, ids, w,
+                               ids_out);
   else if (E <= 256)
-    router_topk_warp_t<8>(P, splits, rows_cap, t, E, k, score_fn, scale, scores, ids, w);
+    router_topk_warp_t<8, kL2>(P, splits, rows_cap, t, E, k, score_fn, scale, scores, ids, w,
+                               ids_out);
   else
-    router_topk_warp_t<kRouterMaxE / 32>(P, splits, rows_cap, t, E, k, score_fn, scale, scores,
-                                         ids, w);
+    router_topk_warp_t<kRouterMaxE / 32, kL2>(P, splits, rows_cap, t, E, k, score_fn, scale,
+                                              scores, ids, w, ids_out);
 }
 
 }  // namespace moe

@@ -191,6 +191,21 @@ def make(cfg: int, T: int | None = None, device="cpu", *, H=None, I=None, E=None
     return wl
 
 
+# The router on its own at the "HPC-Ops × SGLang" post's router-GEMM table
+# shape (section "Router GEMM", Table 2: K = 4096, N = 192, BF16 activations
+# times FP32 router weights), over the table's token counts M.
+ROUTER_SHAPE = dict(H=4096, E=192, k=8, sweep=(1, 16, 48, 96, 208, 512, 1024, 2048, 4096))
+
+
+def router_inputs(M: int, device="cpu", H: int = ROUTER_SHAPE["H"], E: int = ROUTER_SHAPE["E"],
+                  seed: int = 6000):
+    """x [M, H] ~ N(0, 1) rounded to bf16 and fp32 router weights [E, H] ~
+    N(0, 1/sqrt(H)) (weights from `seed`, x from seed + M)."""
+    wr = torch.randn((E, H), generator=_gen(seed, device), device=device) / math.sqrt(H)
+    x = torch.randn((M, H), generator=_gen(seed + M, device), device=device).bfloat16()
+    return x, wr
+
+
 def bf16_bits(t: torch.Tensor):
     """numpy uint16 view of a bf16 tensor (bit patterns), on the host."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")

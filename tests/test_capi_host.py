@@ -158,12 +158,21 @@ def test_align_ex_host_checks():
 
 def test_routed_plan():
     s = moe.make_shape(64, 2048, 768, 128, 8, 0, True)
-    assert moe.moe_plan_routed(s).route_fused == 0          # opt-in
+    assert moe.moe_plan_routed(s).route_fused == 0          # separate kernels by default
     L = moe.moe_plan_routed(s, moe.make_opts(fuse_routing=True))
     assert L.route_fused == 1 and L.off_router >= L.off_y and L.off_route_counter > L.off_router
-    assert moe.moe_routed_workspace_bytes(s) == L.total_bytes > moe.moe_workspace_bytes(s)
-    assert moe.moe_plan_routed(moe.make_shape(512, 2048, 768, 128, 8, 0, True),
-                               moe.make_opts(fuse_routing=True)).route_fused == 0
+    assert L.off_route_hist > L.off_route_counter
+    assert L.off_route_hist + 4 * 11 * 128 <= L.total_bytes   # a histogram row per owner CTA (6 tokens each)
+    assert moe.moe_routed_workspace_bytes(s, moe.make_opts(fuse_routing=True)) == L.total_bytes
+    assert L.total_bytes > moe.moe_workspace_bytes(s)
+    L2 = moe.moe_plan_routed(s, moe.make_opts(fuse_routing=False))
+    assert L2.route_fused == 0 and L2.total_bytes < L.total_bytes
+    assert moe.moe_plan_routed(moe.make_shape(4096, 2048, 768, 128, 8, 0, True),
+                               moe.make_opts(fuse_routing=True)).route_fused == 1
+    o = moe.make_opts()
+    o.fuse_routing = 2
+    with pytest.raises(moe.MoeError):
+        moe.moe_plan_routed(s, o)
     for o in (moe.make_opts(smem_index=True), moe.make_opts(num_shared_experts=1),
               moe.make_opts(ep_first_expert=0, ep_num_experts=256)):
         with pytest.raises(moe.MoeError):
