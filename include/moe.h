@@ -180,6 +180,16 @@ typedef struct {
    * call's output is undefined.  The waits for the kernel's own copies and
    * MMAs before it exits keep the 2-s limit. */
   int32_t pipeline_wait_ns;
+  /* Coalesced token tiles for small row tiles (block_m 16 or 32).  The index
+   * still pads each expert to block_m rows, but the expert GEMMs take an
+   * expert's rows in tiles of up to C consecutive rows (a work list written
+   * next to the task map), so an expert holding many rows (skewed routing)
+   * has its weight tiles streamed once per C rows instead of once per
+   * block_m, while a tile with few rows still loads and multiplies only
+   * those (rounded up to 16).  0: planner; -1: off; 32 or 64: C, used where
+   * C > block_m (not for MOE_W8A16).  Other values: MOE_ERR_ARG.  Results do
+   * not depend on it. */
+  int32_t coalesce_rows;
 } moe_forward_opts;
 
 /* Options of moe_align_ex: the same shared-expert and expert-parallel mapping
@@ -216,6 +226,9 @@ typedef struct {
   size_t off_route_counter; /* fused routing: two grid-barrier counters (8 bytes) */
   size_t total_bytes;
   size_t off_route_hist;    /* fused routing: per-CTA expert counts           */
+  int32_t coalesce_rows;    /* C of the work list, 0 when the GEMMs take the task map */
+  size_t off_work_tiles;    /* work list: int32 [tiles_cap][4] {expert, first row, rows, 0} */
+  size_t off_num_work_tiles;  /* its length (int32) */
 } moe_workspace_layout;
 
 /* tiles_cap of the index for these sizes (0 on invalid arguments). */

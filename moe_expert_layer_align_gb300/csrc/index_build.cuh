@@ -77,10 +77,11 @@ struct IndexScratch {
   int32_t* offs;   // [E + 1]: padded offsets
   int32_t* tot;    // [E]: per-expert counts
   int32_t* flag;   // [1]: an invalid id was seen
-  int32_t* wsum;   // [33]: per-warp sums of the offset scan, then its total
+  int32_t* wsum;   // [2][33]: per-warp sums of the two offset scans, then their totals
+  int32_t* coffs;  // [E + 1]: work-list offsets (coalesced tiles before each expert)
   int remote_ok;   // kRemoteId entries are another rank's: dropped, not flagged
   static __host__ __device__ constexpr size_t words(int nwarps, int E) {
-    return static_cast<size_t>(nwarps) * E + (E + 1) + E + 1 + 33;
+    return static_cast<size_t>(nwarps) * E + (E + 1) + E + 1 + 66 + (E + 1);
   }
   __device__ void carve(int32_t* base, int nwarps, int E, int remote = 0) {
     remote_ok = remote;
@@ -89,6 +90,7 @@ struct IndexScratch {
     tot = offs + E + 1;
     flag = tot + E;
     wsum = flag + 1;
+    coffs = wsum + 66;
   }
 };
 
@@ -102,51 +104,78 @@ __device__ __forceinline__ int index_warps(int tk) {
   return need < 1 ? 1 : (need < nwarps ? need : nwarps);
 }
 
+// Inclusive warp scan of v.
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += o;
+  }
+  return v;
+}
+
 // offs[0..E] = exclusive prefix of tot[] rounded up to multiples of bm (a
 // power of two, as the host checks): one expert per thread, a shuffle scan
 // per warp and one over the warps' sums, blockDim.x experts at a time.  (A
 // single warp walking the experts with divisions took ~2-4 us for 128
-// experts.)  Ends with a block barrier.
-__device__ __forceinline__ void index_scan_offsets(int E, int bm, const IndexScratch& sc) {
+// experts.)  With coalesce C > 0 (a power of two) the same pass also gives
+// coffs[0..E], the exclusive prefix of ceil(tot / C): the work-list tiles of
+// up to C rows before each expert (index_work_tile).  Ends with a block
+// barrier.
+__device__ __forceinline__ void index_scan_offsets(int E, int bm, const IndexScratch& sc,
+                                                   int C = 0) {
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31, nw = nthreads >> 5;
   const int mask = bm - 1;
-  int carry = 0;   // padded rows of the experts before this round's
+  const int cs = C > 0 ? __ffs(C) - 1 : 0;
+  int carry = 0, ccarry = 0;   // padded rows (work tiles) of the experts before this round's
   for (int e0 = 0; e0 < E; e0 += nthreads) {
     const int e = e0 + tid;
-    const int v = e < E ? (sc.tot[e] + mask) & ~mask : 0;
-    int incl = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += o;
+    const int t = e < E ? sc.tot[e] : 0;
+    const int v = (t + mask) & ~mask;
+    const int cv = C > 0 ? (t + C - 1) >> cs : 0;
+    const int incl = warp_incl_scan(v, lane);
+    const int cincl = C > 0 ? warp_incl_scan(cv, lane) : 0;
+    if (lane == 31) {
+      sc.wsum[warp] = incl;
+      sc.wsum[33 + warp] = cincl;
     }
-    if (lane == 31) sc.wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
       const int x = lane < nw ? sc.wsum[lane] : 0;
-      int xi = x;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, xi, d);
-        if (lane >= d) xi += o;
+      const int xi = warp_incl_scan(x, lane);
+      const int cx = lane < nw ? sc.wsum[33 + lane] : 0;
+      const int cxi = C > 0 ? warp_incl_scan(cx, lane) : 0;
+      if (lane < nw) {              // exclusive warp bases
+        sc.wsum[lane] = xi - x;
+        sc.wsum[33 + lane] = cxi - cx;
       }
-      if (lane < nw) sc.wsum[lane] = xi - x;   // exclusive warp bases
-      if (lane == 31) sc.wsum[32] = xi;        // this round's total
+      if (lane == 31) {             // this round's totals
+        sc.wsum[32] = xi;
+        sc.wsum[65] = cxi;
+      }
     }
     __syncthreads();
-    if (e < E) sc.offs[e] = carry + sc.wsum[warp] + incl - v;
+    if (e < E) {
+      sc.offs[e] = carry + sc.wsum[warp] + incl - v;
+      if (C > 0) sc.coffs[e] = ccarry + sc.wsum[33 + warp] + cincl - cv;
+    }
     carry += sc.wsum[32];
+    ccarry += sc.wsum[65];
     __syncthreads();   // wsum is rewritten by the next round
   }
-  if (tid == 0) sc.offs[E] = carry;
+  if (tid == 0) {
+    sc.offs[E] = carry;
+    if (C > 0) sc.coffs[E] = ccarry;
+  }
   __syncthreads();
 }
 
-// Steps 1-2: counts, per-warp bases and padded offsets, all in `sc`.  `src`
-// holds the T*k ids (shared or global memory).  Ends with a block barrier.
+// Steps 1-2: counts, per-warp bases and padded offsets (and with C > 0 the
+// work-list offsets), all in `sc`.  `src` holds the T*k ids (shared or global
+// memory).  Ends with a block barrier.
 __device__ __forceinline__ void index_count_and_scan(const int32_t* src, int tk, int E, int bm,
-                                                     const IndexScratch& sc) {
+                                                     const IndexScratch& sc, int C = 0) {
   const int tid = threadIdx.x, nthreads = blockDim.x, nwarps = index_warps(tk);
   const int warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < nwarps * E; i += nthreads) sc.cnt[i] = 0;
@@ -177,7 +206,7 @@ __device__ __forceinline__ void index_count_and_scan(const int32_t* src, int tk,
     sc.tot[e] = run;
   }
   __syncthreads();
-  index_scan_offsets(E, bm, sc);
+  index_scan_offsets(E, bm, sc, C);
 }
 
 // Step 3: every valid assignment a goes to row(pos, a); an invalid one to
@@ -229,6 +258,41 @@ __device__ __forceinline__ int4 index_tile(int q, int E, int bm, const IndexScra
     if (sc.offs[mid] <= row0) lo = mid; else hi = mid - 1;
   }
   return make_int4(lo, row0, min(bm, sc.offs[lo] + sc.tot[lo] - row0), 0);
+}
+
+// Work-list entry q with coalesce C (after index_scan_offsets(.., C)): the
+// expert's rows in tiles of up to C consecutive rows from its first, so a
+// hot expert's weight tiles are streamed once per C rows rather than once
+// per bm; {expert, first row, rows, 0}, or {-1, 0, 0, 0} past the last
+// (coffs[E] entries).
+__device__ __forceinline__ int4 index_work_tile(int q, int E, int C, const IndexScratch& sc) {
+  if (q >= sc.coffs[E]) return make_int4(-1, 0, 0, 0);
+  int lo = 0, hi = E - 1;   // largest e with coffs[e] <= q (an expert with rows)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sc.coffs[mid] <= q) lo = mid; else hi = mid - 1;
+  }
+  const int j = (q - sc.coffs[lo]) * C;   // rows of the expert before this tile
+  return make_int4(lo, sc.offs[lo] + j, min(C, sc.tot[lo] - j), 0);
+}
+
+// The task map (tile_expert, tiles, num_tiles: tiles of bm rows) and, where
+// idx.work_tiles is set, the work list of tiles of up to C rows, written by
+// the block's threads from `sc`.  No barrier.
+__device__ __forceinline__ void index_write_tiles(int E, int bm, int tiles_cap, int C,
+                                                  const IndexScratch& sc, const IndexPtrs& idx) {
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  if (tid == 0) *idx.num_tiles = sc.offs[E] / bm;
+  for (int q = tid; q < tiles_cap; q += nthreads) {
+    const int4 t = index_tile(q, E, bm, sc);
+    idx.tile_expert[q] = t.x;
+    reinterpret_cast<int4*>(idx.tiles)[q] = t;
+  }
+  if (C > 0 && idx.work_tiles) {
+    if (tid == 0) *idx.num_work_tiles = sc.coffs[E];
+    for (int q = tid; q < tiles_cap; q += nthreads)
+      reinterpret_cast<int4*>(idx.work_tiles)[q] = index_work_tile(q, E, C, sc);
+  }
 }
 
 }  // namespace moe

@@ -69,6 +69,15 @@ struct GemmParams {
   int early_weights;         // contiguous token operand: stream weights before the wait
   uint64_t pipe_wait_ns;     // limit of the pipeline waits (0: kWaitLimitNs); drains keep
                              // the full limit
+  // Coalesced work list (gather / direct operands): the index pads experts
+  // to index_bm rows, and the GEMM's token tiles are the work list's tiles of
+  // up to `coalesce` (<= BN) consecutive rows of one expert, each entry
+  // carrying its first row (tiles / num_tiles then point at the work list).
+  // A direct token operand is loaded as ceil(rows / index_bm) boxes of
+  // index_bm rows (the map's box).  0: off (tile q is rows q*BN.., a box of
+  // BN rows).
+  int coalesce;
+  int index_bm;              // rows per index tile (0: BN)
   int scale_by_token;        // FP8 gathered operand: b_scale rows are tokens
 };
 
@@ -98,6 +107,10 @@ cudaError_t launch_gemm_w8(int bn, int bsrc, int grid, cudaStream_t st, bool pdl
 // Index build, pointwise stages (k_align.cu, k_pointwise.cu).
 struct IndexPtrs {
   int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
+  // Optional (moe_forward with coalesced units): the work list of tiles of up
+  // to `coalesce` rows, {expert, first row, rows, 0} x tiles_cap, and its length.
+  int32_t *work_tiles = nullptr, *num_work_tiles = nullptr;
+  int coalesce = 0;
 };
 // k and E below count assignments per token and experts of the index (map.kk
 // and map.E + shared experts); `map` turns topk_ids into index experts.

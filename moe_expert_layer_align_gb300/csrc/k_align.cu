@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   }
   const int32_t* src = stage_ids ? sids : ids;
 
-  index_count_and_scan(src, tk, E, bm, sc);
+  index_count_and_scan(src, tk, E, bm, sc, idx.coalesce);
   for (int e = tid; e < E; e += nthreads) idx.counts[e] = sc.tot[e];
   for (int e = tid; e <= E; e += nthreads) idx.offsets[e] = sc.offs[e];
   index_scatter(
@@ -61,12 +61,7 @@ __global__ void __launch_bounds__(kAlignThreads)
       },
       [&](int a) { idx.inv_pos[a] = -1; });
   index_pads(E, tiles_cap * bm, sc, [&](int pos) { idx.sorted_ids[pos] = tk; });
-  if (tid == 0) *idx.num_tiles = sc.offs[E] / bm;
-  for (int q = tid; q < tiles_cap; q += nthreads) {
-    const int4 t = index_tile(q, E, bm, sc);
-    idx.tile_expert[q] = t.x;
-    reinterpret_cast<int4*>(idx.tiles)[q] = t;
-  }
+  index_write_tiles(E, bm, tiles_cap, idx.coalesce, sc, idx);
   __syncthreads();
   if (tid == 0 && *sc.flag && dev_status) atomicOr(dev_status, kStatusExpertId);
 }
@@ -173,15 +168,10 @@ __global__ void __launch_bounds__(kAlignThreads)
     idx.counts[e] = run;
   }
   __syncthreads();
-  index_scan_offsets(E, bm, sc);
+  index_scan_offsets(E, bm, sc, idx.coalesce);
   for (int e = tid; e <= E; e += kAlignThreads) idx.offsets[e] = sc.offs[e];
   index_pads(E, tiles_cap * bm, sc, [&](int pos) { idx.sorted_ids[pos] = tk; });
-  if (tid == 0) *idx.num_tiles = sc.offs[E] / bm;
-  for (int q = tid; q < tiles_cap; q += kAlignThreads) {
-    const int4 t = index_tile(q, E, bm, sc);
-    idx.tile_expert[q] = t.x;
-    reinterpret_cast<int4*>(idx.tiles)[q] = t;
-  }
+  index_write_tiles(E, bm, tiles_cap, idx.coalesce, sc, idx);
   if (tid == 0 && dev_status) {
     int any = 0;
     for (int b = 0; b < nb; ++b) any |= flags[b];

@@ -193,11 +193,17 @@ __device__ __forceinline__ int4 load_tile(int q, const GemmParams& p, const int4
   // L2-coherent load: the Down GEMM may read the task map before its PDL wait
   const int4 t = smem_tiles ? smem_tiles[q] : __ldcg(reinterpret_cast<const int4*>(p.tiles) + q);
   // Every address below derives from this entry: row 0 of tile q is q*BN
-  // by construction, and an entry that is not a well-formed one (a workspace
-  // overwritten between the stages) becomes an empty tile of expert 0
-  // rather than an out-of-range access.
-  const bool ok = t.x >= 0 && t.x < p.E && t.z >= 0 && t.z <= BN;
-  return make_int4(ok ? t.x : 0, q * BN, ok ? t.z : 0, 0);
+  // by construction (a work-list entry carries its own, checked to lie in
+  // [0, rows_cap - rows]), and an entry that is not a well-formed one (a
+  // workspace overwritten between the stages) becomes an empty tile of
+  // expert 0 rather than an out-of-range access.
+  if (p.coalesce == 0) {
+    const bool ok = t.x >= 0 && t.x < p.E && t.z >= 0 && t.z <= BN;
+    return make_int4(ok ? t.x : 0, q * BN, ok ? t.z : 0, 0);
+  }
+  const bool ok = t.x >= 0 && t.x < p.E && t.z >= 0 && t.z <= BN && t.y >= 0 &&
+                  t.y <= p.rows_cap - t.z;
+  return ok ? make_int4(t.x, t.y, t.z, 0) : make_int4(0, 0, 0, 0);
 }
 
 // Token of sorted row `a`'s assignment, or -1 for padding and any value
@@ -318,18 +324,21 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
 
   SmemIndex si;
   const bool smem_idx = BSRC != kDense && p.smem_index;
+  const int ibm = p.index_bm ? p.index_bm : BN;   // rows per index tile
   if (smem_idx) {
     // The top-k ids are an input of the call: complete before its first
     // kernel started, so they are read without waiting on the predecessor.
     si.carve(reinterpret_cast<int32_t*>(smem + S::kOffIdx), S::kWarps, p.E, tk, p.rows_cap,
              p.idmap.Eg != 0);
     for (int i = threadIdx.x; i < tk; i += S::kThreads) si.ids[i] = mapped_id(p.topk_ids, i, p.idmap);
-    index_count_and_scan(si.ids, tk, p.E, BN, si.sc);
+    index_count_and_scan(si.ids, tk, p.E, ibm, si.sc, p.coalesce);
     index_scatter(si.ids, tk, p.E, si.sc, [&](int pos, int a) { si.rows[pos] = a; },
                   [](int) {});
     index_pads(p.E, p.rows_cap, si.sc, [&](int pos) { si.rows[pos] = tk; });
+    // this CTA's task map: the work list with coalesced units
     for (int q = threadIdx.x; q < p.tiles_cap; q += S::kThreads)
-      si.tiles[q] = index_tile(q, p.E, BN, si.sc);
+      si.tiles[q] = p.coalesce ? index_work_tile(q, p.E, p.coalesce, si.sc)
+                               : index_tile(q, p.E, ibm, si.sc);
   }
   tc_fence_before();
   __syncthreads();
@@ -344,7 +353,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
   // before letting this grid launch).
   const bool early = smem_idx || (BSRC == kDirect && p.early_weights);
   if (smem_idx) {
-    num_tiles = si.sc.offs[p.E] / BN;
+    num_tiles = p.coalesce ? si.sc.coffs[p.E] : si.sc.offs[p.E] / ibm;
     smem_tiles = si.tiles;
   } else {
     if (!early) pdl_wait();
@@ -367,9 +376,18 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
     uint32_t phase = 0;
     long issued = 0;
     bool ok = true;
-    constexpr uint32_t bytes =
-        S::kAStage + (BSRC == kGather ? static_cast<uint32_t>(S::kTmaRows * kKBytes)
-                                      : static_cast<uint32_t>(S::kBBytes));
+    // Contiguous token operand: one box of BN rows, or with the work list
+    // (coalesce) ceil(rows / box) boxes of the index's box rows, so that a
+    // tile with few valid rows loads few rows.
+    const bool b_boxes = BSRC == kDirect && p.coalesce != 0;
+    const int box = b_boxes ? min(ibm, BN) : BN;
+    auto b_box_count = [&](const WorkUnit& w) {
+      return b_boxes ? min(BN / box, (w.rows + box - 1) / box) : 1;
+    };
+    auto load_b = [&](uint32_t dst, uint32_t bar, int kc, int row0, int nbox) {
+      for (int b = 0; b < nbox; ++b)
+        tma_load_2d(dst + b * box * kKBytes, &tmB, bar, kc, row0 + b * box);
+    };
     int tma_tok[S::kTmaRows > 0 ? S::kTmaRows : 1];   // token rows this warp gathers (lane 0)
     bool b_now = !(early && BSRC == kDirect);
     int deferred = 0;
@@ -379,10 +397,10 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
       for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); i < deferred && it.valid();
            it.advance()) {
         const WorkUnit w = it.take(p);
+        const int nbox = b_box_count(w);
         for (int kt = w.kt0; kt < w.kt1 && i < deferred; ++kt, ++i)
           if (lane == 0)
-            tma_load_2d(sB + i * S::kBBytes, &tmB, bar_full + 8 * i, kt * S::kElemsPerStage,
-                        w.row0);
+            load_b(sB + i * S::kBBytes, bar_full + 8 * i, kt * S::kElemsPerStage, w.row0, nbox);
       }
       __syncwarp();
       b_now = true;
@@ -390,6 +408,10 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
     for (UnitIter<BN, BSRC> it(units, num_tiles, p, smem_tiles); ok && it.valid(); it.advance()) {
       if (warp_aborted()) break;
       const WorkUnit w = it.take(p);
+      const int nbox = b_box_count(w);
+      const uint32_t bytes =
+          S::kAStage + (BSRC == kGather ? static_cast<uint32_t>(S::kTmaRows * kKBytes)
+                                        : static_cast<uint32_t>(nbox * box * kKBytes));
       if constexpr (S::kTmaRows > 0) {
         // lane l looks up row l's token; padding rows read token 0 (their
         // columns are never stored)
@@ -419,8 +441,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
             else
               tma_load_3d(a_dst + me * kABytes, &tmA, full, kc, mt * kTileM, w.e);
           }
-          if (BSRC != kGather && b_now)
-            tma_load_2d(sB + stage * S::kBBytes, &tmB, full, kc, w.row0);
+          if (BSRC != kGather && b_now) load_b(sB + stage * S::kBBytes, full, kc, w.row0, nbox);
           if constexpr (S::kTmaRows > 0) {
 #pragma unroll
             for (int g = 0; g < S::kTmaRows / 4; ++g)
@@ -602,12 +623,12 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
         if (e < 0 || e >= p.E) p.index_out.inv_pos[a] = -1;
       }
       for (int q = et; q < p.tiles_cap; q += kET) {
-        const int4 t = si.tiles[q];
+        const int4 t = p.coalesce ? index_tile(q, p.E, ibm, si.sc) : si.tiles[q];
         p.index_out.tile_expert[q] = t.x;
         reinterpret_cast<int4*>(p.index_out.tiles)[q] = t;
       }
       if (et == 0) {
-        *p.index_out.num_tiles = num_tiles;
+        *p.index_out.num_tiles = si.sc.offs[p.E] / ibm;
         if (p.dev_status && *si.sc.flag) atomicOr(p.dev_status, kStatusExpertId);
       }
     }

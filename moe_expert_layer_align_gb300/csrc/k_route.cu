@@ -141,19 +141,14 @@ __global__ void __launch_bounds__(GemmShape<0, BN, kDense>::kThreads, 1)
     bse[e] = base;
   }
   __syncthreads();
-  index_scan_offsets(q.Ei, q.bm, sc);   // sc.offs: the layer's padded offsets
+  index_scan_offsets(q.Ei, q.bm, sc, q.idx.coalesce);   // sc.offs: the layer's padded offsets
   const IndexPtrs& idx = q.idx;
   const int tk = q.T * q.k;
   if (c == 0) {
     for (int e = tid; e < q.Ei; e += kThreads) idx.counts[e] = sc.tot[e];
     for (int e = tid; e <= q.Ei; e += kThreads) idx.offsets[e] = sc.offs[e];
     index_pads(q.Ei, q.tiles_cap * q.bm, sc, [&](int pos) { idx.sorted_ids[pos] = tk; });
-    if (tid == 0) *idx.num_tiles = sc.offs[q.Ei] / q.bm;
-    for (int i = tid; i < q.tiles_cap; i += kThreads) {
-      const int4 tile = index_tile(i, q.Ei, q.bm, sc);
-      idx.tile_expert[i] = tile.x;
-      reinterpret_cast<int4*>(idx.tiles)[i] = tile;
-    }
+    index_write_tiles(q.Ei, q.bm, q.tiles_cap, idx.coalesce, sc, idx);
   }
   __syncthreads();
   for (int e = tid; e < q.Ei; e += kThreads) sc.offs[e] += bse[e];

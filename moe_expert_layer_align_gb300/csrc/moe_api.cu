@@ -25,19 +25,24 @@ constexpr int kMaxSplits = 32;
 constexpr int kSmemIndexMaxAssignments = 4096;
 // Above this many assignments the index is built over chunks by several CTAs.
 constexpr int kSplitIndexMinAssignments = 2048;
+// Coalesced work list the planner uses over 16- and 32-row index tiles
+// (0: none).
+constexpr int kPlanCoalesce = 0;
 // Router GEMM split-K count bound (the top-k sums at most this many partials).
 constexpr int kRouterMaxSplitsHost = 4;
 
 enum {
   kOffCounts, kOffOffsets, kOffSorted, kOffTileExpert, kOffTiles, kOffInvPos, kOffNumTiles,
   kOffIdxScratch, kOffXq, kOffXs, kOffXsRows, kOffG, kOffA, kOffAs, kOffY, kOffRouterP,
-  kOffCounter, kOffRouteHist, kNumOff
+  kOffCounter, kOffRouteHist, kOffWorkTiles, kOffNumWorkTiles, kNumOff
 };
 
 struct Plan {
   // k, E: assignments per token and experts of the index and the weights
   // (routed + shared); the IdMap maps topk_ids onto them.
   int T, H, I, E, k, bm, fp8, out_bf16;
+  int co;                  // coalesced work list: tiles of up to co rows (0: the task map)
+  int bn;                  // token rows of the GEMM kernels' tile: co, else bm
   int w8;                  // w8a16: e4m3 weights dequantised on chip, bf16 activations
   IdMap map;
   float w_shared;
@@ -228,6 +233,16 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   const bool pair = !p->fp8 && !p->w8 && !(o && o->single_weight_tile) &&
                     (s->I / 64) % 2 == 0 && (s->H / 128) % 2 == 0;
   p->bm = s->block_m ? s->block_m : auto_bm(p->T, p->k, p->E, p->fp8, pair);
+  // Coalesced work list over a 16- or 32-row index.
+  if (o && !(o->coalesce_rows == 0 || o->coalesce_rows == -1 || o->coalesce_rows == 32 ||
+             o->coalesce_rows == 64))
+    return MOE_ERR_ARG;
+  {
+    const int want = o ? o->coalesce_rows : 0;
+    const int c = want == 0 ? kPlanCoalesce : want;
+    p->co = (c > p->bm && !p->w8) ? c : 0;
+  }
+  p->bn = p->co ? p->co : p->bm;
   const int64_t tc = tiles_cap_of(p->T, p->k, p->E, p->bm);
   if (tc * p->bm >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
   p->tiles_cap = static_cast<int>(tc);
@@ -283,8 +298,8 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     const int tk = p->T * p->k;
     bool fits = tk <= kSmemIndexMaxAssignments && (want == 1 || auto_on) && !p->w8;
     for (int bsrc : {static_cast<int>(kGather), static_cast<int>(kDirect)}) {
-      const size_t need = gemm_smem_bytes(p->fp8, p->bm, bsrc) +
-                          gemm_index_smem_bytes(gemm_warps(p->fp8, p->bm, bsrc), p->E, tk, p->rows_cap,
+      const size_t need = gemm_smem_bytes(p->fp8, p->bn, bsrc) +
+                          gemm_index_smem_bytes(gemm_warps(p->fp8, p->bn, bsrc), p->E, tk, p->rows_cap,
                                                 p->tiles_cap);
       if (need > kMaxGemmSmem) fits = false;
     }
@@ -323,6 +338,8 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
       p->routed ? p->rp_bytes : 0,
       p->route_fused ? 8u : 0u,
       p->route_fused ? 4 * static_cast<size_t>(p->rp_owners_cap) * p->E : 0,
+      p->co ? 16u * p->tiles_cap : 0,
+      p->co ? 4u : 0u,
   };
   size_t cur = 0;
   for (int i = 0; i < kNumOff; ++i) {
@@ -366,6 +383,9 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->off_as = p.off[kOffAs];
   L->off_y = p.off[kOffY];
   L->total_bytes = p.total;
+  L->coalesce_rows = p.co;
+  L->off_work_tiles = p.off[kOffWorkTiles];
+  L->off_num_work_tiles = p.off[kOffNumWorkTiles];
 }
 
 // ---------------------------------------------------------------- devices
@@ -590,6 +610,11 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
                reinterpret_cast<int32_t*>(at(kOffSorted)),     reinterpret_cast<int32_t*>(at(kOffTileExpert)),
                reinterpret_cast<int32_t*>(at(kOffTiles)),      reinterpret_cast<int32_t*>(at(kOffInvPos)),
                reinterpret_cast<int32_t*>(at(kOffNumTiles))};
+  if (p.co) {
+    ip.work_tiles = reinterpret_cast<int32_t*>(at(kOffWorkTiles));
+    ip.num_work_tiles = reinterpret_cast<int32_t*>(at(kOffNumWorkTiles));
+    ip.coalesce = p.co;
+  }
   uint8_t* xq = at(kOffXq);
   float* xs = reinterpret_cast<float*>(at(kOffXs));
   float* xs_rows = reinterpret_cast<float*>(at(kOffXsRows));
@@ -728,8 +753,10 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.kt_per_split = p.kts1;
   g1.kt_total = p.kt1;
   g1.tile_major = p.ord1 == 2;
-  g1.tiles = ip.tiles;
-  g1.num_tiles = ip.num_tiles;
+  g1.tiles = p.co ? ip.work_tiles : ip.tiles;
+  g1.num_tiles = p.co ? ip.num_work_tiles : ip.num_tiles;
+  g1.coalesce = p.co;
+  g1.index_bm = p.bm;
   g1.sorted_ids = ip.sorted_ids;
   g1.b_rows = p.fp8 ? static_cast<const void*>(xq) : x;
   g1.b_row_bytes = p.H * esize;
@@ -757,7 +784,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.pipe_wait_ns = wait_ns;
   const int units1 = g1.m_tiles * p.s1 * p.tiles_cap;
   e = p.w8 ? launch_gemm_w8(p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13, tmX, g1)
-           : launch_gemm(p.fp8, p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13,
+           : launch_gemm(p.fp8, p.bn, kGather, std::min(grid_cap, units1), s, chain(), tmW13,
                          tmX, g1, p.me1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -777,8 +804,10 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g2.kt_per_split = p.kts2;
   g2.kt_total = p.kt2;
   g2.tile_major = p.ord2 == 2;
-  g2.tiles = ip.tiles;
-  g2.num_tiles = ip.num_tiles;
+  g2.tiles = p.co ? ip.work_tiles : ip.tiles;
+  g2.num_tiles = p.co ? ip.num_work_tiles : ip.num_tiles;
+  g2.coalesce = p.co;
+  g2.index_bm = p.bm;
   g2.sorted_ids = ip.sorted_ids;
   g2.topk = p.k;
   g2.sentinel = tk;
@@ -797,7 +826,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g2.pipe_wait_ns = wait_ns;
   const int units2 = g2.m_tiles * p.s2 * p.tiles_cap;
   e = p.w8 ? launch_gemm_w8(p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2)
-           : launch_gemm(p.fp8, p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2,
+           : launch_gemm(p.fp8, p.bn, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2,
                          p.me2);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -236,3 +236,32 @@ def test_wait_limit_option_changes_no_plan_and_rejects_negatives():
     assert moe.moe_workspace_bytes(s, moe.make_opts(pipeline_wait_ns=1)) == moe.moe_workspace_bytes(s)
     with pytest.raises(moe.MoeError):
         moe.moe_plan(s, moe.make_opts(pipeline_wait_ns=-5))
+
+
+@pytest.mark.parametrize("T,H,I,E,k,fp8,bm", [
+    (64, 2048, 768, 128, 8, True, 0), (256, 2048, 768, 128, 8, True, 0),
+    (64, 2048, 768, 128, 8, False, 0), (8, 256, 512, 8, 2, False, 16),
+])
+def test_coalesce_option_plan(T, H, I, E, k, fp8, bm):
+    s = moe.make_shape(T, H, I, E, k, bm, fp8, True)
+    base = moe.moe_plan(s, moe.make_opts(coalesce_rows=-1))
+    assert base.coalesce_rows == 0 and base.off_work_tiles == base.off_num_work_tiles
+    for c in (32, 64):
+        L = moe.moe_plan(s, moe.make_opts(coalesce_rows=c))
+        # the index is the same (block_m, caps); the work list is used where C > block_m
+        assert (L.block_m, L.tiles_cap, L.rows_cap) == (base.block_m, base.tiles_cap, base.rows_cap)
+        assert L.coalesce_rows == (c if c > L.block_m else 0)
+        if L.coalesce_rows:
+            assert L.off_work_tiles >= L.off_route_hist
+            assert L.off_work_tiles + 16 * L.tiles_cap <= L.off_num_work_tiles
+            assert L.off_num_work_tiles + 4 <= L.total_bytes
+            assert L.total_bytes > base.total_bytes
+    for bad in (-2, 16, 48, 128):
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_plan(s, moe.make_opts(coalesce_rows=bad))
+        assert ei.value.status == moe.MOE_ERR_ARG
+    # w8a16 keeps the task map
+    if fp8:
+        sw = moe.make_shape(T, H, I, E, k, bm, False, True)
+        sw.mode = moe.MOE_W8A16
+        assert moe.moe_plan(sw, moe.make_opts(coalesce_rows=64)).coalesce_rows == 0
