@@ -221,7 +221,8 @@ typedef struct {
   size_t off_g;    /* fp32 Gate-Up partials  [S1][rows_cap][2I] (0 bytes when fused_act) */
   size_t off_a;    /* activation: bf16 [rows_cap][I] or e4m3 [rows_cap][I]  */
   size_t off_as;   /* FP8: fp32 act scales   [rows_cap][I/128]              */
-  size_t off_y;    /* fp32 Down partials     [S2][rows_cap][H] (sorted rows)*/
+  size_t off_y;    /* Down output rows (sorted): fp32 partials [S2][rows_cap][H], or
+                      bf16 [rows_cap][H] when y_bf16 (S2 = 1) */
   size_t off_router;        /* moe_forward_routed: router GEMM partial sums   */
   size_t off_route_counter; /* fused routing: two grid-barrier counters (8 bytes) */
   size_t total_bytes;
@@ -229,6 +230,7 @@ typedef struct {
   int32_t coalesce_rows;    /* C of the work list, 0 when the GEMMs take the task map */
   size_t off_work_tiles;    /* work list: int32 [tiles_cap][4] {expert, first row, rows, 0} */
   size_t off_num_work_tiles;  /* its length (int32) */
+  int32_t y_bf16;           /* 1: the Down GEMM is unsplit and stores bf16 rows at off_y */
 } moe_workspace_layout;
 
 /* tiles_cap of the index for these sizes (0 on invalid arguments). */

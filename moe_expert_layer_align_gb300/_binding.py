@@ -64,7 +64,8 @@ class moe_workspace_layout(ctypes.Structure):
                            "off_tiles", "off_inv_pos", "off_num_tiles", "off_index_scratch", "off_xq", "off_xs",
                            "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "off_router",
                            "off_route_counter", "total_bytes", "off_route_hist")] + [
-        ("coalesce_rows", _i32), ("off_work_tiles", _sz), ("off_num_work_tiles", _sz)]
+        ("coalesce_rows", _i32), ("off_work_tiles", _sz), ("off_num_work_tiles", _sz),
+        ("y_bf16", _i32)]
 
 
 def _load() -> ctypes.CDLL:
@@ -395,7 +396,8 @@ def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None, routed
         tiles=v(L.off_tiles, 4 * tc, torch.int32, (tc, 4)),
         inv_pos=v(L.off_inv_pos, T * k, torch.int32, (T * k,)),
         num_tiles=v(L.off_num_tiles, 1, torch.int32, (1,)),
-        Y=v(L.off_y, L.split_down * rc * H, torch.float32, (L.split_down, rc, H)),
+        Y=(v(L.off_y, rc * H, torch.bfloat16, (1, rc, H)) if L.y_bf16 else
+           v(L.off_y, L.split_down * rc * H, torch.float32, (L.split_down, rc, H))),
     )
     if L.coalesce_rows:
         out["work_tiles"] = v(L.off_work_tiles, 4 * tc, torch.int32, (tc, 4))

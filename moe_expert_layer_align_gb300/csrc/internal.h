@@ -78,6 +78,9 @@ struct GemmParams {
   // BN rows).
   int coalesce;
   int index_bm;              // rows per index tile (0: BN)
+  // Unsplit GEMM (splits == 1), no fused activation: the output rows are
+  // stored as bf16 [rows_cap][M] instead of fp32 partials.
+  int out_bf16;
   int scale_by_token;        // FP8 gathered operand: b_scale rows are tokens
 };
 
@@ -133,8 +136,9 @@ cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
                        const int32_t* sorted_ids, int sentinel, void* A, float* As,
                        cudaStream_t st, bool pdl);
 // k assignments per token, the first k_routed weighted by topk_w[t][j], the
-// others (shared experts) by w_shared.
-cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H,
+// others (shared experts) by w_shared.  Y: fp32 partials [splits][rows_cap][H],
+// or with y_bf16 the bf16 rows [rows_cap][H] of an unsplit Down GEMM.
+cudaError_t launch_combine(const void* Y, int y_bf16, int splits, int rows_cap, int H,
                            const int32_t* inv_pos, const float* topk_w, int T, int k,
                            int k_routed, float w_shared, void* out, int out_bf16,
                            cudaStream_t st, bool pdl);

@@ -252,6 +252,21 @@ struct UnitIter {
   __device__ __forceinline__ bool has_next() const { return u + static_cast<int>(gridDim.x) < units; }
 };
 
+// Sixteen fp32 values (raw bits) as two 16-byte stores of bf16 (dst 16-byte
+// aligned).
+__device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const uint32_t* v) {
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162 b2 =
+        __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  d[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+}
+
 __device__ __forceinline__ void report_timeout(const GemmParams& p, volatile int* abort_flag) {
   *abort_flag = 1;
   if (p.dev_status) atomicOr(p.dev_status, kStatusTimeout);
@@ -709,11 +724,16 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                 col0 = (j0 & 31) < 16 ? feat : p.I + feat;
               }
               if (live && col0 + 16 <= p.M) {
-                float4* dst = reinterpret_cast<float4*>(orow + col0);
+                if (p.out_bf16) {
+                  store_bf16x16(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                    static_cast<size_t>(w.row0 + n) * p.M + col0, v);
+                } else {
+                  float4* dst = reinterpret_cast<float4*>(orow + col0);
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                  dst[q4] = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
-                                        __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
+                  for (int q4 = 0; q4 < 4; ++q4)
+                    dst[q4] = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
+                                          __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
+                }
               }
             }
           }
@@ -767,6 +787,15 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                 const int n = c * 16 + (lo ? jj : 8 + jj);
                 if (n < w.rows)
                   arow[static_cast<size_t>(n) * p.I] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+              }
+            } else if (p.out_bf16) {
+              __nv_bfloat16* outb = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                    static_cast<size_t>(w.row0) * p.M + col;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int n = c * 16 + j;
+                if (n < w.rows && col_ok)
+                  outb[static_cast<size_t>(n) * p.M] = __float2bfloat16_rn(__uint_as_float(v[j]));
               }
             } else {
 #pragma unroll
@@ -862,13 +891,23 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
               col0 = (j0 & 31) < 16 ? feat : p.I + feat;
             }
             if (col0 + 16 <= p.M) {
-              float4* dst = reinterpret_cast<float4*>(orow + col0);
+              uint32_t vv[16];
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                float4 o;
-                unpack_f32x2(acc2[g * 8 + 2 * q], o.x, o.y);
-                unpack_f32x2(acc2[g * 8 + 2 * q + 1], o.z, o.w);
-                dst[q] = o;
+              for (int q = 0; q < 8; ++q) {
+                float a, b;
+                unpack_f32x2(acc2[g * 8 + q], a, b);
+                vv[2 * q] = __float_as_uint(a);
+                vv[2 * q + 1] = __float_as_uint(b);
+              }
+              if (p.out_bf16) {
+                store_bf16x16(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                  static_cast<size_t>(w.row0 + n) * p.M + col0, vv);
+              } else {
+                float4* dst = reinterpret_cast<float4*>(orow + col0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  dst[q] = make_float4(__uint_as_float(vv[4 * q]), __uint_as_float(vv[4 * q + 1]),
+                                       __uint_as_float(vv[4 * q + 2]), __uint_as_float(vv[4 * q + 3]));
               }
             }
           }
@@ -978,13 +1017,21 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
           if (!ok) break;
         }
         if (!ok) break;
+        __nv_bfloat16* outb = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                              static_cast<size_t>(w.row0) * p.M + col;
 #pragma unroll
         for (int h = 0; h < kWarpCols / 2; ++h) {
           float a0, a1;
           unpack_f32x2(acc2[h], a0, a1);
           const int n = c_base + 2 * h;
-          if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = a0;
-          if (n + 1 < w.rows && col_ok) outp[static_cast<size_t>(n + 1) * p.M] = a1;
+          if (p.out_bf16) {
+            if (n < w.rows && col_ok) outb[static_cast<size_t>(n) * p.M] = __float2bfloat16_rn(a0);
+            if (n + 1 < w.rows && col_ok)
+              outb[static_cast<size_t>(n + 1) * p.M] = __float2bfloat16_rn(a1);
+          } else {
+            if (n < w.rows && col_ok) outp[static_cast<size_t>(n) * p.M] = a0;
+            if (n + 1 < w.rows && col_ok) outp[static_cast<size_t>(n + 1) * p.M] = a1;
+          }
         }
       }
     }

@@ -209,9 +209,21 @@ cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
 // and all of a token's rows in flight at once cut the latency.
 constexpr int kCombineThreads = 256;
 
-template <int kCols, int kBatch>
+// Four consecutive values of Y (fp32 partials, or bf16 rows of an unsplit
+// Down GEMM) as a float4.
+__device__ __forceinline__ float4 load_y4(const float* Y, size_t off) {
+  return __ldg(reinterpret_cast<const float4*>(Y + off));
+}
+__device__ __forceinline__ float4 load_y4(const __nv_bfloat16* Y, size_t off) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(Y + off));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <int kCols, int kBatch, typename TY>
 __global__ void __launch_bounds__(kCombineThreads)
-    moe_combine_kernel(const float* __restrict__ Y, int splits, int rows_cap, int H,
+    moe_combine_kernel(const TY* __restrict__ Y, int splits, int rows_cap, int H,
                        const int32_t* __restrict__ inv_pos, const float* __restrict__ topk_w,
                        int T, int k, int k_routed, float w_shared, void* __restrict__ out,
                        int out_bf16) {
@@ -245,8 +257,7 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
       for (int q = 0; q < kQ; ++q)
         y[b][q] = (pos[b] >= 0 && (q == 0 || q1))
-                      ? __ldg(reinterpret_cast<const float4*>(Y + static_cast<size_t>(pos[b]) * H +
-                                                              h + 4 * q))
+                      ? load_y4(Y, static_cast<size_t>(pos[b]) * H + h + 4 * q)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 2
     for (int s = 1; s < splits; ++s) {
@@ -256,8 +267,7 @@ __global__ void __launch_bounds__(kCombineThreads)
 #pragma unroll
         for (int q = 0; q < kQ; ++q) {
           if (q == 1 && !q1) continue;
-          const float4 ys = __ldg(reinterpret_cast<const float4*>(
-              Y + s * slice + static_cast<size_t>(pos[b]) * H + h + 4 * q));
+          const float4 ys = load_y4(Y, s * slice + static_cast<size_t>(pos[b]) * H + h + 4 * q);
           y[b][q].x += ys.x; y[b][q].y += ys.y; y[b][q].z += ys.z; y[b][q].w += ys.w;
         }
       }
@@ -291,24 +301,36 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
-cudaError_t launch_combine(const float* Y, int splits, int rows_cap, int H, const int32_t* inv_pos,
-                           const float* topk_w, int T, int k,
-                           int k_routed, float w_shared, void* out, int out_bf16,
-                           cudaStream_t st, bool pdl) {
+template <typename TY>
+cudaError_t launch_combine_t(const TY* Y, int splits, int rows_cap, int H,
+                             const int32_t* inv_pos, const float* topk_w, int T, int k,
+                             int k_routed, float w_shared, void* out, int out_bf16,
+                             cudaStream_t st, bool pdl) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int wide_blocks = T * ((H + 8 * kCombineThreads - 1) / (8 * kCombineThreads));
   if (wide_blocks >= 4 * sms) {
     const dim3 grid(T, (H + 8 * kCombineThreads - 1) / (8 * kCombineThreads));
-    return launch_kernel(moe_combine_kernel<8, 4>, grid, dim3(kCombineThreads), 0, st, pdl, Y,
-                         splits, rows_cap, H, inv_pos, topk_w, T, k, k_routed, w_shared, out,
+    return launch_kernel(moe_combine_kernel<8, 4, TY>, grid, dim3(kCombineThreads), 0, st, pdl,
+                         Y, splits, rows_cap, H, inv_pos, topk_w, T, k, k_routed, w_shared, out,
                          out_bf16);
   }
   const dim3 grid(T, (H + 4 * kCombineThreads - 1) / (4 * kCombineThreads));
-  return launch_kernel(moe_combine_kernel<4, 8>, grid, dim3(kCombineThreads), 0, st, pdl, Y,
+  return launch_kernel(moe_combine_kernel<4, 8, TY>, grid, dim3(kCombineThreads), 0, st, pdl, Y,
                        splits, rows_cap, H, inv_pos, topk_w, T, k, k_routed, w_shared, out,
                        out_bf16);
+}
+
+cudaError_t launch_combine(const void* Y, int y_bf16, int splits, int rows_cap, int H,
+                           const int32_t* inv_pos, const float* topk_w, int T, int k,
+                           int k_routed, float w_shared, void* out, int out_bf16,
+                           cudaStream_t st, bool pdl) {
+  if (y_bf16)
+    return launch_combine_t(static_cast<const __nv_bfloat16*>(Y), 1, rows_cap, H, inv_pos,
+                            topk_w, T, k, k_routed, w_shared, out, out_bf16, st, pdl);
+  return launch_combine_t(static_cast<const float*>(Y), splits, rows_cap, H, inv_pos, topk_w, T,
+                          k, k_routed, w_shared, out, out_bf16, st, pdl);
 }
 
 // ---------------------------------------------------------------- router

@@ -42,6 +42,7 @@ struct Plan {
   // (routed + shared); the IdMap maps topk_ids onto them.
   int T, H, I, E, k, bm, fp8, out_bf16;
   int co;                  // coalesced work list: tiles of up to co rows (0: the task map)
+  int y16;                 // unsplit Down: bf16 output rows (else fp32 partials)
   int bn;                  // token rows of the GEMM kernels' tile: co, else bm
   int w8;                  // w8a16: e4m3 weights dequantised on chip, bf16 activations
   IdMap map;
@@ -278,6 +279,10 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     p->s2 = (p->kt2 + p->kts2 - 1) / p->kts2;
   }
   p->fused_act = !p->fp8 && p->s1 == 1 && !(o && o->separate_act);
+  // An unsplit Down GEMM stores its rows in bf16 (the combine's input), half
+  // the bytes of fp32 partials written and read back (prefill: 268 MB of
+  // fp32 rows at the Qwen3-shaped T=4096)
+  p->y16 = p->s2 == 1 && !p->w8;
   if (o && (o->unit_order < 0 || o->unit_order > 2)) return MOE_ERR_ARG;
   if (o && o->pipeline_wait_ns < 0) return MOE_ERR_ARG;
   if (o && o->unit_order) {
@@ -334,7 +339,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
       p->fused_act ? 0 : 4 * static_cast<size_t>(p->s1) * rc * 2 * s->I,
       rc * s->I * (p->fp8 ? 1 : 2),
       p->fp8 ? 4 * rc * (s->I / 128) : 0,
-      4 * static_cast<size_t>(p->s2) * rc * s->H,
+      (p->y16 ? 2 : 4 * static_cast<size_t>(p->s2)) * rc * s->H,
       p->routed ? p->rp_bytes : 0,
       p->route_fused ? 8u : 0u,
       p->route_fused ? 4 * static_cast<size_t>(p->rp_owners_cap) * p->E : 0,
@@ -384,6 +389,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->off_y = p.off[kOffY];
   L->total_bytes = p.total;
   L->coalesce_rows = p.co;
+  L->y_bf16 = p.y16;
   L->off_work_tiles = p.off[kOffWorkTiles];
   L->off_num_work_tiles = p.off[kOffNumWorkTiles];
 }
@@ -821,6 +827,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g2.tiles_cap = p.tiles_cap;
   g2.early_weights = 1;   // the index is complete before this grid launches
   g2.out = Y;
+  g2.out_bf16 = p.y16;
   g2.rows_cap = p.rows_cap;
   g2.dev_status = dev_status;
   g2.pipe_wait_ns = wait_ns;
@@ -831,7 +838,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   record(opts, 5, s);
-  e = launch_combine(Y, p.s2, p.rows_cap, p.H, ip.inv_pos, topk_w, p.T, p.k, p.map.k, p.w_shared,
+  e = launch_combine(Y, p.y16, p.s2, p.rows_cap, p.H, ip.inv_pos, topk_w, p.T, p.k, p.map.k, p.w_shared,
                      out, p.out_bf16, s,
                      pdl);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -901,7 +908,7 @@ moe_status moe_combine(const moe_shape* shape, int32_t splits, int32_t rows_cap,
   if (shape->T < 1 || shape->k < 1 || shape->H < 4 || shape->H % 4 || splits < 1 || rows_cap < 1)
     return MOE_ERR_SHAPE;
   if (!aligned(y, 16) || !aligned(out, 16)) return MOE_ERR_ALIGN;
-  return cuda_status(launch_combine(y, splits, rows_cap, shape->H, inv_pos, topk_w, shape->T,
+  return cuda_status(launch_combine(y, 0, splits, rows_cap, shape->H, inv_pos, topk_w, shape->T,
                                     shape->k, shape->k, 1.0f, out,
                                     shape->out_dtype == MOE_OUT_BF16,
                                     static_cast<cudaStream_t>(stream), false));

@@ -48,7 +48,8 @@ def test_plan_is_consistent(T, H, I, E, k, fp8):
             L.off_inv_pos, L.off_num_tiles, L.off_index_scratch, L.off_xq, L.off_xs, L.off_g, L.off_a, L.off_as,
             L.off_y]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
-    assert L.off_y + 4 * L.split_down * L.rows_cap * H <= L.total_bytes
+    assert L.y_bf16 == (L.split_down == 1)   # an unsplit Down stores bf16 rows
+    assert L.off_y + (2 if L.y_bf16 else 4 * L.split_down) * L.rows_cap * H <= L.total_bytes
     assert moe.moe_workspace_bytes(s) == L.total_bytes
     # forced splits are honoured and resize the workspace
     o = moe.make_opts(split_gateup=2, split_down=3)
