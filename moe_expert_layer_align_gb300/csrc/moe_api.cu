@@ -81,17 +81,19 @@ int64_t tiles_cap_of(int64_t T, int64_t k, int64_t E, int64_t bm) {
 // FP8 takes 128 where this gives 64: 128-row FP8 tiles run token-major with
 // per-thread block scales, cheaper to promote than the swap-AB 64-row tile
 // (DeepSeek-shaped layer at T=1024: 2.23 ms against 2.47 ms).
-// bf16 takes 256 where an active expert holds 384 rows or more on average and
-// both GEMMs pair two weight tiles per unit (`pair`): the 256 x 256 token-major
-// tile then stages 64 MACs per operand byte against the 128-row tiles' 43
-// (Mixtral-shaped layer at T=2048: 1366 -> 1248 us).  With fewer rows per
-// expert its half-empty tiles cost more than it saves (Mixtral-shaped T=512:
-// 572 -> 610 us; Qwen3-shaped T=4096, 256 rows per expert: 495 -> 543 us).
+// bf16 takes 256 where an active expert holds 128 rows or more on average and
+// both GEMMs pair two weight tiles per unit (`pair`): the token-major tile
+// (one or two 128-row token halves against one N = 256 operand of both
+// weight tiles) stages 64 MACs per operand byte with two halves against the
+// 128-row tiles' 43, and issues half as many MMAs per stage even with one
+// (Mixtral-shaped layer at T=2048: 1366 -> 1248 us; T=512, 128 rows per
+// expert: 576 -> 527 us; Qwen3-shaped T=4096, 256 +- 16 rows: 445 -> 422 us;
+// at 64 rows, Qwen3-shaped T=1024, it measured 279 -> 284 us).
 int auto_bm(int T, int k, int E, int fp8, bool pair) {
   const double tk = static_cast<double>(T) * k;
   const double active = E * (1.0 - std::pow(1.0 - static_cast<double>(k) / E, T));
   const double mean = tk / std::max(1.0, std::min(active, tk));
-  if (!fp8 && pair && mean >= 384) return 256;
+  if (!fp8 && pair && mean >= 128) return 256;
   const int cap = 128;
   int bm = 16;
   while (bm < cap && bm < 1.5 * mean) bm *= 2;
