@@ -190,6 +190,13 @@ typedef struct {
    * C > block_m (not for MOE_W8A16).  Other values: MOE_ERR_ARG.  Results do
    * not depend on it. */
   int32_t coalesce_rows;
+  /* Layers whose index has 256-row tiles (the planner's choice for BF16
+   * layers with 128 or more rows per active expert): 128 makes the Down GEMM
+   * take each expert's rows in tiles of up to 128 (a work list over the same
+   * index) with the 128-row tile instead of the 256-row token-major one;
+   * -1 keeps the 256-row tiles; 0: planner.  Other values: MOE_ERR_ARG.
+   * Results do not depend on it. */
+  int32_t down_tile_rows;
 } moe_forward_opts;
 
 /* Options of moe_align_ex: the same shared-expert and expert-parallel mapping
@@ -227,10 +234,12 @@ typedef struct {
   size_t off_route_counter; /* fused routing: two grid-barrier counters (8 bytes) */
   size_t total_bytes;
   size_t off_route_hist;    /* fused routing: per-CTA expert counts           */
-  int32_t coalesce_rows;    /* C of the work list, 0 when the GEMMs take the task map */
-  size_t off_work_tiles;    /* work list: int32 [tiles_cap][4] {expert, first row, rows, 0} */
+  int32_t coalesce_rows;    /* Gate-Up: C of the work list it takes, 0 for the task map */
+  size_t off_work_tiles;    /* work list: int32 [work_cap][4] {expert, first row, rows, 0} */
   size_t off_num_work_tiles;  /* its length (int32) */
   int32_t y_bf16;           /* 1: the Down GEMM is unsplit and stores bf16 rows at off_y */
+  int32_t down_tile_rows;   /* Down: C of the work list it takes, 0 for the task map */
+  int32_t work_cap;         /* entries of the work list (0 when there is none) */
 } moe_workspace_layout;
 
 /* tiles_cap of the index for these sizes (0 on invalid arguments). */

@@ -48,7 +48,8 @@ class moe_forward_opts(ctypes.Structure):
                 ("smem_index", _i32), ("single_weight_tile", _i32),
                 ("num_shared_experts", _i32), ("shared_expert_weight", ctypes.c_float),
                 ("ep_first_expert", _i32), ("ep_num_experts", _i32), ("fuse_routing", _i32),
-                ("unit_order", _i32), ("pipeline_wait_ns", _i32), ("coalesce_rows", _i32)]
+                ("unit_order", _i32), ("pipeline_wait_ns", _i32), ("coalesce_rows", _i32),
+                ("down_tile_rows", _i32)]
 
 
 class moe_align_opts(ctypes.Structure):
@@ -65,7 +66,7 @@ class moe_workspace_layout(ctypes.Structure):
                            "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "off_router",
                            "off_route_counter", "total_bytes", "off_route_hist")] + [
         ("coalesce_rows", _i32), ("off_work_tiles", _sz), ("off_num_work_tiles", _sz),
-        ("y_bf16", _i32)]
+        ("y_bf16", _i32), ("down_tile_rows", _i32), ("work_cap", _i32)]
 
 
 def _load() -> ctypes.CDLL:
@@ -162,8 +163,10 @@ def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
               stage_events=None, separate_act=False, smem_index=None,
               single_weight_tile=False, num_shared_experts=0, shared_expert_weight=0.0,
               ep_first_expert=0, ep_num_experts=0, fuse_routing=None,
-              unit_order=0, pipeline_wait_ns=0, coalesce_rows=0) -> moe_forward_opts:
+              unit_order=0, pipeline_wait_ns=0, coalesce_rows=0,
+              down_tile_rows=0) -> moe_forward_opts:
     o = moe_forward_opts()
+    o.down_tile_rows = down_tile_rows   # 0 planner, -1 off, 128
     o.coalesce_rows = coalesce_rows   # 0 planner, -1 off, 32 / 64
     o.pipeline_wait_ns = pipeline_wait_ns
     o.unit_order = unit_order
@@ -399,8 +402,9 @@ def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None, routed
         Y=(v(L.off_y, rc * H, torch.bfloat16, (1, rc, H)) if L.y_bf16 else
            v(L.off_y, L.split_down * rc * H, torch.float32, (L.split_down, rc, H))),
     )
-    if L.coalesce_rows:
-        out["work_tiles"] = v(L.off_work_tiles, 4 * tc, torch.int32, (tc, 4))
+    if L.work_cap:
+        wc = L.work_cap
+        out["work_tiles"] = v(L.off_work_tiles, 4 * wc, torch.int32, (wc, 4))
         out["num_work_tiles"] = v(L.off_num_work_tiles, 1, torch.int32, (1,))
     if not L.fused_act:
         out["G"] = v(L.off_g, L.split_gateup * rc * 2 * I, torch.float32,

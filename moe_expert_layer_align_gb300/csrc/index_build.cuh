@@ -290,7 +290,7 @@ __device__ __forceinline__ void index_write_tiles(int E, int bm, int tiles_cap, 
   }
   if (C > 0 && idx.work_tiles) {
     if (tid == 0) *idx.num_work_tiles = sc.coffs[E];
-    for (int q = tid; q < tiles_cap; q += nthreads)
+    for (int q = tid; q < idx.work_cap; q += nthreads)
       reinterpret_cast<int4*>(idx.work_tiles)[q] = index_work_tile(q, E, C, sc);
   }
 }

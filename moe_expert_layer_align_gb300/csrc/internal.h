@@ -78,6 +78,8 @@ struct GemmParams {
   // BN rows).
   int coalesce;
   int index_bm;              // rows per index tile (0: BN)
+  int list_cap;              // entries of the list at `tiles` (0: tiles_cap; the work
+                             // list of smaller tiles than the index's holds more)
   // Unsplit GEMM (splits == 1), no fused activation: the output rows are
   // stored as bf16 [rows_cap][M] instead of fp32 partials.
   int out_bf16;
@@ -111,9 +113,10 @@ cudaError_t launch_gemm_w8(int bn, int bsrc, int grid, cudaStream_t st, bool pdl
 struct IndexPtrs {
   int32_t *counts, *offsets, *sorted_ids, *tile_expert, *tiles, *inv_pos, *num_tiles;
   // Optional (moe_forward with coalesced units): the work list of tiles of up
-  // to `coalesce` rows, {expert, first row, rows, 0} x tiles_cap, and its length.
+  // to `coalesce` rows, {expert, first row, rows, 0} x work_cap, and its length.
   int32_t *work_tiles = nullptr, *num_work_tiles = nullptr;
   int coalesce = 0;
+  int work_cap = 0;
 };
 // k and E below count assignments per token and experts of the index (map.kk
 // and map.E + shared experts); `map` turns topk_ids into index experts.

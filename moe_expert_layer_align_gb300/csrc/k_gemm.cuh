@@ -340,6 +340,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
   SmemIndex si;
   const bool smem_idx = BSRC != kDense && p.smem_index;
   const int ibm = p.index_bm ? p.index_bm : BN;   // rows per index tile
+  const int lcap = p.list_cap ? p.list_cap : p.tiles_cap;   // entries of this GEMM's list
   if (smem_idx) {
     // The top-k ids are an input of the call: complete before its first
     // kernel started, so they are read without waiting on the predecessor.
@@ -351,7 +352,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
                   [](int) {});
     index_pads(p.E, p.rows_cap, si.sc, [&](int pos) { si.rows[pos] = tk; });
     // this CTA's task map: the work list with coalesced units
-    for (int q = threadIdx.x; q < p.tiles_cap; q += S::kThreads)
+    for (int q = threadIdx.x; q < lcap; q += S::kThreads)
       si.tiles[q] = p.coalesce ? index_work_tile(q, p.E, p.coalesce, si.sc)
                                : index_tile(q, p.E, ibm, si.sc);
   }
@@ -368,12 +369,12 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
   // before letting this grid launch).
   const bool early = smem_idx || (BSRC == kDirect && p.early_weights);
   if (smem_idx) {
-    num_tiles = p.coalesce ? si.sc.coffs[p.E] : si.sc.offs[p.E] / ibm;
+    num_tiles = min(p.coalesce ? si.sc.coffs[p.E] : si.sc.offs[p.E] / ibm, lcap);
     smem_tiles = si.tiles;
   } else {
     if (!early) pdl_wait();
     num_tiles = (BSRC == kDense) ? (p.dense_rows + BN - 1) / BN
-                                 : min(max(__ldcg(p.num_tiles), 0), p.tiles_cap);
+                                 : min(max(__ldcg(p.num_tiles), 0), lcap);
   }
   pdl_launch_dependents();   // dependents read nothing of ours before their own wait
   const int units = num_tiles * p.m_tiles * p.splits;
@@ -1164,7 +1165,8 @@ cudaError_t launch_gemm_inst(int grid, cudaStream_t st, bool pdl, const CUtensor
   }
   size_t smem = S::kSmemBytes;
   if (BSRC != kDense && p.smem_index)
-    smem += SmemIndex::bytes(S::kWarps, p.E, p.T * p.topk, p.rows_cap, p.tiles_cap);
+    smem += SmemIndex::bytes(S::kWarps, p.E, p.T * p.topk, p.rows_cap,
+                             p.list_cap ? p.list_cap : p.tiles_cap);
   if (smem > kMaxGemmSmem) return cudaErrorInvalidValue;
   return launch_kernel(kern, dim3(grid), dim3(S::kThreads), smem, st, pdl, a, b, p);
 }

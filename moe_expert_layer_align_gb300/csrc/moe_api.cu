@@ -28,6 +28,9 @@ constexpr int kSplitIndexMinAssignments = 2048;
 // Coalesced work list the planner uses over 16- and 32-row index tiles
 // (0: none).
 constexpr int kPlanCoalesce = 0;
+// 256-row token tiles: the planner gives the Down GEMM 128-row tiles of a
+// work list where I (its K) is at most this (0: never).
+constexpr int kPlanDownSplitMaxI = 0;
 // Router GEMM split-K count bound (the top-k sums at most this many partials).
 constexpr int kRouterMaxSplitsHost = 4;
 
@@ -41,13 +44,16 @@ struct Plan {
   // k, E: assignments per token and experts of the index and the weights
   // (routed + shared); the IdMap maps topk_ids onto them.
   int T, H, I, E, k, bm, fp8, out_bf16;
-  int co;                  // coalesced work list: tiles of up to co rows (0: the task map)
+  int co;                  // work list written by the index: tiles of up to co rows (0: none)
+  int co1, co2;            // work-list tile rows each GEMM takes (0: the task map)
+  int bn1, bn2;            // token rows of each GEMM kernel's tile
   int y16;                 // unsplit Down: bf16 output rows (else fp32 partials)
   int bn;                  // token rows of the GEMM kernels' tile: co, else bm
   int w8;                  // w8a16: e4m3 weights dequantised on chip, bf16 activations
   IdMap map;
   float w_shared;
   int tiles_cap, rows_cap;
+  int work_cap;            // work-list entries (tiles of co rows; co < bm needs more)
   int s1, kts1, kt1, mt1;  // Gate-Up: splits, k-tiles per split, k-tiles, weight tiles
   int s2, kts2, kt2, mt2;  // Down
   int me1, me2;            // weight tiles per work unit (2: large token tiles, bf16)
@@ -245,11 +251,26 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     const int c = want == 0 ? kPlanCoalesce : want;
     p->co = (c > p->bm && !p->w8) ? c : 0;
   }
-  p->bn = p->co ? p->co : p->bm;
+  p->co1 = p->co2 = p->co;
+  // 256-row token-major tiles: the Down GEMM may instead take the experts'
+  // rows in tiles of up to 128 (a work list over the same index) with the
+  // 128-row swap-AB tile.
+  if (o && !(o->down_tile_rows == 0 || o->down_tile_rows == -1 || o->down_tile_rows == 128))
+    return MOE_ERR_ARG;
+  if (p->bm == 256) {
+    const int want = o ? o->down_tile_rows : 0;
+    const bool split = want == 128 || (want == 0 && s->I <= kPlanDownSplitMaxI);
+    if (split) p->co = p->co2 = 128;
+  }
+  p->bn1 = p->co1 ? p->co1 : p->bm;
+  p->bn2 = p->co2 ? p->co2 : p->bm;
   const int64_t tc = tiles_cap_of(p->T, p->k, p->E, p->bm);
   if (tc * p->bm >= (int64_t(1) << 31) / 2) return MOE_ERR_SHAPE;
   p->tiles_cap = static_cast<int>(tc);
   p->rows_cap = static_cast<int>(tc * p->bm);
+  // a work list of tiles smaller than the index's holds up to this many
+  p->work_cap = p->co ? static_cast<int>(tiles_cap_of(p->T, p->k, p->E, std::min(p->co, p->bm)))
+                      : 0;
   const int kstage = (p->fp8 || p->w8) ? 128 : 64;   // K elements per pipeline stage
   p->kt1 = s->H / kstage;
   p->mt1 = s->I / 64;
@@ -305,9 +326,11 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     const int tk = p->T * p->k;
     bool fits = tk <= kSmemIndexMaxAssignments && (want == 1 || auto_on) && !p->w8;
     for (int bsrc : {static_cast<int>(kGather), static_cast<int>(kDirect)}) {
-      const size_t need = gemm_smem_bytes(p->fp8, p->bn, bsrc) +
-                          gemm_index_smem_bytes(gemm_warps(p->fp8, p->bn, bsrc), p->E, tk, p->rows_cap,
-                                                p->tiles_cap);
+      const int bn = bsrc == kGather ? p->bn1 : p->bn2;
+      const int lcap = (bsrc == kGather ? p->co1 : p->co2) ? p->work_cap : p->tiles_cap;
+      const size_t need = gemm_smem_bytes(p->fp8, bn, bsrc) +
+                          gemm_index_smem_bytes(gemm_warps(p->fp8, bn, bsrc), p->E, tk, p->rows_cap,
+                                                lcap);
       if (need > kMaxGemmSmem) fits = false;
     }
     p->smem_index = fits;
@@ -345,7 +368,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
       p->routed ? p->rp_bytes : 0,
       p->route_fused ? 8u : 0u,
       p->route_fused ? 4 * static_cast<size_t>(p->rp_owners_cap) * p->E : 0,
-      p->co ? 16u * p->tiles_cap : 0,
+      16u * p->work_cap,
       p->co ? 4u : 0u,
   };
   size_t cur = 0;
@@ -390,7 +413,9 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->off_as = p.off[kOffAs];
   L->off_y = p.off[kOffY];
   L->total_bytes = p.total;
-  L->coalesce_rows = p.co;
+  L->coalesce_rows = p.co1;
+  L->down_tile_rows = p.co2;
+  L->work_cap = p.work_cap;
   L->y_bf16 = p.y16;
   L->off_work_tiles = p.off[kOffWorkTiles];
   L->off_num_work_tiles = p.off[kOffNumWorkTiles];
@@ -622,6 +647,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
     ip.work_tiles = reinterpret_cast<int32_t*>(at(kOffWorkTiles));
     ip.num_work_tiles = reinterpret_cast<int32_t*>(at(kOffNumWorkTiles));
     ip.coalesce = p.co;
+    ip.work_cap = p.work_cap;
   }
   uint8_t* xq = at(kOffXq);
   float* xs = reinterpret_cast<float*>(at(kOffXs));
@@ -638,7 +664,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   if (!make_map_gateup(&tmW13, w13, wsize, p.H, p.I, p.E, p.w8) ||
       !make_map_2d(&tmX, p.fp8 ? static_cast<const void*>(xq) : x, esize, p.H, p.T, 1) ||
       !make_map_3d(&tmW2, w2, wsize, p.I, p.H, p.E, 128, p.w8) ||
-      !make_map_2d(&tmA, A, esize, p.I, p.rows_cap, p.bm))
+      !make_map_2d(&tmA, A, esize, p.I, p.rows_cap, p.co2 ? std::min(p.bm, p.bn2) : p.bm))
     return MOE_ERR_CUDA;
 
   const int sms = device_sms();
@@ -761,9 +787,9 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.kt_per_split = p.kts1;
   g1.kt_total = p.kt1;
   g1.tile_major = p.ord1 == 2;
-  g1.tiles = p.co ? ip.work_tiles : ip.tiles;
-  g1.num_tiles = p.co ? ip.num_work_tiles : ip.num_tiles;
-  g1.coalesce = p.co;
+  g1.tiles = p.co1 ? ip.work_tiles : ip.tiles;
+  g1.num_tiles = p.co1 ? ip.num_work_tiles : ip.num_tiles;
+  g1.coalesce = p.co1;
   g1.index_bm = p.bm;
   g1.sorted_ids = ip.sorted_ids;
   g1.b_rows = p.fp8 ? static_cast<const void*>(xq) : x;
@@ -781,6 +807,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.E = p.E;
   g1.idmap = p.map;
   g1.tiles_cap = p.tiles_cap;
+  g1.list_cap = p.co1 ? p.work_cap : p.tiles_cap;
   g1.write_index = p.smem_index;
   g1.clear_status = p.smem_index && rc == nullptr;   // the Gate-Up is the call's first kernel
   g1.index_out = {ip.counts, ip.offsets, ip.sorted_ids, ip.tile_expert, ip.tiles, ip.inv_pos,
@@ -790,9 +817,9 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.rows_cap = p.rows_cap;
   g1.dev_status = dev_status;
   g1.pipe_wait_ns = wait_ns;
-  const int units1 = g1.m_tiles * p.s1 * p.tiles_cap;
+  const int units1 = g1.m_tiles * p.s1 * g1.list_cap;
   e = p.w8 ? launch_gemm_w8(p.bm, kGather, std::min(grid_cap, units1), s, chain(), tmW13, tmX, g1)
-           : launch_gemm(p.fp8, p.bn, kGather, std::min(grid_cap, units1), s, chain(), tmW13,
+           : launch_gemm(p.fp8, p.bn1, kGather, std::min(grid_cap, units1), s, chain(), tmW13,
                          tmX, g1, p.me1);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -812,9 +839,9 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g2.kt_per_split = p.kts2;
   g2.kt_total = p.kt2;
   g2.tile_major = p.ord2 == 2;
-  g2.tiles = p.co ? ip.work_tiles : ip.tiles;
-  g2.num_tiles = p.co ? ip.num_work_tiles : ip.num_tiles;
-  g2.coalesce = p.co;
+  g2.tiles = p.co2 ? ip.work_tiles : ip.tiles;
+  g2.num_tiles = p.co2 ? ip.num_work_tiles : ip.num_tiles;
+  g2.coalesce = p.co2;
   g2.index_bm = p.bm;
   g2.sorted_ids = ip.sorted_ids;
   g2.topk = p.k;
@@ -827,15 +854,16 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g2.E = p.E;
   g2.idmap = p.map;
   g2.tiles_cap = p.tiles_cap;
+  g2.list_cap = p.co2 ? p.work_cap : p.tiles_cap;
   g2.early_weights = 1;   // the index is complete before this grid launches
   g2.out = Y;
   g2.out_bf16 = p.y16;
   g2.rows_cap = p.rows_cap;
   g2.dev_status = dev_status;
   g2.pipe_wait_ns = wait_ns;
-  const int units2 = g2.m_tiles * p.s2 * p.tiles_cap;
+  const int units2 = g2.m_tiles * p.s2 * g2.list_cap;
   e = p.w8 ? launch_gemm_w8(p.bm, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2)
-           : launch_gemm(p.fp8, p.bn, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2,
+           : launch_gemm(p.fp8, p.bn2, kDirect, std::min(grid_cap, units2), s, pdl, tmW2, tmA, g2,
                          p.me2);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

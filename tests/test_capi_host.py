@@ -246,15 +246,17 @@ def test_wait_limit_option_changes_no_plan_and_rejects_negatives():
 def test_coalesce_option_plan(T, H, I, E, k, fp8, bm):
     s = moe.make_shape(T, H, I, E, k, bm, fp8, True)
     base = moe.moe_plan(s, moe.make_opts(coalesce_rows=-1))
-    assert base.coalesce_rows == 0 and base.off_work_tiles == base.off_num_work_tiles
+    assert base.coalesce_rows == 0 and base.work_cap == 0
+    assert base.off_work_tiles == base.off_num_work_tiles
     for c in (32, 64):
         L = moe.moe_plan(s, moe.make_opts(coalesce_rows=c))
         # the index is the same (block_m, caps); the work list is used where C > block_m
         assert (L.block_m, L.tiles_cap, L.rows_cap) == (base.block_m, base.tiles_cap, base.rows_cap)
         assert L.coalesce_rows == (c if c > L.block_m else 0)
         if L.coalesce_rows:
+            assert L.work_cap == L.tiles_cap        # tiles larger than the index's: no more of them
             assert L.off_work_tiles >= L.off_route_hist
-            assert L.off_work_tiles + 16 * L.tiles_cap <= L.off_num_work_tiles
+            assert L.off_work_tiles + 16 * L.work_cap <= L.off_num_work_tiles
             assert L.off_num_work_tiles + 4 <= L.total_bytes
             assert L.total_bytes > base.total_bytes
     for bad in (-2, 16, 48, 128):
@@ -266,3 +268,22 @@ def test_coalesce_option_plan(T, H, I, E, k, fp8, bm):
         sw = moe.make_shape(T, H, I, E, k, bm, False, True)
         sw.mode = moe.MOE_W8A16
         assert moe.moe_plan(sw, moe.make_opts(coalesce_rows=64)).coalesce_rows == 0
+
+
+def test_down_tile_rows_option_plan():
+    # Qwen3-shaped T=4096: 256 rows per expert, 256-row token tiles
+    s = moe.make_shape(4096, 2048, 768, 128, 8, 0, False, True)
+    L0 = moe.moe_plan(s, moe.make_opts(down_tile_rows=-1))
+    assert L0.block_m == 256 and L0.down_tile_rows == 0 and L0.work_cap == 0
+    L = moe.moe_plan(s, moe.make_opts(down_tile_rows=128))
+    assert L.block_m == 256 and L.down_tile_rows == 128 and L.coalesce_rows == 0
+    # 128-row tiles of an index padded to 256: up to ceil(T*k/128) + E of them
+    assert L.work_cap == moe.moe_index_tiles_cap(4096, 8, 128, 128) > L.tiles_cap
+    assert L.off_work_tiles + 16 * L.work_cap <= L.off_num_work_tiles < L.total_bytes
+    # no effect where the index tiles are not 256 rows
+    s2 = moe.make_shape(64, 2048, 768, 128, 8, 0, False, True)
+    assert moe.moe_plan(s2, moe.make_opts(down_tile_rows=128)).down_tile_rows == 0
+    for bad in (-2, 64, 256):
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_plan(s, moe.make_opts(down_tile_rows=bad))
+        assert ei.value.status == moe.MOE_ERR_ARG

@@ -88,7 +88,7 @@ def test_coalesced_tiles_match_oracle_and_task_map(cfg, T, kw, C, smem_index, ex
             np.testing.assert_array_equal(v[n].cpu().numpy().reshape(-1), ref[n].reshape(-1), n)
         if c > 0 and not smem_index:
             # (with the shared-memory index each CTA keeps its work list on chip)
-            exp, n_exp = expected_work_list(ref["counts"], ref["offsets"], C, L.tiles_cap)
+            exp, n_exp = expected_work_list(ref["counts"], ref["offsets"], C, L.work_cap)
             assert v["num_work_tiles"].item() == n_exp
             np.testing.assert_array_equal(v["work_tiles"].cpu().numpy(), exp)
     counts = np.bincount(ids.cpu().numpy().reshape(-1), minlength=wl.E)
@@ -98,3 +98,39 @@ def test_coalesced_tiles_match_oracle_and_task_map(cfg, T, kw, C, smem_index, ex
     assert_layer_close(outs[C].double().cpu().numpy(),
                        oracle_layer(wl, topk_ids=ids.cpu(), topk_w=w.cpu()), wl.mode,
                        f"cfg{cfg} T={T} C={C}")
+
+
+DOWN_SPLIT_CASES = [
+    # cfg, T, overrides: 150, 175 and 300 rows per expert (256-row index tiles)
+    (3, 300, dict(H=256, I=128, E=16)),
+    (2, 700, dict(H=256, I=384)),
+    (3, 600, dict(H=256, I=128, E=16)),
+    (1, 600, dict(E=8)),
+]
+
+
+@pytest.mark.parametrize("cfg,T,kw", DOWN_SPLIT_CASES)
+def test_down_tiles_of_128_rows_over_a_256_row_index(cfg, T, kw):
+    """down_tile_rows=128: the Gate-Up keeps the 256-row token-major tiles of
+    the task map, the Down GEMM takes a work list of tiles of up to 128 rows
+    of the same index (more entries than the task map: its own capacity)."""
+    import moe_expert_layer_align_gb300 as moe
+    wl = workloads.make(cfg, T, "cpu", **kw).to("cuda")
+    out_dtype = torch.float32 if wl.out == "f32" else torch.bfloat16
+    shape = moe.layer_shape(wl.x, wl.w13, wl.topk_ids, 0, out_dtype)
+    opts = moe.make_opts(down_tile_rows=128, smem_index=False)
+    ws = torch.zeros(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    out = run_layer(wl, opts=opts, dev_status=status, workspace=ws)
+    torch.cuda.synchronize()
+    assert status.item() == 0, moe.device_status_bits(status.item())
+    v = moe.workspace_views(ws, shape, opts)
+    L = v["layout"]
+    assert L.block_m == 256 and L.down_tile_rows == 128 and L.coalesce_rows == 0
+    ref = oracle.align(wl.topk_ids.cpu().numpy(), wl.E, 256)
+    for n in INDEX_FIELDS:
+        np.testing.assert_array_equal(v[n].cpu().numpy().reshape(-1), ref[n].reshape(-1), n)
+    exp, n_exp = expected_work_list(ref["counts"], ref["offsets"], 128, L.work_cap)
+    assert v["num_work_tiles"].item() == n_exp > int(v["num_tiles"].item())
+    np.testing.assert_array_equal(v["work_tiles"].cpu().numpy(), exp)
+    assert_layer_close(out.double().cpu().numpy(), oracle_layer(wl), wl.mode, f"cfg{cfg} T={T}")
