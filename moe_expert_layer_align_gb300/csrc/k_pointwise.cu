@@ -370,9 +370,85 @@ __global__ void __launch_bounds__(128)
   if (t < T) router_topk_warp(P, splits, rows_cap, t, E, k, score_fn, scale, scores, ids, w);
 }
 
+// Many split-K partials (few tokens, the router GEMM spread over many CTAs):
+// a block of eight warps per token.  Warp g loads the partials of splits
+// [g*G, (g+1)*G) (G = ceil(splits / 8) <= 4) all at once and sums them in
+// split order; warp 0 adds the eight group sums in group order, then selects.
+// (One warp looping over 32 splits would wait for eight L2 round trips.)
+constexpr int kTopkGroups = 8;
+template <int kPer>
+__global__ void __launch_bounds__(32 * kTopkGroups)
+    moe_router_topk_block_kernel(const float* __restrict__ P, int splits, int rows_cap, int T,
+                                 int E, int k, int score_fn, float scale,
+                                 float* __restrict__ scores, int32_t* __restrict__ ids,
+                                 float* __restrict__ w) {
+  __shared__ float part[kTopkGroups][2][32 * kPer];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t slice = static_cast<size_t>(rows_cap) * 2 * E;
+  const float* row = P + static_cast<size_t>(t) * 2 * E;
+  const int G = (splits + kTopkGroups - 1) / kTopkGroups;
+  float ph[kRouterMaxSplits][kPer], pl[kRouterMaxSplits][kPer];
+#pragma unroll
+  for (int j = 0; j < kRouterMaxSplits; ++j)
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int sp = g * G + j, e = lane + 32 * i;
+      const bool in = j < G && sp < splits && e < E;
+      ph[j][i] = in ? __ldg(row + sp * slice + e) : 0.f;
+      pl[j][i] = in ? __ldg(row + sp * slice + E + e) : 0.f;
+    }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    float hi = ph[0][i], lo = pl[0][i];
+#pragma unroll
+    for (int j = 1; j < kRouterMaxSplits; ++j) {
+      hi += ph[j][i];
+      lo += pl[j][i];
+    }
+    part[g][0][lane + 32 * i] = hi;
+    part[g][1][lane + 32 * i] = lo;
+  }
+  __syncthreads();
+  if (g != 0) return;
+  float s[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    float v = -INFINITY;
+    if (e < E) {
+      float hi = part[0][0][e], lo = part[0][1][e];
+#pragma unroll
+      for (int q = 1; q < kTopkGroups; ++q) {
+        hi += part[q][0][e];
+        lo += part[q][1][e];
+      }
+      v = hi + lo * (1.0f / 256.0f);
+      scores[static_cast<size_t>(t) * E + e] = v;
+    }
+    s[i] = v;
+  }
+  router_select_warp<kPer>(s, t, E, k, score_fn, scale, ids, w, nullptr);
+}
+
 cudaError_t launch_router_topk(const float* P, int splits, int rows_cap, int T, int E, int k,
                                int score_fn, float scale, float* scores, int32_t* ids, float* w,
                                cudaStream_t st, bool pdl) {
+  if (splits > kRouterMaxSplits) {
+    if (splits > kRouterMaxSplits * kTopkGroups) return cudaErrorInvalidValue;
+    if (E <= 128)
+      return launch_kernel(moe_router_topk_block_kernel<4>, dim3(T), dim3(32 * kTopkGroups), 0,
+                           st, pdl, P, splits, rows_cap, T, E, k, score_fn, scale, scores, ids,
+                           w);
+    if (E <= 256)
+      return launch_kernel(moe_router_topk_block_kernel<8>, dim3(T), dim3(32 * kTopkGroups), 0,
+                           st, pdl, P, splits, rows_cap, T, E, k, score_fn, scale, scores, ids,
+                           w);
+    return launch_kernel(moe_router_topk_block_kernel<kRouterMaxE / 32>, dim3(T),
+                         dim3(32 * kTopkGroups), 0, st, pdl, P, splits, rows_cap, T, E, k,
+                         score_fn, scale, scores, ids, w);
+  }
   return launch_kernel(moe_router_topk_kernel, dim3((T + 3) / 4), dim3(128), 0, st, pdl, P, splits,
                        rows_cap, T, E, k, score_fn, scale, scores, ids, w);
 }

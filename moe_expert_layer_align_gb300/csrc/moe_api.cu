@@ -31,8 +31,11 @@ constexpr int kPlanCoalesce = 0;
 // 256-row token tiles: the planner gives the Down GEMM 128-row tiles of a
 // work list where I (its K) is at most this (0: never).
 constexpr int kPlanDownSplitMaxI = 0;
-// Router GEMM split-K count bound (the top-k sums at most this many partials).
+// Router GEMM split-K count bound: one top-k warp per token sums at most 4
+// partials at once; the block top-k (few tokens) up to 32.
 constexpr int kRouterMaxSplitsHost = 4;
+constexpr int kRouterMaxSplitsWide = 32;
+constexpr int kRouterWideMaxT = 256;
 
 enum {
   kOffCounts, kOffOffsets, kOffSorted, kOffTileExpert, kOffTiles, kOffInvPos, kOffNumTiles,
@@ -197,7 +200,7 @@ struct RouterPlan {
   int bn, rows_cap, splits, kts, kt, mt;
   size_t bytes;
 };
-bool router_plan(int T, int H, int E, RouterPlan* r);
+bool router_plan(int T, int H, int E, RouterPlan* r, bool fused_front = false);
 
 // Shared experts and the expert-parallel range (moe_forward_opts /
 // moe_align_opts) as an IdMap; MOE_ERR_SHAPE on inconsistent values.
@@ -221,7 +224,8 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     // them before waiting on the previous stage) is off, and the id mapping
     // variants are not combined with the in-path router
     RouterPlan r;
-    if (!router_plan(s->T, s->H, s->E, &r) || s->k > 32) return MOE_ERR_SHAPE;
+    const bool fused = o && o->fuse_routing == 1 && !o->num_shared_experts && !o->ep_num_experts;
+    if (!router_plan(s->T, s->H, s->E, &r, fused) || s->k > 32) return MOE_ERR_SHAPE;
     if (o && (o->smem_index == 1 || o->num_shared_experts || o->ep_num_experts)) return MOE_ERR_SHAPE;
     p->routed = 1;
     p->rp_bn = r.bn, p->rp_rows_cap = r.rows_cap, p->rp_splits = r.splits, p->rp_kts = r.kts;
@@ -525,15 +529,22 @@ cudaError_t launch_gemm(int fp8, int bn, int bsrc, int grid, cudaStream_t st, bo
              : launch_gemm_bf16(bn, bsrc, grid, st, pdl, a, b, p, me);
 }
 
-bool router_plan(int T, int H, int E, RouterPlan* r) {
+// The router GEMM over [hi; lo] (2E rows, K = H) for T tokens.  Few tokens
+// leave most SMs idle at the split counts one top-k warp can sum at once, so
+// with few token tiles the split may go up to 32, which the top-k kernel
+// then reduces with a block of eight warps per token (router table shape,
+// K = 4096, N = 192 experts: 12 CTAs streaming 256 KB each at one token);
+// the fused routing front sums in one warp per token and keeps at most four.
+bool router_plan(int T, int H, int E, RouterPlan* r, bool fused_front) {
   if (T < 1 || H < 128 || H % 128 || E < 64 || E > 512 || E % 64) return false;
   r->bn = T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : 128;
   r->rows_cap = (T + r->bn - 1) / r->bn * r->bn;
   r->kt = H / 64;
   r->mt = 2 * E / 128;
-  // few splits: every score sums its partials in the top-k kernel
-  choose_split(r->mt, r->kt, r->rows_cap / r->bn, r->bn, &r->splits, &r->kts,
-               kRouterMaxSplitsHost);
+  const int tiles = r->rows_cap / r->bn;
+  const bool wide = !fused_front && T <= kRouterWideMaxT;
+  choose_split(r->mt, r->kt, tiles, r->bn, &r->splits, &r->kts,
+               wide ? kRouterMaxSplitsWide : kRouterMaxSplitsHost);
   r->bytes = 4ull * r->splits * r->rows_cap * 2 * E;
   return true;
 }

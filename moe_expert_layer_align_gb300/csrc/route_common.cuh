@@ -75,6 +75,14 @@ __device__ __forceinline__ void quant_x_groups4_warp(const __nv_bfloat16* __rest
 constexpr int kRouterMaxE = 512;
 constexpr int kRouterMaxSplits = 4;   // router GEMM split-K partials per score
 
+// Softmax (or sigmoid) and top-k of token t from its raw scores, lane l
+// holding experts l + 32 i in s[i] (-inf beyond E); one warp.
+template <int kPer>
+__device__ __forceinline__ void router_select_warp(float (&s)[kPer], int t, int E, int k,
+                                                   int score_fn, float scale,
+                                                   int32_t* __restrict__ ids,
+                                                   float* __restrict__ w, int32_t* ids_out);
+
 // kPer score slots per lane (E <= 32 * kPer).  kL2: the partials were written
 // by other CTAs of the same grid, so they are read through L2 (ld.global.cg)
 // rather than the non-coherent path.  ids_out (nullable): the selected ids
@@ -91,9 +99,8 @@ __device__ __forceinline__ void router_topk_warp_t(const float* __restrict__ P, 
   float s[kPer];
   const size_t slice = static_cast<size_t>(rows_cap) * 2 * E;
   const int per = (E + 31) / 32;   // slots this warp really uses
-  float mx = -INFINITY;
   const float* row = P + static_cast<size_t>(t) * 2 * E;
-  if constexpr (kPer <= 8) {
+  if (kPer <= 8 && splits <= kRouterMaxSplits) {
     // every partial of this lane's slots is loaded before any is summed (one
     // L2 round trip, not one per slot and split); sums run in split order
     float ph[kRouterMaxSplits][kPer], pl[kRouterMaxSplits][kPer];
@@ -122,7 +129,6 @@ __device__ __forceinline__ void router_topk_warp_t(const float* __restrict__ P, 
         scores[static_cast<size_t>(t) * E + e] = v;
       }
       s[i] = v;
-      mx = fmaxf(mx, v);
     }
   } else {
 #pragma unroll
@@ -140,9 +146,20 @@ __device__ __forceinline__ void router_topk_warp_t(const float* __restrict__ P, 
         scores[static_cast<size_t>(t) * E + e] = v;
       }
       s[i] = v;
-      mx = fmaxf(mx, v);
     }
   }
+  router_select_warp<kPer>(s, t, E, k, score_fn, scale, ids, w, ids_out);
+}
+
+template <int kPer>
+__device__ __forceinline__ void router_select_warp(float (&s)[kPer], int t, int E, int k,
+                                                   int score_fn, float scale,
+                                                   int32_t* __restrict__ ids,
+                                                   float* __restrict__ w, int32_t* ids_out) {
+  const int lane = threadIdx.x & 31;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) mx = fmaxf(mx, s[i]);
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
   float prob[kPer];

@@ -167,7 +167,10 @@ def test_routed_plan():
     assert moe.moe_routed_workspace_bytes(s, moe.make_opts(fuse_routing=True)) == L.total_bytes
     assert L.total_bytes > moe.moe_workspace_bytes(s)
     L2 = moe.moe_plan_routed(s, moe.make_opts(fuse_routing=False))
-    assert L2.route_fused == 0 and L2.total_bytes < L.total_bytes
+    assert L2.route_fused == 0 and L2.total_bytes > moe.moe_workspace_bytes(s)
+    # separate kernels: the router GEMM may split further (a block of warps per
+    # token sums the partials), the fused front keeps at most four splits
+    assert L2.off_route_counter - L2.off_router >= L.off_route_counter - L.off_router
     assert moe.moe_plan_routed(moe.make_shape(4096, 2048, 768, 128, 8, 0, True),
                                moe.make_opts(fuse_routing=True)).route_fused == 1
     o = moe.make_opts()
