@@ -4,24 +4,29 @@
 //
 // The weights stream from HBM as e4m3 bytes (half the bytes of bf16) with one
 // fp32 scale per 128x128 block.  tcgen05's kind::f16 MMA needs both operands
-// bf16, so converter warps turn every weight stage into a bf16 tile in shared
-// memory — e4m3 to fp16 (exact), to fp32 (exact), times the block scale, to
-// bf16 (round to nearest even) — and the MMA, the epilogue (with the fused
-// SiLU-and-mul) and the token operand are those of the bf16 layer.
+// bf16, so converter warps turn every weight stage into a bf16 tile — e4m3 to
+// fp16 (exact), to fp32 (exact), times the block scale, to bf16 (round to
+// nearest even) — and the MMA, the epilogue (with the fused SiLU-and-mul) and
+// the token operand are those of the bf16 layer.  The converted tile goes to
+// tensor memory, as the MMA's A operand (a weight row per TMEM lane, two bf16
+// of K per column): a converter thread owns one weight row, reads its e4m3
+// bytes from shared memory and writes the row's bf16 values with one
+// tcgen05.st.  (Converting into shared memory instead put the bf16 tile's
+// write and the MMA's read of it — 64 KB per 16 KB stage — on the shared
+// memory the TMA and the gathered token rows also use.)
 //
 // A stage is one 128-wide K block (one block scale).  Two rings: R raw slots
 // (the e4m3 weight stage as two 64-wide halves of 128 rows x 64 bytes, one TMA
-// box each, plus for the Down GEMM its token rows as two 64-wide bf16
-// sub-tiles) filled by TMA, and C converted
-// slots (two 128-row x 64-wide bf16 sub-tiles, 128-byte swizzle, plus for the
-// Gate-Up GEMM the gathered token rows as two sub-tiles).  The MMA issues
-// eight instructions per stage.  (64-wide stages cost the MMA thread the same
-// waits, fence and commits per stage for half the bytes, and it was the
-// kernel's limit: issuing 65 % of the time.)  A Gate-Up raw slot is released
-// by the converter warps once they have read it; a Down raw slot, whose token
-// rows the MMA reads, when that MMA completes; a converted slot likewise.
-// The raw ring is as deep as shared memory allows
-// because in the decode regime the weight stream is what the kernel waits on.
+// box each with the 64-byte swizzle, so that the 32 rows a converter warp
+// reads fall in different banks, plus for the Down GEMM its token rows as two
+// 64-wide bf16 sub-tiles) filled by TMA, and C converted slots: 64 TMEM
+// columns of A each (plus for the Gate-Up GEMM the gathered token rows as two
+// 64-wide sub-tiles in shared memory).  The MMA issues eight instructions per
+// stage.  A Gate-Up raw slot is released by the converter warps once they have
+// read it; a Down raw slot, whose token rows the MMA reads, when that MMA
+// completes; a converted slot likewise.  The raw ring is as deep as shared
+// memory allows because in the decode regime the weight stream is what the
+// kernel waits on.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -34,9 +39,11 @@ constexpr int kW8RawHalf = kTileM * 64;  // one 64-wide K half of a stage, 64-by
 constexpr int kW8RawA = 2 * kW8RawHalf;  // e4m3 weight stage: 128 rows x 128 K
 constexpr int kW8Budget = 214 * 1024;    // both rings
 
-__host__ __device__ constexpr int w8_conv_slots(int) { return 2; }
+// converted slots: A operands in tensor memory (64 columns each, next to the
+// accumulators), plus shared memory for the Gate-Up's gathered token rows
+__host__ __device__ constexpr int w8_conv_slots(int bn) { return bn <= 64 ? 4 : 2; }
 __host__ __device__ constexpr int w8_conv_slot_bytes(int bn, int bsrc) {
-  return 2 * kABytes + (bsrc == kGather ? 2 * bn * kKBytes : 0);
+  return bsrc == kGather ? 2 * bn * kKBytes : 0;
 }
 __host__ __device__ constexpr int w8_raw_slot_bytes(int bn, int bsrc) {
   return kW8RawA + (bsrc == kDirect ? 2 * bn * kKBytes : 0);
@@ -54,7 +61,7 @@ struct W8Shape {
   static constexpr int kBBytes = BN * kKBytes;            // one 64-wide token sub-tile
   static constexpr int kRawB = BSRC == kDirect ? 2 * kBBytes : 0;   // token rows (Down)
   static constexpr int kRawSlot = w8_raw_slot_bytes(BN, BSRC);
-  static constexpr int kConvSlot = w8_conv_slot_bytes(BN, BSRC);   // 2 bf16 sub-tiles (+ rows)
+  static constexpr int kConvSlot = w8_conv_slot_bytes(BN, BSRC);   // Gate-Up token rows
   static constexpr int kRawSlots = w8_raw_slots(BN, BSRC);
   static constexpr int kConvSlots = w8_conv_slots(BN);
   static constexpr int kEpiWarps = 4;
@@ -70,7 +77,8 @@ struct W8Shape {
   static constexpr int kWarps = kThreads / 32;
   static constexpr int kRowsPerGatherThread = kGatherWarps ? BN / (4 * kGatherWarps) : 1;
   static constexpr int kAccBufs = (512 / BN < 2) ? 1 : 2;
-  static constexpr int kTmemCols = (kAccBufs * BN < 32) ? 32 : kAccBufs * BN;
+  static constexpr int kACol0 = kAccBufs * BN;   // TMEM column of converted slot 0
+  static constexpr int kTmemCols = 512;
   static constexpr uint32_t kIdesc = mma_idesc(1u, kTileM, BN);   // bf16 x bf16 -> fp32
   static constexpr int kOffConv = kRawSlots * kRawSlot;
   static constexpr int kOffBar = kOffConv + kConvSlots * kConvSlot;
@@ -78,6 +86,8 @@ struct W8Shape {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr size_t kSmemBytes = 1024 + ((kOffMisc + 16 + 15) & ~15);
   static_assert(kRawSlot % 1024 == 0 && kConvSlot % 1024 == 0, "slots keep 1024-byte alignment");
+  static_assert(kACol0 + kConvSlots * 64 <= kTmemCols, "accumulators and A slots fit TMEM");
+  static_assert(kConvWarps == 4 || kConvWarps == 8, "converter warps cover the four lane quadrants");
   static_assert(kRawSlots >= 3, "raw ring too shallow");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
@@ -251,20 +261,20 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
             ok = false;
             break;
           }
-          tc_fence_after();
-          fence_proxy_async_smem();   // converted tile and gathered rows: generic-proxy writes
+          tc_fence_after();   // the converted A slot: tcgen05.st of other threads
+          if (BSRC == kGather) fence_proxy_async_smem();   // gathered rows: generic-proxy writes
           const uint32_t conv = sConv + cs * S::kConvSlot;
           const uint32_t d = tmem_base + static_cast<uint32_t>(ab * BN);
+          const uint32_t a_tm = tmem_base + static_cast<uint32_t>(S::kACol0 + cs * 64);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {   // the stage's two 64-wide sub-tiles
-            const uint64_t adesc = smem_desc_sw128(conv + h * kABytes);
+          for (int h = 0; h < 2; ++h) {   // the stage's two 64-wide halves of K
             const uint64_t bdesc = smem_desc_sw128(
-                BSRC == kGather ? conv + 2 * kABytes + h * S::kBBytes
+                BSRC == kGather ? conv + h * S::kBBytes
                                 : sRaw + rs * S::kRawSlot + kW8RawA + h * S::kBBytes);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc,
-                       (kt > w.kt0 || h > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k)   // 16 of K: 8 columns of A
+              mma_bf16_tmem_a(d, a_tm + static_cast<uint32_t>(h * 32 + k * 8), bdesc + 2 * k,
+                              idesc, (kt > w.kt0 || h > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(bar_cempty + 8 * cs);
           if (BSRC != kGather) tc_commit(bar_rempty + 8 * rs);
@@ -355,17 +365,24 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
     }
   } else if (warp < S::kGatherBase / 32) {
     // ------------------------------------------------------------ converters
-    // A stage has 1024 items (half h, row, 16-byte chunk c of the 64-byte
-    // half-row): item j = t + NT i (NT converter threads) is c = j % 4, row
-    // (j / 4) % 128, h = j / 512.  Eight consecutive threads read two whole
-    // 64-byte rows of one half (128 contiguous bytes) and write two swizzled
-    // bf16 rows whose chunks fall in disjoint banks.  All of a thread's rows
-    // sit at the same place in their 32-row quadrant (NT / 4 is a multiple of
-    // 32), so they share one block scale: Down's, or the gate or up scale.
-    constexpr int kItems = 1024 / S::kConvThreads;
+    // Lane l of a converter warp owns weight row r = 32 (warp % 4) + l of the
+    // stage's 128-row tile (the TMEM lanes this warp may write) and converts
+    // K half(s) kh of it: 64 e4m3 bytes, four 16-byte chunks read from the
+    // 64-byte-swizzled raw half (chunk c of row r sits at c ^ ((r >> 1) & 3),
+    // so a warp's 32 rows spread over eight bank groups), into 32 columns of
+    // packed bf16 written with one tcgen05.st.  Eight warps: one K half each
+    // (two warps per lane quadrant); four: both halves.  A row's block scale
+    // is Down's, or (Gate-Up: rows 16..31 of each 32-row group are up rows)
+    // the gate or up scale.
+    constexpr int kHalves = S::kConvWarps == 8 ? 1 : 2;
+    const int cw = warp - S::kRoleThreads / 32;   // converter warp 0..kConvWarps-1
+    const int quad = warp & 3;
+    const int kh0 = S::kConvWarps == 8 ? (cw >> 2) : 0;
+    const int r = quad * 32 + lane;
+    const int rsw = (r >> 1) & 3;
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    const bool up_rows = BSRC == kGather && lane >= 16;
     const int t = threadIdx.x - S::kRoleThreads;
-    const int c4 = t & 3;
-    const bool up_rows = BSRC == kGather && ((t >> 2) & 31) >= 16;
     const int KB = p.kt_total;      // 128-wide K blocks = stages
     int rs = 0, cs = 0;
     uint32_t rph = 0, cph = 0;
@@ -388,22 +405,24 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
           ok = false;
           break;
         }
-        const uint8_t* raw = smem + rs * S::kRawSlot;
-        uint8_t* conv = smem + S::kOffConv + cs * S::kConvSlot;
+        const uint8_t* raw = smem + rs * S::kRawSlot + r * 64;
 #pragma unroll
-        for (int i = 0; i < kItems; ++i) {
-          const int j = t + S::kConvThreads * i;
-          const int rr = (j >> 2) & 127;   // tile row
-          const int h = j >> 9;            // K half
-          const uint4 q = *reinterpret_cast<const uint4*>(raw + h * kW8RawHalf + rr * 64 + c4 * 16);
-          uint4 lo, hi;
-          dequant16_bf16(q, sc, lo, hi);
-          const int c0 = 2 * c4, sw = rr & 7;
-          uint8_t* sub = conv + h * kABytes + rr * kKBytes;
-          *reinterpret_cast<uint4*>(sub + ((c0 ^ sw) << 4)) = lo;
-          *reinterpret_cast<uint4*>(sub + (((c0 + 1) ^ sw) << 4)) = hi;
+        for (int hh = 0; hh < kHalves; ++hh) {
+          const int kh = kh0 + hh;
+          uint32_t col[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 q =
+                *reinterpret_cast<const uint4*>(raw + kh * kW8RawHalf + ((c ^ rsw) << 4));
+            uint4 lo, hi;
+            dequant16_bf16(q, sc, lo, hi);
+            col[8 * c + 0] = lo.x, col[8 * c + 1] = lo.y, col[8 * c + 2] = lo.z, col[8 * c + 3] = lo.w;
+            col[8 * c + 4] = hi.x, col[8 * c + 5] = hi.y, col[8 * c + 6] = hi.z, col[8 * c + 7] = hi.w;
+          }
+          tmem_st32(t_row + static_cast<uint32_t>(S::kACol0 + cs * 64 + kh * 32), col);
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();   // the MMA thread reads the slot after its wait
         mbar_arrive(bar_cfull + 8 * cs);
         if (BSRC == kGather) {
           // this warp's reads of the raw slot are done (their values were used)
@@ -448,7 +467,7 @@ __global__ void __launch_bounds__(W8Shape<BN, BSRC>::kThreads, 1)
           break;
         }
         // the stage's 128 K of each row: two 128-byte halves, one per sub-tile
-        const uint32_t b_dst = sConv + cs * S::kConvSlot + 2 * kABytes;
+        const uint32_t b_dst = sConv + cs * S::kConvSlot;
         const uint8_t* src = rows + static_cast<size_t>(kt) * 2 * kKBytes;
 #pragma unroll
         for (int h = 0; h < 2; ++h)

@@ -477,12 +477,13 @@ bool make_map_3d(CUtensorMap* m, const void* base, int esize, uint64_t cols, uin
   if (!fn) return false;
   const cuuint64_t dims[3] = {cols, rows, experts};
   const cuuint64_t strides[2] = {cols * esize, cols * rows * esize};
-  // raw64: 64-byte rows, no swizzle (e4m3 weight stages of the w8a16 GEMM)
+  // raw64: 64-byte rows with the 64-byte swizzle (e4m3 weight stages of the
+  // w8a16 GEMM, read a row per converter thread)
   const cuuint32_t box[3] = {static_cast<cuuint32_t>((raw64 ? 64 : 128) / esize), box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            raw64 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+            raw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -502,7 +503,7 @@ bool make_map_gateup(CUtensorMap* m, const void* base, int esize, uint64_t cols,
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            raw64 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+            raw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
