@@ -237,13 +237,17 @@ __device__ __forceinline__ void index_scatter(const int32_t* src, int tk, int E,
   }
 }
 
-// Padding rows of every expert interval (a thread per expert: fewer than bm
-// rows each), then the tail [offs[E], rows_end).
+// Padding rows of every expert interval (fewer than bm each), a warp per
+// expert with its lanes on consecutive rows, then the tail [offs[E],
+// rows_end).  (A thread per expert wrote its padding row by row: with
+// 256-row tiles up to 255 stores each, 32 scattered rows per warp store —
+// 13 us of the index scan kernel at the Qwen3-shaped T=4096.)
 template <class PadFn>
 __device__ __forceinline__ void index_pads(int E, int rows_end, const IndexScratch& sc, PadFn pad) {
   const int tid = threadIdx.x, nthreads = blockDim.x;
-  for (int e = tid; e < E; e += nthreads)
-    for (int pos = sc.offs[e] + sc.tot[e]; pos < sc.offs[e + 1]; ++pos) pad(pos);
+  const int lane = tid & 31, nwarps = nthreads >> 5;
+  for (int e = tid >> 5; e < E; e += nwarps)
+    for (int pos = sc.offs[e] + sc.tot[e] + lane; pos < sc.offs[e + 1]; pos += 32) pad(pos);
   for (int pos = sc.offs[E] + tid; pos < rows_end; pos += nthreads) pad(pos);
 }
 

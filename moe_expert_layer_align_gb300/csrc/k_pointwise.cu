@@ -301,6 +301,72 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
+// Unsplit Down GEMM (bf16 rows, one per assignment): a thread takes eight
+// columns, one 16-byte load per row, and has all of a token's (up to eight)
+// rows in flight as raw bf16 before reducing them in j order — one index
+// load and one row load latency per token instead of two each for batches of
+// four (the fp32 kernel converts rows on load and keeps float4s, twice the
+// registers per row).
+constexpr int kCombineRows = 8;
+__global__ void __launch_bounds__(kCombineThreads)
+    moe_combine_rows_kernel(const __nv_bfloat16* __restrict__ Y, int rows_cap, int H,
+                            const int32_t* __restrict__ inv_pos, const float* __restrict__ topk_w,
+                            int T, int k, int k_routed, float w_shared, void* __restrict__ out,
+                            int out_bf16) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x;
+  const int h = (blockIdx.y * kCombineThreads + threadIdx.x) * 8;
+  if (h >= H) return;   // H % 8 == 0
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int j0 = 0; j0 < k; j0 += kCombineRows) {
+    int pos[kCombineRows];
+    float w[kCombineRows];
+    uint4 raw[kCombineRows];
+#pragma unroll
+    for (int b = 0; b < kCombineRows; ++b) {
+      const int j = j0 + b;
+      pos[b] = j < k ? __ldg(inv_pos + static_cast<size_t>(t) * k + j) : -1;
+      if (pos[b] >= rows_cap) pos[b] = -1;   // only rows of the index are read
+      w[b] = j < k_routed ? __ldg(topk_w + static_cast<size_t>(t) * k_routed + j)
+                          : (j < k ? w_shared : 0.f);
+    }
+#pragma unroll
+    for (int b = 0; b < kCombineRows; ++b)
+      raw[b] = pos[b] >= 0
+                   ? __ldg(reinterpret_cast<const uint4*>(Y + static_cast<size_t>(pos[b]) * H + h))
+                   : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int b = 0; b < kCombineRows; ++b) {
+      if (pos[b] < 0) continue;   // dropped assignment contributes 0
+      const uint32_t u[4] = {raw[b].x, raw[b].y, raw[b].z, raw[b].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+        acc[2 * i] = fmaf(w[b], f.x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(w[b], f.y, acc[2 * i + 1]);
+      }
+    }
+  }
+  const size_t o = static_cast<size_t>(t) * H + h;   // a multiple of 8
+  if (out_bf16) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+      pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) =
+        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  } else {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+    d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
 template <typename TY>
 cudaError_t launch_combine_t(const TY* Y, int splits, int rows_cap, int H,
                              const int32_t* inv_pos, const float* topk_w, int T, int k,
@@ -326,9 +392,12 @@ cudaError_t launch_combine(const void* Y, int y_bf16, int splits, int rows_cap, 
                            const int32_t* inv_pos, const float* topk_w, int T, int k,
                            int k_routed, float w_shared, void* out, int out_bf16,
                            cudaStream_t st, bool pdl) {
-  if (y_bf16)
-    return launch_combine_t(static_cast<const __nv_bfloat16*>(Y), 1, rows_cap, H, inv_pos,
-                            topk_w, T, k, k_routed, w_shared, out, out_bf16, st, pdl);
+  if (y_bf16) {
+    const dim3 grid(T, (H + 8 * kCombineThreads - 1) / (8 * kCombineThreads));
+    return launch_kernel(moe_combine_rows_kernel, grid, dim3(kCombineThreads), 0, st, pdl,
+                         static_cast<const __nv_bfloat16*>(Y), rows_cap, H, inv_pos, topk_w, T,
+                         k, k_routed, w_shared, out, out_bf16);
+  }
   return launch_combine_t(static_cast<const float*>(Y), splits, rows_cap, H, inv_pos, topk_w, T,
                           k, k_routed, w_shared, out, out_bf16, st, pdl);
 }
