@@ -144,19 +144,17 @@ void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int*
                   int max_splits = kMaxSplits) {
   double best = 1e300;
   int bs = 1, bk = kt_total;
-  // Large token tiles: every split adds a full fp32 partial slice of the
-  // rows, written here and re-read by the reduction, so split only as far
-  // as keeping every CTA busy for about two units needs, and at most 3 ways
-  // (measured on the Mixtral-shaped Down GEMM at T=512: 3 ways 10% faster
-  // than 1 or 7).
+  // Large token tiles: unsplit.  Every split adds a full fp32 partial slice
+  // of the rows, written here and re-read by the reduction, where an
+  // unsplit GEMM stores bf16 rows; with those, one split measured best even
+  // where it leaves SMs idle (Mixtral-shaped Down at T=512, 128 units for
+  // 152 SMs: 507 us per layer against 521 / 525 / 536 us with 2 / 3 / 4
+  // splits; T=2048: 1117 against 1125 / 1153; Qwen3- and DeepSeek-shaped
+  // prefill: 1 by 2-50 %).  (Before the bf16 rows, 3 splits were 10 % faster
+  // than 1 on that Down GEMM.)
   if (bn >= 128) {
-    const double u1 = static_cast<double>(m_tiles) * tiles;
-    int want = static_cast<int>(std::ceil(2.0 * kPlanCtas / std::max(1.0, u1)));
-    want = std::max(1, std::min(3, want));
-    while (want > 1 && (kt_total + want - 1) / want < 4) --want;
-    const int kts = (kt_total + want - 1) / want;
-    *s_out = (kt_total + kts - 1) / kts;
-    *kts_out = kts;
+    *s_out = 1;
+    *kts_out = kt_total;
     return;
   }
   for (int s = 1; s <= std::min(max_splits, kt_total); ++s) {
