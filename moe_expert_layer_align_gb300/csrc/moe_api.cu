@@ -141,7 +141,7 @@ int unit_order(int T, int k, int E, int bm, int mk) {
 // Split-K count minimising (waves of units) x (k-tiles per unit) plus the
 // cost of writing and re-reading fp32 partial rows, in k-tile units.
 void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int* kts_out,
-                  int max_splits = kMaxSplits) {
+                  int max_splits = kMaxSplits, bool large_tiles_unsplit = true) {
   double best = 1e300;
   int bs = 1, bk = kt_total;
   // Large token tiles: unsplit.  Every split adds a full fp32 partial slice
@@ -151,8 +151,9 @@ void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int*
   // 152 SMs: 507 us per layer against 521 / 525 / 536 us with 2 / 3 / 4
   // splits; T=2048: 1117 against 1125 / 1153; Qwen3- and DeepSeek-shaped
   // prefill: 1 by 2-50 %).  (Before the bf16 rows, 3 splits were 10 % faster
-  // than 1 on that Down GEMM.)
-  if (bn >= 128) {
+  // than 1 on that Down GEMM.)  The router GEMM writes fp32 partials either
+  // way and has only 2E/128 weight tiles, so it keeps the split search.
+  if (bn >= 128 && large_tiles_unsplit) {
     *s_out = 1;
     *kts_out = kt_total;
     return;
@@ -543,7 +544,7 @@ bool router_plan(int T, int H, int E, RouterPlan* r, bool fused_front) {
   const int tiles = r->rows_cap / r->bn;
   const bool wide = !fused_front && T <= kRouterWideMaxT;
   choose_split(r->mt, r->kt, tiles, r->bn, &r->splits, &r->kts,
-               wide ? kRouterMaxSplitsWide : kRouterMaxSplitsHost);
+               wide ? kRouterMaxSplitsWide : kRouterMaxSplitsHost, false);
   r->bytes = 4ull * r->splits * r->rows_cap * 2 * E;
   return true;
 }

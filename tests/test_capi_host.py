@@ -185,6 +185,17 @@ def test_routed_plan():
         moe.moe_plan_routed(moe.make_shape(64, 2048, 768, 100, 8))
 
 
+def test_router_plan_keeps_split_k_at_large_token_tiles():
+    """The expert GEMMs run 128-row token tiles unsplit; the router GEMM, whose
+    output is fp32 partials either way and whose 2E/128 weight tiles alone
+    would leave most SMs idle, keeps splitting K (router table shape: K = 4096,
+    192 experts)."""
+    for T in (96, 512, 2048):
+        rows_cap = -(-T // 128) * 128
+        one_split = 4 * rows_cap * 2 * 192
+        assert moe.moe_router_workspace_bytes(T, 4096, 192) >= 3 * one_split, T
+
+
 def test_unit_order_plan():
     """Token-tile-major where an expert's token tiles x units per tile fit one
     wave of CTAs; weight-tile-major for the Mixtral-shaped prefill Gate-Up
