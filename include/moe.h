@@ -124,7 +124,10 @@ typedef struct {
    * stages serialises them (PDL overlap is lost); use for profiling only. */
   void* stage_events[8];
   /* 1: run SiLU-and-mul as its own stage even where the plan fuses it into
-   * the Gate-Up epilogue (BF16 layer with an unsplit Gate-Up). */
+   * the Gate-Up epilogue (BF16 layer with an unsplit Gate-Up), and read the
+   * Gate-Up's gate and up sums there even where the plan has the Gate-Up
+   * epilogue store SiLU(gate)*up (FP8 layer, unsplit 128-row Gate-Up: see
+   * moe_workspace_layout.g_act_rows).  Results are the same either way. */
   int32_t separate_act;
   /* Every GEMM CTA rebuilds the routing index from the top-k ids in its
    * shared memory (T*k <= 4096 and room next to the pipeline), instead of
@@ -225,7 +228,8 @@ typedef struct {
   size_t off_xq;   /* FP8: e4m3 x            [T][H]                         */
   size_t off_xs;   /* FP8: fp32 x scales     [T][H/128]                     */
   size_t off_xs_rows; /* FP8: the same scales in index-row order [rows_cap][H/128] */
-  size_t off_g;    /* fp32 Gate-Up partials  [S1][rows_cap][2I] (0 bytes when fused_act) */
+  size_t off_g;    /* fp32 Gate-Up partials  [S1][rows_cap][2I] (0 bytes when fused_act),
+                      or fp32 SiLU(gate)*up rows [rows_cap][I] when g_act_rows */
   size_t off_a;    /* activation: bf16 [rows_cap][I] or e4m3 [rows_cap][I]  */
   size_t off_as;   /* FP8: fp32 act scales   [rows_cap][I/128]              */
   size_t off_y;    /* Down output rows (sorted): fp32 partials [S2][rows_cap][H], or
@@ -240,6 +244,9 @@ typedef struct {
   int32_t y_bf16;           /* 1: the Down GEMM is unsplit and stores bf16 rows at off_y */
   int32_t down_tile_rows;   /* Down: C of the work list it takes, 0 for the task map */
   int32_t work_cap;         /* entries of the work list (0 when there is none) */
+  int32_t g_act_rows;       /* 1: the Gate-Up epilogue stores SiLU(gate)*up in fp32 at off_g
+                               and the activation stage only quantises it (FP8 layer whose
+                               Gate-Up runs unsplit on 128-row token tiles) */
 } moe_workspace_layout;
 
 /* tiles_cap of the index for these sizes (0 on invalid arguments). */

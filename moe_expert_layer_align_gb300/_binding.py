@@ -66,7 +66,7 @@ class moe_workspace_layout(ctypes.Structure):
                            "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "off_router",
                            "off_route_counter", "total_bytes", "off_route_hist")] + [
         ("coalesce_rows", _i32), ("off_work_tiles", _sz), ("off_num_work_tiles", _sz),
-        ("y_bf16", _i32), ("down_tile_rows", _i32), ("work_cap", _i32)]
+        ("y_bf16", _i32), ("down_tile_rows", _i32), ("work_cap", _i32), ("g_act_rows", _i32)]
 
 
 def _load() -> ctypes.CDLL:
@@ -377,8 +377,8 @@ def moe_forward_routed(x, hi_lo, k, w13, w2, *, score_fn=MOE_SCORE_SOFTMAX, scal
 
 def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None, routed=False) -> dict:
     """Views of the intermediates moe_forward (moe_forward_routed with
-    routed=True) left in `workspace` (index, quantised x, Gate-Up partials,
-    activation, Down partials)."""
+    routed=True) left in `workspace` (index, quantised x, Gate-Up partials or
+    SiLU(gate)*up rows, activation, Down partials)."""
     L = moe_plan_routed(shape, opts) if routed else moe_plan(shape, opts)
     T, H, I, E, k = shape.T, shape.H, shape.I, shape.E, shape.k
     ns = opts.num_shared_experts if opts is not None else 0
@@ -406,7 +406,9 @@ def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None, routed
         wc = L.work_cap
         out["work_tiles"] = v(L.off_work_tiles, 4 * wc, torch.int32, (wc, 4))
         out["num_work_tiles"] = v(L.off_num_work_tiles, 1, torch.int32, (1,))
-    if not L.fused_act:
+    if L.g_act_rows:
+        out["Gact"] = v(L.off_g, rc * I, torch.float32, (rc, I))   # SiLU(gate) * up
+    elif not L.fused_act:
         out["G"] = v(L.off_g, L.split_gateup * rc * 2 * I, torch.float32,
                      (L.split_gateup, rc, 2 * I))
     if fp8:

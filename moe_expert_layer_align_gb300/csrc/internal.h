@@ -53,6 +53,8 @@ struct GemmParams {
   float* out;                // [splits][rows_cap][M] fp32 partial sums
   void* act_out;             // Gate-Up, bf16, one split: SiLU(g)*u as bf16 [rows_cap][I]
                              // instead of the partial sums
+  int g_act;                 // Gate-Up, FP8 128-row token-major tile, one split: SiLU(g)*u
+                             // as fp32 rows [rows_cap][I] in `out` instead of the sums
   int rows_cap;              // rows of one split slice of `out` (and of the index)
   int32_t* dev_status;
   // Shared-memory index mode: every CTA rebuilds the routing index from the
@@ -135,6 +137,9 @@ cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* in
                            uint8_t* xq, float* xs, float* xs_rows, int rows_cap, cudaStream_t st,
                            bool pdl);
 // (inv_pos / xs_rows may be null: then only the per-token scales are written)
+// G: Gate-Up partial sums [splits][rows_cap][2I]; splits = 0: G holds the
+// rows of SiLU(gate)*up [rows_cap][I] already (FP8 only), which are only
+// quantised.
 cudaError_t launch_act(int fp8, const float* G, int splits, int rows_cap, int I,
                        const int32_t* sorted_ids, int sentinel, void* A, float* As,
                        cudaStream_t st, bool pdl);

@@ -815,7 +815,7 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
           ab = 0;
           aph ^= 1u;
         }
-      } else if (S::kTokM) {
+      } else if constexpr (S::kTokM) {
         // Token-major FP8 tile: lane n of the accumulator is token row n of
         // the tile, column j weight row j of the 128-row tile (Gate-Up: rows
         // 32q..32q+15 gate, 32q+16..32q+31 up, as the weight map stages
@@ -881,7 +881,34 @@ __device__ __forceinline__ void gemm_cta(const CUtensorMap& tmA, const CUtensorM
           }
         }
         if (!ok) break;
-        if (n < w.rows) {
+        if (BSRC == kGather && p.g_act) {
+          // SiLU(gate)*up: column group g (16 gate rows) and g + 1 (the up
+          // rows of the same 16 channels) give 16 values of the token's row
+          // of I, stored as fp32 (the activation stage quantises them).
+          static_assert(kWarpCols % 32 == 0, "a warp's columns hold whole gate/up pairs");
+          if (n < w.rows) {
+            float* arow = p.out + static_cast<size_t>(w.row0 + n) * p.I;
+#pragma unroll
+            for (int g = 0; g < kWarpCols / 16; g += 2) {
+              const int feat = w.mt * 64 + 16 * ((c_base + g * 16) >> 5);
+              if (feat + 16 <= p.I) {
+                float av[16];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  float g0, g1, u0, u1;
+                  unpack_f32x2(acc2[g * 8 + q], g0, g1);
+                  unpack_f32x2(acc2[(g + 1) * 8 + q], u0, u1);
+                  av[2 * q] = silu_mul_fast(g0, u0);
+                  av[2 * q + 1] = silu_mul_fast(g1, u1);
+                }
+                float4* dst = reinterpret_cast<float4*>(arow + feat);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  dst[q] = make_float4(av[4 * q], av[4 * q + 1], av[4 * q + 2], av[4 * q + 3]);
+              }
+            }
+          }
+        } else if (n < w.rows) {
           float* orow = p.out + (static_cast<size_t>(w.ks) * p.rows_cap + w.row0 + n) * p.M;
 #pragma unroll
           for (int g = 0; g < kWarpCols / 16; ++g) {

@@ -95,14 +95,13 @@ cudaError_t launch_quant_x(const void* x, int T, int H, int k, const int32_t* in
 //   g = sum_s G[s][p][i], u = sum_s G[s][p][I + i] (split-K partials in order)
 //   a = SiLU(g) * u = g / (1 + exp(-g)) * u
 // BF16: A[p][i] = bf16(a).  FP8: per 128 channels s = amax/448, codes e4m3.
+// FP8 with no splits: the unsplit token-major Gate-Up stored a itself
+// (G = [rows_cap][I], the same silu_mul_fast), so only the quantisation runs.
 // SiLU with the fast exponential and division intrinsics (relative error
 // ~1e-6, far below the bf16 rounding of a bf16 result and the e4m3 step of
-// an FP8 one; a very negative g still gives 0), as in the GEMM epilogues:
-// with expf and an IEEE division the kernel was compute-bound (DeepSeek-
-// shaped T=4096: 165 us for 670 MB of traffic).
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
-}
+// an FP8 one), as in the GEMM epilogues: with expf and an IEEE division the
+// kernel was compute-bound (DeepSeek-shaped T=4096: 165 us for 670 MB of
+// traffic).
 
 constexpr int kActThreads = 256;
 
@@ -133,27 +132,34 @@ __global__ void __launch_bounds__(kActThreads, 4)
   for (int pb = blockIdx.x * rows_per; pb < rows_cap; pb += gridDim.x * rows_per) {
     const int p = pb + my_row;
     if (p >= rows_cap || __ldg(sorted_ids + p) >= sentinel) continue;   // padding row
-    const float* row = G + static_cast<size_t>(p) * two_i;
+    const float* row = G + static_cast<size_t>(p) * (splits ? two_i : static_cast<size_t>(I));
     for (int c = c_first; c < chunks; c += c_step) {
       const int i = 8 * c;
-      float g[8], u[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) g[j] = u[j] = 0.f;
-#pragma unroll 4
-      for (int sp = 0; sp < splits; ++sp) {
-        const float* r = row + sp * slice + i;
-        const float4 g0 = __ldg(reinterpret_cast<const float4*>(r));
-        const float4 g1 = __ldg(reinterpret_cast<const float4*>(r + 4));
-        const float4 u0 = __ldg(reinterpret_cast<const float4*>(r + I));
-        const float4 u1 = __ldg(reinterpret_cast<const float4*>(r + I + 4));
-        g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
-        g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
-        u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
-        u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
-      }
       float v[8];
+      if (FP8 && splits == 0) {   // SiLU(gate)*up stored by the Gate-Up epilogue
+        const float4 a0 = __ldg(reinterpret_cast<const float4*>(row + i));
+        const float4 a1 = __ldg(reinterpret_cast<const float4*>(row + i + 4));
+        v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+        v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+      } else {
+        float g[8], u[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = silu_mul(g[j], u[j]);
+        for (int j = 0; j < 8; ++j) g[j] = u[j] = 0.f;
+#pragma unroll 4
+        for (int sp = 0; sp < splits; ++sp) {
+          const float* r = row + sp * slice + i;
+          const float4 g0 = __ldg(reinterpret_cast<const float4*>(r));
+          const float4 g1 = __ldg(reinterpret_cast<const float4*>(r + 4));
+          const float4 u0 = __ldg(reinterpret_cast<const float4*>(r + I));
+          const float4 u1 = __ldg(reinterpret_cast<const float4*>(r + I + 4));
+          g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
+          g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
+          u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
+          u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = silu_mul_fast(g[j], u[j]);
+      }
       if (FP8) {
         float amax = 0.f;
 #pragma unroll

@@ -61,6 +61,7 @@ struct Plan {
   int s2, kts2, kt2, mt2;  // Down
   int me1, me2;            // weight tiles per work unit (2: large token tiles, bf16)
   int fused_act;           // SiLU-and-mul in the Gate-Up epilogue
+  int g_act;               // the Gate-Up epilogue stores SiLU(gate)*up in fp32 (FP8)
   int ord1, ord2;          // unit order per GEMM: 1 weight-tile-major, 2 token-tile-major
   int smem_index;          // GEMM CTAs rebuild the index in shared memory
   size_t off[kNumOff];
@@ -305,6 +306,13 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     p->s2 = (p->kt2 + p->kts2 - 1) / p->kts2;
   }
   p->fused_act = !p->fp8 && p->s1 == 1 && !(o && o->separate_act);
+  // FP8, unsplit 128-row (token-major) Gate-Up: each epilogue thread holds
+  // its token's gate and up sums of the same channels, so it stores
+  // SiLU(gate)*up, I fp32 values a row instead of 2I, and the activation
+  // stage only quantises (DeepSeek-shaped T=4096: 268 MB less written and
+  // read back).  The quantisation needs all 128 channels of a group, which
+  // span two units, so it stays a separate stage.
+  p->g_act = p->fp8 && p->bn1 == 128 && p->s1 == 1 && !(o && o->separate_act);
   // An unsplit Down GEMM stores its rows in bf16 (the combine's input), half
   // the bytes of fp32 partials written and read back (prefill: 268 MB of
   // fp32 rows at the Qwen3-shaped T=4096)
@@ -364,7 +372,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
       p->fp8 ? static_cast<size_t>(s->T) * s->H : 0,
       p->fp8 ? 4 * static_cast<size_t>(s->T) * (s->H / 128) : 0,
       p->fp8 ? 4 * rc * (s->H / 128) : 0,
-      p->fused_act ? 0 : 4 * static_cast<size_t>(p->s1) * rc * 2 * s->I,
+      p->fused_act ? 0 : p->g_act ? 4 * rc * s->I : 4 * static_cast<size_t>(p->s1) * rc * 2 * s->I,
       rc * s->I * (p->fp8 ? 1 : 2),
       p->fp8 ? 4 * rc * (s->I / 128) : 0,
       (p->y16 ? 2 : 4 * static_cast<size_t>(p->s2)) * rc * s->H,
@@ -393,6 +401,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->grid_gateup = kPlanCtas;
   L->grid_down = kPlanCtas;
   L->fused_act = p.fused_act;
+  L->g_act_rows = p.g_act;
   L->smem_index = p.smem_index;
   L->weight_tiles_per_unit = p.me1 | (p.me2 << 8);
   L->off_counts = p.off[kOffCounts];
@@ -825,6 +834,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
                   ip.num_tiles};
   g1.out = G;
   g1.act_out = p.fused_act ? A : nullptr;
+  g1.g_act = p.g_act;
   g1.rows_cap = p.rows_cap;
   g1.dev_status = dev_status;
   g1.pipe_wait_ns = wait_ns;
@@ -836,7 +846,8 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
 
   record(opts, 3, s);
   if (!p.fused_act) {
-    e = launch_act(p.fp8, G, p.s1, p.rows_cap, p.I, ip.sorted_ids, tk, A, As, s, pdl);
+    e = launch_act(p.fp8, G, p.g_act ? 0 : p.s1, p.rows_cap, p.I, ip.sorted_ids, tk, A, As, s,
+                   pdl);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
 

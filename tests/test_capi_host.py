@@ -185,6 +185,25 @@ def test_routed_plan():
         moe.moe_plan_routed(moe.make_shape(64, 2048, 768, 100, 8))
 
 
+def test_fp8_silu_rows_plan():
+    """FP8 layers whose Gate-Up runs unsplit on 128-row token tiles store
+    SiLU(gate)*up (I fp32 values a row) instead of the gate and up sums (2I);
+    separate_act, forced splits, decode tiles and bf16 layers keep the sums."""
+    ds = moe.make_shape(4096, 7168, 2048, 256, 8, 0, True)
+    L = moe.moe_plan(ds)
+    assert (L.block_m, L.split_gateup, L.g_act_rows, L.fused_act) == (128, 1, 1, 0)
+    assert L.off_a - L.off_g >= 4 * L.rows_cap * 2048
+    sep = moe.make_opts(separate_act=True)
+    assert moe.moe_plan(ds, sep).g_act_rows == 0
+    grow = moe.moe_workspace_bytes(ds, sep) - moe.moe_workspace_bytes(ds)
+    assert abs(grow - 4 * L.rows_cap * 2048) < 256            # the half of G it no longer needs
+    assert moe.moe_plan(ds, moe.make_opts(split_gateup=2)).g_act_rows == 0
+    assert moe.moe_plan(moe.make_shape(64, 7168, 2048, 256, 8, 0, True)).g_act_rows == 0
+    assert moe.moe_plan(moe.make_shape(4096, 2048, 768, 128, 8, 0)).g_act_rows == 0
+    w8 = moe.make_shape(4096, 7168, 2048, 256, 8, 0, mode=moe.MOE_W8A16)
+    assert moe.moe_plan(w8).g_act_rows == 0
+
+
 def test_router_plan_keeps_split_k_at_large_token_tiles():
     """The expert GEMMs run 128-row token tiles unsplit; the router GEMM, whose
     output is fp32 partials either way and whose 2E/128 weight tiles alone

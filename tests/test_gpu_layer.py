@@ -149,6 +149,40 @@ def test_intermediates_fp8_codes(smem_index, H, I):
     assert n_diff <= max(2, wl.T * wl.k * wl.I // 2000), n_diff
 
 
+@pytest.mark.parametrize("T,kw", [(300, dict(H=512, I=384, E=4, k=2)),
+                                  (150, dict(H=384, I=256, E=3, k=3))])
+def test_fp8_gateup_stores_silu_rows(T, kw):
+    """FP8 on 128-row token tiles: the unsplit Gate-Up's epilogue stores the
+    rows of SiLU(gate)*up and the activation stage only quantises them.  The
+    codes, scales and layer output are bitwise those of the path that stores
+    the gate and up sums instead (separate_act), the stored rows are SiLU of
+    those sums, and the output matches the oracle."""
+    import moe_expert_layer_align_gb300 as moe
+    wl = small(4, T, **kw)
+    shape = moe.layer_shape(wl.x, wl.w13q, wl.topk_ids, 0, torch.bfloat16)
+    res = {}
+    for sep in (False, True):
+        opts = moe.make_opts(separate_act=sep)
+        ws = torch.zeros(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
+        out = run_layer(wl, workspace=ws, opts=opts)
+        torch.cuda.synchronize()
+        res[sep] = (out, moe.workspace_views(ws, shape, opts))
+    (o1, v1), (o0, v0) = res[False], res[True]
+    L = v1["layout"]
+    assert (L.block_m, L.split_gateup, L.g_act_rows, v0["layout"].g_act_rows) == (128, 1, 1, 0)
+    assert torch.equal(o1, o0)
+    sid = v1["sorted_ids"].cpu().numpy()
+    rows = np.flatnonzero(sid < wl.T * wl.k)
+    for n in ("A", "As"):
+        np.testing.assert_array_equal(v1[n].cpu().numpy()[rows], v0[n].cpu().numpy()[rows], n)
+    I = wl.I
+    G = v0["G"][0].double().cpu().numpy()[rows]
+    ref = G[:, :I] / (1 + np.exp(-G[:, :I])) * G[:, I:]
+    got = v1["Gact"].double().cpu().numpy()[rows]
+    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6 * np.abs(ref).max())
+    assert_layer_close(o1.float().cpu().numpy(), oracle_layer(wl), "fp8", "SiLU rows")
+
+
 @pytest.mark.parametrize("smem_index", [False, True])
 def test_invalid_ids_contribute_zero_and_are_flagged(smem_index):
     import moe_expert_layer_align_gb300 as moe
