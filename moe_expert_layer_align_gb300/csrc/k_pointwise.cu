@@ -129,9 +129,16 @@ __global__ void __launch_bounds__(kActThreads, 4)
   const int lane = threadIdx.x & 31;
   const uint32_t half_mask = lane < 16 ? 0x0000ffffu : 0xffff0000u;
   if (my_row >= rows_per) return;   // threads past rows_per whole rows
-  for (int pb = blockIdx.x * rows_per; pb < rows_cap; pb += gridDim.x * rows_per) {
-    const int p = pb + my_row;
-    if (p >= rows_cap || __ldg(sorted_ids + p) >= sentinel) continue;   // padding row
+  // The next row's sorted id is loaded while this row is processed, so an
+  // iteration waits on one load latency (the row's), not two.
+  const int stride = gridDim.x * rows_per;
+  int p = blockIdx.x * rows_per + my_row;
+  int sid = p < rows_cap ? __ldg(sorted_ids + p) : sentinel;
+  for (; p < rows_cap; p += stride) {
+    const int sid_next = p + stride < rows_cap ? __ldg(sorted_ids + p + stride) : sentinel;
+    const bool padding = sid >= sentinel;
+    sid = sid_next;
+    if (padding) continue;
     const float* row = G + static_cast<size_t>(p) * (splits ? two_i : static_cast<size_t>(I));
     for (int c = c_first; c < chunks; c += c_step) {
       const int i = 8 * c;
