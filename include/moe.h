@@ -197,8 +197,9 @@ typedef struct {
    * layers with 128 or more rows per active expert): 128 makes the Down GEMM
    * take each expert's rows in tiles of up to 128 (a work list over the same
    * index) with the 128-row tile instead of the 256-row token-major one;
-   * -1 keeps the 256-row tiles; 0: planner.  Other values: MOE_ERR_ARG.
-   * Results do not depend on it. */
+   * -1 keeps the 256-row tiles; 0: planner (128-row tiles from 256 rows per
+   * active expert on average).  Other values: MOE_ERR_ARG.  Results do not
+   * depend on it. */
   int32_t down_tile_rows;
 } moe_forward_opts;
 

@@ -29,8 +29,8 @@ constexpr int kSplitIndexMinAssignments = 2048;
 // (0: none).
 constexpr int kPlanCoalesce = 0;
 // 256-row token tiles: the planner gives the Down GEMM 128-row tiles of a
-// work list where I (its K) is at most this (0: never).
-constexpr int kPlanDownSplitMaxI = 0;
+// work list where an active expert holds at least this many rows on average.
+constexpr int kPlanDownSplitMinRows = 256;
 // Router GEMM split-K count bound: one top-k warp per token sums at most 4
 // partials at once; the block top-k (few tokens) up to 32.
 constexpr int kRouterMaxSplitsHost = 4;
@@ -99,10 +99,16 @@ int64_t tiles_cap_of(int64_t T, int64_t k, int64_t E, int64_t bm) {
 // (Mixtral-shaped layer at T=2048: 1366 -> 1248 us; T=512, 128 rows per
 // expert: 576 -> 527 us; Qwen3-shaped T=4096, 256 +- 16 rows: 445 -> 422 us;
 // at 64 rows, Qwen3-shaped T=1024, it measured 279 -> 284 us).
-int auto_bm(int T, int k, int E, int fp8, bool pair) {
+// Mean rows of an active expert: T*k assignments over the experts that
+// uniform routing is expected to reach.
+double mean_rows(int T, int k, int E) {
   const double tk = static_cast<double>(T) * k;
   const double active = E * (1.0 - std::pow(1.0 - static_cast<double>(k) / E, T));
-  const double mean = tk / std::max(1.0, std::min(active, tk));
+  return tk / std::max(1.0, std::min(active, tk));
+}
+
+int auto_bm(int T, int k, int E, int fp8, bool pair) {
+  const double mean = mean_rows(T, k, E);
   if (!fp8 && pair && mean >= 128) return 256;
   const int cap = 128;
   int bm = 16;
@@ -258,12 +264,18 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   p->co1 = p->co2 = p->co;
   // 256-row token-major tiles: the Down GEMM may instead take the experts'
   // rows in tiles of up to 128 (a work list over the same index) with the
-  // 128-row swap-AB tile.
+  // 128-row swap-AB tile and its two accumulator sets, whose epilogue
+  // overlaps the next unit's MMAs.  The planner does so from 256 rows per
+  // active expert (Qwen3-shaped T=4096: 404 -> 394 us; Mixtral-shaped
+  // T=2048, 512 rows: 1144 -> 1104 us); at 128 rows the 256 x 256 tile is
+  // faster (Qwen3-shaped T=2048: 296 against 302 us; Mixtral-shaped T=512:
+  // 509 against 568 us).
   if (o && !(o->down_tile_rows == 0 || o->down_tile_rows == -1 || o->down_tile_rows == 128))
     return MOE_ERR_ARG;
   if (p->bm == 256) {
     const int want = o ? o->down_tile_rows : 0;
-    const bool split = want == 128 || (want == 0 && s->I <= kPlanDownSplitMaxI);
+    const bool split =
+        want == 128 || (want == 0 && mean_rows(p->T, p->k, p->E) >= kPlanDownSplitMinRows);
     if (split) p->co = p->co2 = 128;
   }
   p->bn1 = p->co1 ? p->co1 : p->bm;

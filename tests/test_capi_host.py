@@ -313,6 +313,11 @@ def test_down_tile_rows_option_plan():
     # 128-row tiles of an index padded to 256: up to ceil(T*k/128) + E of them
     assert L.work_cap == moe.moe_index_tiles_cap(4096, 8, 128, 128) > L.tiles_cap
     assert L.off_work_tiles + 16 * L.work_cap <= L.off_num_work_tiles < L.total_bytes
+    # the planner's choice: 128-row Down tiles from 256 rows per active expert
+    assert moe.moe_plan(s).down_tile_rows == 128                        # 256 rows
+    assert moe.moe_plan(moe.make_shape(2048, 4096, 14336, 8, 2, 0)).down_tile_rows == 128  # 512
+    assert moe.moe_plan(moe.make_shape(2048, 2048, 768, 128, 8, 0)).down_tile_rows == 0   # 128
+    assert moe.moe_plan(moe.make_shape(512, 4096, 14336, 8, 2, 0)).down_tile_rows == 0    # 128
     # no effect where the index tiles are not 256 rows
     s2 = moe.make_shape(64, 2048, 768, 128, 8, 0, False, True)
     assert moe.moe_plan(s2, moe.make_opts(down_tile_rows=128)).down_tile_rows == 0
