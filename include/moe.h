@@ -111,8 +111,9 @@ typedef struct {
 } moe_scales;
 
 /* Options of moe_forward_ex (zero-initialised = defaults of moe_forward).
- * Stage events: with the shared-memory index there is no align stage (its
- * two events are recorded back to back). */
+ * Stage events: with the shared-memory index there is no align stage, and
+ * where the index launch also quantises x (see separate_quant) no x-quant
+ * stage (their two events are recorded back to back). */
 typedef struct {
   int32_t disable_pdl;      /* 1: plain stream order instead of PDL chaining */
   int32_t split_gateup;     /* 0: planner; else forced split-K count, Gate-Up */
@@ -201,6 +202,12 @@ typedef struct {
    * active expert on average).  Other values: MOE_ERR_ARG.  Results do not
    * depend on it. */
   int32_t down_tile_rows;
+  /* FP8 layers whose index is built by one CTA (T*k <= 2048, no shared-
+   * memory index): the plan quantises x on the index launch's other blocks,
+   * with per-token scales the Gate-Up looks up through the index
+   * (moe_workspace_layout.xs_by_token).  1: quantise x in its own kernel,
+   * which also writes the scales per index row.  Results are the same. */
+  int32_t separate_quant;
 } moe_forward_opts;
 
 /* Options of moe_align_ex: the same shared-expert and expert-parallel mapping
@@ -228,7 +235,8 @@ typedef struct {
   size_t off_index_scratch; /* per-chunk histograms of the split index build */
   size_t off_xq;   /* FP8: e4m3 x            [T][H]                         */
   size_t off_xs;   /* FP8: fp32 x scales     [T][H/128]                     */
-  size_t off_xs_rows; /* FP8: the same scales in index-row order [rows_cap][H/128] */
+  size_t off_xs_rows; /* FP8: the same scales in index-row order [rows_cap][H/128]
+                         (0 bytes when xs_by_token) */
   size_t off_g;    /* fp32 Gate-Up partials  [S1][rows_cap][2I] (0 bytes when fused_act),
                       or fp32 SiLU(gate)*up rows [rows_cap][I] when g_act_rows */
   size_t off_a;    /* activation: bf16 [rows_cap][I] or e4m3 [rows_cap][I]  */
@@ -248,6 +256,8 @@ typedef struct {
   int32_t g_act_rows;       /* 1: the Gate-Up epilogue stores SiLU(gate)*up in fp32 at off_g
                                and the activation stage only quantises it (FP8 layer whose
                                Gate-Up runs unsplit on 128-row token tiles) */
+  int32_t xs_by_token;      /* FP8: 1 when the Gate-Up reads the x scales per token (off_xs)
+                               and off_xs_rows is not written */
 } moe_workspace_layout;
 
 /* tiles_cap of the index for these sizes (0 on invalid arguments). */

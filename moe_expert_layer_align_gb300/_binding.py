@@ -49,7 +49,7 @@ class moe_forward_opts(ctypes.Structure):
                 ("num_shared_experts", _i32), ("shared_expert_weight", ctypes.c_float),
                 ("ep_first_expert", _i32), ("ep_num_experts", _i32), ("fuse_routing", _i32),
                 ("unit_order", _i32), ("pipeline_wait_ns", _i32), ("coalesce_rows", _i32),
-                ("down_tile_rows", _i32)]
+                ("down_tile_rows", _i32), ("separate_quant", _i32)]
 
 
 class moe_align_opts(ctypes.Structure):
@@ -66,7 +66,8 @@ class moe_workspace_layout(ctypes.Structure):
                            "off_xs_rows", "off_g", "off_a", "off_as", "off_y", "off_router",
                            "off_route_counter", "total_bytes", "off_route_hist")] + [
         ("coalesce_rows", _i32), ("off_work_tiles", _sz), ("off_num_work_tiles", _sz),
-        ("y_bf16", _i32), ("down_tile_rows", _i32), ("work_cap", _i32), ("g_act_rows", _i32)]
+        ("y_bf16", _i32), ("down_tile_rows", _i32), ("work_cap", _i32), ("g_act_rows", _i32),
+        ("xs_by_token", _i32)]
 
 
 def _load() -> ctypes.CDLL:
@@ -164,8 +165,9 @@ def make_opts(disable_pdl=False, split_gateup=0, split_down=0, grid_ctas=0,
               single_weight_tile=False, num_shared_experts=0, shared_expert_weight=0.0,
               ep_first_expert=0, ep_num_experts=0, fuse_routing=None,
               unit_order=0, pipeline_wait_ns=0, coalesce_rows=0,
-              down_tile_rows=0) -> moe_forward_opts:
+              down_tile_rows=0, separate_quant=False) -> moe_forward_opts:
     o = moe_forward_opts()
+    o.separate_quant = int(separate_quant)
     o.down_tile_rows = down_tile_rows   # 0 planner, -1 off, 128
     o.coalesce_rows = coalesce_rows   # 0 planner, -1 off, 32 / 64
     o.pipeline_wait_ns = pipeline_wait_ns
@@ -414,7 +416,8 @@ def workspace_views(workspace: torch.Tensor, shape: moe_shape, opts=None, routed
     if fp8:
         out["xq"] = v(L.off_xq, T * H, torch.uint8, (T, H))
         out["xs"] = v(L.off_xs, T * (H // 128), torch.float32, (T, H // 128))
-        out["xs_rows"] = v(L.off_xs_rows, rc * (H // 128), torch.float32, (rc, H // 128))
+        if not L.xs_by_token:
+            out["xs_rows"] = v(L.off_xs_rows, rc * (H // 128), torch.float32, (rc, H // 128))
         out["A"] = v(L.off_a, rc * I, torch.uint8, (rc, I))
         out["As"] = v(L.off_as, rc * (I // 128), torch.float32, (rc, I // 128))
     else:

@@ -127,6 +127,12 @@ struct IndexPtrs {
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                          const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st,
                          bool pdl, const IdMap& map, bool clear);
+// FP8: the same index (block 0) and, on the launch's other blocks, the e4m3
+// codes xq [T][H] and per-token scales xs [T][H/128] of x (bf16 [T][H]).
+cudaError_t launch_align_quant(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
+                               const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st,
+                               bool pdl, const IdMap& map, bool clear, const void* x, int H,
+                               uint8_t* xq, float* xs);
 // The same index built by three kernels over chunks of assignments (count,
 // scan, scatter); `scratch` holds align_split_scratch_words(T, k, E) ints.
 size_t align_split_scratch_words(int T, int k, int E);

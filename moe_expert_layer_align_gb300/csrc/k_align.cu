@@ -3,11 +3,13 @@
 // to rebuild the index in shared memory.  The algorithm is index_build.cuh's
 // (HPC-Ops × SGLang, section "MoE", fused pipeline, "routing and index
 // build"); here rows, inverse positions and the task map go to global memory.
+#include <cuda_bf16.h>
 #include <cstdint>
 
 #include "index_build.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 
@@ -17,11 +19,12 @@ namespace moe {
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignMaxStagedIds = 32768;  // ids staged in shared memory up to this many
 
-__global__ void __launch_bounds__(kAlignThreads)
-    moe_align_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int tiles_cap,
-                     IndexPtrs idx, int32_t* dev_status, int stage_ids, IdMap map,
-                     int clear_status) {
-  extern __shared__ int32_t sm[];
+// The whole index by one block (the block's threads and dynamic shared
+// memory).
+__device__ __forceinline__ void align_block(const int32_t* __restrict__ ids, int T, int k, int E,
+                                            int bm, int tiles_cap, const IndexPtrs& idx,
+                                            int32_t* dev_status, int stage_ids, const IdMap& map,
+                                            int clear_status, int32_t* sm) {
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
   IndexScratch sc;
   sc.carve(sm, nwarps, E, map.Eg != 0);
@@ -66,6 +69,48 @@ __global__ void __launch_bounds__(kAlignThreads)
   if (tid == 0 && *sc.flag && dev_status) atomicOr(dev_status, kStatusExpertId);
 }
 
+__global__ void __launch_bounds__(kAlignThreads)
+    moe_align_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm, int tiles_cap,
+                     IndexPtrs idx, int32_t* dev_status, int stage_ids, IdMap map,
+                     int clear_status) {
+  extern __shared__ int32_t sm[];
+  align_block(ids, T, k, E, bm, tiles_cap, idx, dev_status, stage_ids, map, clear_status, sm);
+}
+
+// FP8 layers: block 0 builds the index as moe_align_kernel does, the other
+// blocks quantise x meanwhile (HPC-Ops × SGLang, section "MoE": per token and
+// 128-channel group, s = amax/448, e4m3 codes), four groups per warp at a
+// time.  Neither needs the other, so one launch replaces two dependent ones
+// in front of the Gate-Up.  The scales stay per token (xs): the Gate-Up
+// looks each index row's token up in the index instead of reading a copy of
+// the scales per index row, which would need the index first.
+__global__ void __launch_bounds__(kAlignThreads)
+    moe_align_quant_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int bm,
+                           int tiles_cap, IndexPtrs idx, int32_t* dev_status, int stage_ids,
+                           IdMap map, int clear_status, const __nv_bfloat16* __restrict__ x,
+                           int H, uint8_t* __restrict__ xq, float* __restrict__ xs) {
+  extern __shared__ int32_t sm[];
+  if (blockIdx.x == 0) {
+    align_block(ids, T, k, E, bm, tiles_cap, idx, dev_status, stage_ids, map, clear_status, sm);
+    return;
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  constexpr int kWarps = kAlignThreads / 32;
+  const int G = H / 128, items = T * G;
+  const int nw = (gridDim.x - 1) * kWarps;
+  for (int i0 = (blockIdx.x - 1) * kWarps + (threadIdx.x >> 5); i0 < items; i0 += 4 * nw) {
+    int tt[4], gg[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j * nw;
+      tt[j] = i < items ? i / G : -1;
+      gg[j] = i < items ? i % G : 0;
+    }
+    quant_x_groups4_warp(x, tt, gg, H, xq, xs);
+  }
+}
+
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
                          const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st, bool pdl,
                          const IdMap& map, bool clear) {
@@ -88,6 +133,39 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int bm, int ti
   }
   return launch_kernel(moe_align_kernel, dim3(1), dim3(threads), smem, st, pdl, ids, T, k, E,
                        bm, tiles_cap, idx, dev_status, stage_ids, map, clear ? 1 : 0);
+}
+
+cudaError_t launch_align_quant(const int32_t* ids, int T, int k, int E, int bm, int tiles_cap,
+                               const IndexPtrs& idx, int32_t* dev_status, cudaStream_t st,
+                               bool pdl, const IdMap& map, bool clear, const void* x, int H,
+                               uint8_t* xq, float* xs) {
+  const int tk = T * k;
+  const int stage_ids = tk <= kAlignMaxStagedIds ? 1 : 0;
+  if (!stage_ids && !map.plain()) return cudaErrorInvalidValue;   // mapped ids are staged
+  if (H % 128 != 0) return cudaErrorInvalidValue;
+  const int threads = kAlignThreads;
+  const size_t smem =
+      sizeof(int32_t) * (((IndexScratch::words(threads / 32, E) + 3) & ~static_cast<size_t>(3)) +
+                         (stage_ids ? tk : 0));
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 64 && !configured[dev]) {
+    err = cudaFuncSetAttribute(moe_align_quant_kernel,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (err != cudaSuccess) return err;
+    configured[dev] = 1;
+  }
+  int sms = 148;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // quant blocks: a warp per four groups, at most two per SM (the warps loop)
+  const int items = T * (H / 128);
+  const int want = (items + 4 * (threads / 32) - 1) / (4 * (threads / 32));
+  const int nq = want < 2 * sms ? want : 2 * sms;
+  return launch_kernel(moe_align_quant_kernel, dim3(1 + (nq > 0 ? nq : 1)), dim3(threads), smem,
+                       st, pdl, ids, T, k, E, bm, tiles_cap, idx, dev_status, stage_ids, map,
+                       clear ? 1 : 0, static_cast<const __nv_bfloat16*>(x), H, xq, xs);
 }
 
 // ---------------------------------------------------------------- split build

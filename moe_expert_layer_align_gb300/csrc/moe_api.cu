@@ -64,6 +64,8 @@ struct Plan {
   int g_act;               // the Gate-Up epilogue stores SiLU(gate)*up in fp32 (FP8)
   int ord1, ord2;          // unit order per GEMM: 1 weight-tile-major, 2 token-tile-major
   int smem_index;          // GEMM CTAs rebuild the index in shared memory
+  int align_quant;         // FP8: x-quant on the one-CTA index kernel's other blocks
+  int xs_by_token;         // FP8: the Gate-Up reads x scales per token (no per-row copy)
   size_t off[kNumOff];
   int split_index;         // index built by the count / scan / scatter kernels
   size_t total;
@@ -368,6 +370,12 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   // single grid pays its memset, its two grid barriers and a longer tail.
   if (o && (o->fuse_routing < -1 || o->fuse_routing > 1)) return MOE_ERR_ARG;
   p->route_fused = p->routed && p->map.plain() && o && o->fuse_routing == 1;
+  // FP8 with a one-CTA index kernel: the x-quant runs on the same launch's
+  // other blocks (one launch fewer in front of the Gate-Up), with per-token
+  // scales that the Gate-Up looks up through the index.
+  p->align_quant = p->fp8 && !p->route_fused && !p->split_index && !p->smem_index &&
+                   !(o && o->separate_quant);
+  p->xs_by_token = p->fp8 && (p->smem_index || p->route_fused || p->align_quant);
   p->rp_owners_cap = std::min((p->T + 5) / 6, kPlanCtas);
   // workspace layout
   const size_t tk = static_cast<size_t>(p->T) * p->k;
@@ -383,7 +391,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
       p->split_index ? 4 * align_split_scratch_words(p->T, p->k, p->E) : 0,
       p->fp8 ? static_cast<size_t>(s->T) * s->H : 0,
       p->fp8 ? 4 * static_cast<size_t>(s->T) * (s->H / 128) : 0,
-      p->fp8 ? 4 * rc * (s->H / 128) : 0,
+      p->fp8 && !p->xs_by_token ? 4 * rc * (s->H / 128) : 0,
       p->fused_act ? 0 : p->g_act ? 4 * rc * s->I : 4 * static_cast<size_t>(p->s1) * rc * 2 * s->I,
       rc * s->I * (p->fp8 ? 1 : 2),
       p->fp8 ? 4 * rc * (s->I / 128) : 0,
@@ -414,6 +422,7 @@ void fill_layout(const Plan& p, moe_workspace_layout* L) {
   L->grid_down = kPlanCtas;
   L->fused_act = p.fused_act;
   L->g_act_rows = p.g_act;
+  L->xs_by_token = p.xs_by_token;
   L->smem_index = p.smem_index;
   L->weight_tiles_per_unit = p.me1 | (p.me2 << 8);
   L->off_counts = p.off[kOffCounts];
@@ -794,6 +803,10 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
                            reinterpret_cast<int32_t*>(at(kOffIdxScratch)), dev_status, s, chain(),
                            p.map, rc == nullptr);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (p.align_quant) {
+    e = launch_align_quant(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s,
+                           chain(), p.map, rc == nullptr, x, p.H, xq, xs);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else if (!p.smem_index) {
     e = launch_align(topk_ids, p.T, p.k, p.E, p.bm, p.tiles_cap, ip, dev_status, s, chain(),
                      p.map, rc == nullptr);
@@ -801,7 +814,7 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   }
 
   record(opts, 1, s);
-  if (p.fp8 && !p.route_fused) {
+  if (p.fp8 && !p.route_fused && !p.align_quant) {
     // with the shared-memory index the scales stay per token (the Gate-Up
     // epilogue looks tokens up in its own index)
     e = launch_quant_x(x, p.T, p.H, p.k, p.smem_index ? nullptr : ip.inv_pos, xq, xs,
@@ -830,9 +843,8 @@ moe_status forward_impl(const Plan& p, const void* x, const void* w13, const voi
   g1.sentinel = tk;
   g1.w_scale = (p.fp8 || p.w8) ? scales->w13_scale : nullptr;
   // per-token scales where no index-ordered copy was written
-  const bool by_token = p.smem_index || p.route_fused;
-  g1.b_scale = p.fp8 ? (by_token ? xs : xs_rows) : nullptr;
-  g1.scale_by_token = by_token;
+  g1.b_scale = p.fp8 ? (p.xs_by_token ? xs : xs_rows) : nullptr;
+  g1.scale_by_token = p.xs_by_token;
   g1.smem_index = p.smem_index;
   g1.topk_ids = topk_ids;
   g1.T = p.T;

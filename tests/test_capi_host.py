@@ -185,6 +185,23 @@ def test_routed_plan():
         moe.moe_plan_routed(moe.make_shape(64, 2048, 768, 100, 8))
 
 
+def test_fp8_quant_on_index_launch_plan():
+    """FP8 layers with a one-CTA index quantise x on the index launch (scales
+    per token, no per-row copy); the chunked index, separate_quant, the
+    shared-memory index and bf16 layers keep what they had."""
+    ds = moe.make_shape(64, 7168, 2048, 256, 8, 0, True)
+    L = moe.moe_plan(ds)
+    assert L.xs_by_token == 1
+    sep = moe.make_opts(separate_quant=True)
+    assert moe.moe_plan(ds, sep).xs_by_token == 0
+    rows = 4 * L.rows_cap * (7168 // 128)                 # the per-row scales it no longer needs
+    assert abs(moe.moe_workspace_bytes(ds, sep) - moe.moe_workspace_bytes(ds) - rows) < 256
+    big = moe.make_shape(4096, 7168, 2048, 256, 8, 0, True)   # 32768 assignments: chunked index
+    assert moe.moe_plan(big).xs_by_token == 0
+    assert moe.moe_plan(ds, moe.make_opts(smem_index=True)).xs_by_token == 1
+    assert moe.moe_plan(moe.make_shape(64, 2048, 768, 128, 8, 0)).xs_by_token == 0
+
+
 def test_fp8_silu_rows_plan():
     """FP8 layers whose Gate-Up runs unsplit on 128-row token tiles store
     SiLU(gate)*up (I fp32 values a row) instead of the gate and up sums (2I);

@@ -106,17 +106,21 @@ def test_intermediates_bf16(fused, smem_index, I):
         np.testing.assert_allclose(A[p], act, rtol=1e-2, atol=1e-2 * np.abs(act).max())
 
 
-@pytest.mark.parametrize("smem_index,H,I", [(False, 512, 256), (True, 512, 256),
-                                            (False, 384, 256), (False, 2304, 256),
-                                            (False, 512, 2304)])
-def test_intermediates_fp8_codes(smem_index, H, I):
+@pytest.mark.parametrize("smem_index,sepq,H,I", [(False, False, 512, 256), (True, False, 512, 256),
+                                                 (False, True, 512, 256),
+                                                 (False, False, 384, 256), (False, True, 384, 256),
+                                                 (False, True, 2304, 256),
+                                                 (False, False, 512, 2304)])
+def test_intermediates_fp8_codes(smem_index, sepq, H, I):
     """x codes and scales bit-exact (an odd number of 128-channel groups,
-    several blocks of group pairs per token), the index bit-exact, and the
-    activation codes (rows of more than 256 eight-channel chunks) within a
-    few rounding-edge flips of the oracle's."""
+    several blocks of group pairs per token), quantised on the index launch's
+    other blocks or by their own kernel (sepq, which also writes the scales
+    per index row), the index bit-exact, and the activation codes (rows of
+    more than 256 eight-channel chunks) within a few rounding-edge flips of
+    the oracle's."""
     import moe_expert_layer_align_gb300 as moe
     wl = small(4, 20, H=H, I=I, E=6, k=3)
-    opts = moe.make_opts(smem_index=smem_index)
+    opts = moe.make_opts(smem_index=smem_index, separate_quant=sepq)
     shape = moe.layer_shape(wl.x, wl.w13q, wl.topk_ids, 0, torch.bfloat16)
     ws = torch.zeros(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8, device="cuda")
     got = run_layer(wl, workspace=ws, opts=opts).float().cpu().numpy()
@@ -128,7 +132,8 @@ def test_intermediates_fp8_codes(smem_index, H, I):
     xq, xs = oracle.quant_x(bits16(wl.x))
     np.testing.assert_array_equal(v["xq"].cpu().numpy(), xq)          # bit-exact
     np.testing.assert_array_equal(v["xs"].cpu().numpy(), xs)
-    if not smem_index:
+    assert v["layout"].xs_by_token == int(smem_index or not sepq)
+    if not v["layout"].xs_by_token:
         # the same scales scattered to the index rows that hold each token
         sid = v["sorted_ids"].cpu().numpy()
         rows = np.flatnonzero(sid < wl.T * wl.k)
@@ -147,6 +152,43 @@ def test_intermediates_fp8_codes(smem_index, H, I):
     # codes come from fp32 values that differ from the oracle's only by
     # summation order: at most a few land on the other side of a rounding edge
     assert n_diff <= max(2, wl.T * wl.k * wl.I // 2000), n_diff
+
+
+@pytest.mark.parametrize("cfg,T,kw", [(4, 1, dict(H=512, I=256, E=16)),
+                                      (4, 70, dict(H=384, I=384, E=12)),
+                                      (5, 40, dict(H=256, I=128, E=64))])
+def test_fp8_quant_on_index_launch_equals_separate_kernel(cfg, T, kw):
+    """FP8 with a one-CTA index: x quantised on the index launch's other
+    blocks (per-token scales, looked up through the index by the Gate-Up)
+    gives bitwise the codes, scales and output of the separate x-quant
+    kernel with its per-row scales; the routed layer (workload 5) too."""
+    import moe_expert_layer_align_gb300 as moe
+    wl = small(cfg, T, **kw)
+    routed = wl.wr is not None
+    hi_lo = moe.moe_router_prepare(wl.wr) if routed else None
+    ids = wl.topk_ids if not routed else torch.empty(T, wl.k)   # the shape only
+    shape = moe.layer_shape(wl.x, wl.w13q, ids, 0, torch.bfloat16)
+    res = {}
+    for sepq in (False, True):
+        opts = moe.make_opts(separate_quant=sepq)
+        if routed:
+            ws = torch.zeros(moe.moe_routed_workspace_bytes(shape, opts), dtype=torch.uint8,
+                             device="cuda")
+            out = moe.moe_forward_routed(wl.x, hi_lo, wl.k, wl.w13q, wl.w2q,
+                                         scales=(wl.w13s, wl.w2s), workspace=ws, opts=opts)[0]
+        else:
+            ws = torch.zeros(moe.moe_workspace_bytes(shape, opts), dtype=torch.uint8,
+                             device="cuda")
+            out = run_layer(wl, workspace=ws, opts=opts)
+        torch.cuda.synchronize()
+        res[sepq] = (out, moe.workspace_views(ws, shape, opts, routed=routed))
+    (o1, v1), (o0, v0) = res[False], res[True]
+    assert (v1["layout"].xs_by_token, v0["layout"].xs_by_token) == (1, 0)
+    assert torch.equal(o1, o0)
+    for n in ("xq", "xs", "sorted_ids", "inv_pos"):
+        assert torch.equal(v1[n], v0[n]), n
+    if not routed:
+        assert_layer_close(o1.float().cpu().numpy(), oracle_layer(wl), "fp8", "quant on index")
 
 
 @pytest.mark.parametrize("T,kw", [(300, dict(H=512, I=384, E=4, k=2)),
