@@ -386,10 +386,10 @@ MOE_API moe_status moe_router_topk(const void* x, const void* hi_lo, int32_t T,
                            void* stream);
 
 /* Largest workspace moe_forward_static can serve (128 MiB).  With the plans
- * of this version that covers, for example, the Mixtral-shaped bf16 layer up
- * to T=256, the Qwen3-30B-A3B-shaped layer up to T=512 and the
- * DeepSeek-V3-shaped FP8 layer up to T=8; moe_workspace_bytes(shape, NULL)
- * tells for any shape. */
+ * of this version that covers every T up to 768 for the Mixtral-shaped bf16
+ * layer, up to 912 for the Qwen3-30B-A3B-shaped layer and up to 20 for the
+ * DeepSeek-V3-shaped FP8 layer; moe_workspace_bytes(shape, NULL) tells for
+ * any shape. */
 #define MOE_STATIC_SCRATCH_BYTES ((size_t)128 << 20)
 
 /* moe_forward without a workspace argument, for callers that cannot allocate

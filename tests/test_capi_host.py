@@ -185,6 +185,19 @@ def test_routed_plan():
         moe.moe_plan_routed(moe.make_shape(64, 2048, 768, 100, 8))
 
 
+def test_static_scratch_covers_the_documented_token_counts():
+    """The header's statement of what MOE_STATIC_SCRATCH_BYTES covers with the
+    current plans: every T up to 768 / 912 / 20 for the Mixtral-, Qwen3- and
+    DeepSeek-shaped layers, and not the next token count."""
+    lim = B.STATIC_SCRATCH_BYTES
+    for (H, I, E, k, fp8), tmax in (((4096, 14336, 8, 2, False), 768),
+                                    ((2048, 768, 128, 8, False), 912),
+                                    ((7168, 2048, 256, 8, True), 20)):
+        sizes = [moe.moe_workspace_bytes(moe.make_shape(T, H, I, E, k, 0, fp8))
+                 for T in range(1, tmax + 2)]
+        assert max(sizes[:-1]) <= lim < sizes[-1], (H, tmax)
+
+
 def test_fp8_quant_on_index_launch_plan():
     """FP8 layers with a one-CTA index quantise x on the index launch (scales
     per token, no per-row copy); the chunked index, separate_quant, the
