@@ -19,6 +19,110 @@ namespace moe {
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignMaxStagedIds = 32768;  // ids staged in shared memory up to this many
 
+// Batches of at most 32 assignments with plain ids and no work list: one
+// warp holds every assignment, so the counting, ranking and offset passes of
+// index_build.cuh (and their block barriers) reduce to warp votes.  The warp
+// lists the active experts (at most 32) with their counts and padded offsets
+// in shared memory and writes the assignments' rows; after one barrier every
+// thread writes its share of counts, offsets, padding rows and the task map
+// from that list.  The index is the one index_build.cuh builds: rows of an
+// expert in ascending assignment order, offsets the exclusive prefix of the
+// counts rounded up to bm (a power of two), invalid ids dropped and flagged.
+// (At T*k = 8 and 128 experts the block passes took ~9k cycles after the
+// ids arrived, mostly barrier and shared-memory latency chains.)
+constexpr int kAlignSmallMax = 32;
+
+__device__ __forceinline__ void align_small(const int32_t* __restrict__ ids, int tk, int E,
+                                            int bm, int tiles_cap, const IndexPtrs& idx,
+                                            int32_t* dev_status, int clear_status, int32_t* sm) {
+  // sm: [0, 32) expert, [32, 64) count, [64, 96) padded offset of the active
+  // experts; [96] how many; [97] padded total; [98] an invalid id was seen
+  const int tid = threadIdx.x, lane = tid & 31;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (tid == 0 && dev_status && clear_status) *dev_status = 0;
+  if (tid < 32) {
+    // every lane loads (a valid address), then selects: a load under a
+    // condition left the warp diverged, and each of the votes and shuffles
+    // below then waited for it to reconverge (~300 cycles each at T*k = 8)
+    const bool in = lane < tk;
+    const int loaded = __ldg(ids + (in ? lane : 0));
+    const int e = in ? loaded : -1;
+    __syncwarp();
+    const bool valid = in && e >= 0 && e < E;
+    const int bits = key_bits(E);
+    const unsigned grp = peer_mask(valid ? e : (1 << bits), bits);
+    const bool leader = valid && lane == __ffs(grp) - 1;
+    const int cnt = __popc(grp);
+    const int padded = leader ? (cnt + bm - 1) & ~(bm - 1) : 0;
+    // padded offset of this lane's expert: the padded counts of the smaller
+    // active experts (one leader lane each)
+    int off = 0;
+    for (int j = 0; j < 32; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, e, j);
+      const int pj = __shfl_sync(0xffffffffu, padded, j);
+      if (pj > 0 && ej < e) off += pj;
+    }
+    int total = padded;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) total += __shfl_xor_sync(0xffffffffu, total, d);
+    const unsigned leaders = __ballot_sync(0xffffffffu, leader);
+    const bool bad = __any_sync(0xffffffffu, in && !valid);
+    if (leader) {
+      const int s = __popc(leaders & lanemask_lt());
+      sm[s] = e;
+      sm[32 + s] = cnt;
+      sm[64 + s] = off;
+    }
+    if (lane == 0) {
+      sm[96] = __popc(leaders);
+      sm[97] = total;
+      sm[98] = bad ? 1 : 0;
+    }
+    if (valid) {
+      const int pos = off + __popc(grp & lanemask_lt());
+      idx.sorted_ids[pos] = lane;
+      idx.inv_pos[lane] = pos;
+    } else if (in) {
+      idx.inv_pos[lane] = -1;
+    }
+  }
+  __syncthreads();
+  const int na = sm[96], total = sm[97];
+  for (int e = tid; e <= E; e += blockDim.x) {
+    int c = 0, o = 0;
+    for (int s = 0; s < na; ++s) {
+      const int es = sm[s], cs = sm[32 + s];
+      if (es == e) c = cs;
+      if (es < e) o += (cs + bm - 1) & ~(bm - 1);
+    }
+    if (e < E) idx.counts[e] = c;
+    idx.offsets[e] = o;   // e == E: the padded total
+  }
+  const int rows_end = tiles_cap * bm;
+  for (int r = tid; r < rows_end; r += blockDim.x) {   // rows that hold no assignment
+    bool held = false;
+    for (int s = 0; s < na; ++s) {
+      const int o = sm[64 + s];
+      held = held || (r >= o && r < o + sm[32 + s]);
+    }
+    if (!held) idx.sorted_ids[r] = tk;
+  }
+  if (tid == 0) *idx.num_tiles = total / bm;
+  for (int q = tid; q < tiles_cap; q += blockDim.x) {
+    const int row0 = q * bm;
+    int4 t = make_int4(-1, row0, 0, 0);
+    for (int s = 0; s < na; ++s) {
+      const int o = sm[64 + s], c = sm[32 + s];
+      if (row0 >= o && row0 < o + ((c + bm - 1) & ~(bm - 1)))
+        t = make_int4(sm[s], row0, min(bm, o + c - row0), 0);
+    }
+    idx.tile_expert[q] = t.x;
+    reinterpret_cast<int4*>(idx.tiles)[q] = t;
+  }
+  if (tid == 0 && sm[98] && dev_status) atomicOr(dev_status, kStatusExpertId);
+}
+
 // The whole index by one block (the block's threads and dynamic shared
 // memory).
 __device__ __forceinline__ void align_block(const int32_t* __restrict__ ids, int T, int k, int E,
@@ -33,6 +137,10 @@ __device__ __forceinline__ void align_block(const int32_t* __restrict__ ids, int
 
   const int tid = threadIdx.x;
   const int tk = T * k;
+  if (tk <= kAlignSmallMax && map.plain() && idx.coalesce == 0) {
+    align_small(ids, tk, E, bm, tiles_cap, idx, dev_status, clear_status, sm);
+    return;
+  }
 
   pdl_wait();
   pdl_launch_dependents();

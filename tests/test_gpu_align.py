@@ -82,3 +82,26 @@ def test_invalid_ids_flagged_and_dropped():
     assert ref["invalid"] == 3
     assert status == (1 << 6)                      # bit of MOE_ERR_EXPERT_ID
     assert got["inv_pos"][3 * 4 + 1] == -1
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_small_batches(seed):
+    # at most 32 assignments (and 33, the first batch past the one-warp
+    # build): random experts with repeats and invalid ids, every row tile
+    rng = np.random.default_rng(500 + seed)
+    E = int(rng.choice([1, 2, 7, 64, 128, 256, 512]))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    T = int(rng.integers(1, 32 // k + 1)) if seed % 5 else (32 // k) + 1
+    bm = int(rng.choice([16, 32, 64, 128, 256]))
+    if seed % 3 == 0:
+        ids = topk_ids(T, E, k, seed)
+    else:
+        ids = rng.integers(-2, E + 2, size=(T, k)).astype(np.int32)
+    got, status, ref = assert_index_equal(ids, E, bm)
+    assert status == (1 << 6 if ref["invalid"] else 0)
+
+
+def test_small_batch_one_expert_and_boundaries():
+    assert_index_equal(np.full((32, 1), 3, np.int32), 4, 16)       # 32 rows of one expert
+    assert_index_equal(np.full((4, 8), 511, np.int32), 512, 256)   # the last expert
+    assert_index_equal(np.arange(32, dtype=np.int32).reshape(4, 8), 32, 16)   # 32 experts
