@@ -149,8 +149,19 @@ int unit_order(int T, int k, int E, int bm, int mk) {
 
 // Split-K count minimising (waves of units) x (k-tiles per unit) plus the
 // cost of writing and re-reading fp32 partial rows, in k-tile units.
+// Fixed cost of a bf16 work unit in pipeline stages (its pipeline fill and
+// drain and its epilogue), charged per wave in choose_split.  Without it the
+// planner split the Mixtral-shaped Down (K = 14336) 7 ways at T=16..64 and
+// 16 ways at T=4: now 4 and 7 (T=64 457 -> 449 us, T=4 353 -> 339 us); the
+// Qwen3-shaped Down drops its split at T=4 and 8 (84.5 -> 80.4 us, 109.1 ->
+// 105.6 us).  FP8 and w8a16 units, whose per-K-block work is heavier, keep
+// the plain count: their split Gate-Ups at DeepSeek-shaped T=1 and 4
+// measured 2.5-4.5 % faster than the unsplit ones this cost would choose.
+constexpr double kPlanUnitCost = 4.0;
+
 void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int* kts_out,
-                  int max_splits = kMaxSplits, bool large_tiles_unsplit = true) {
+                  int max_splits = kMaxSplits, bool large_tiles_unsplit = true,
+                  double unit_cost = 0.0) {
   double best = 1e300;
   int bs = 1, bk = kt_total;
   // Large token tiles: unsplit.  Every split adds a full fp32 partial slice
@@ -176,7 +187,7 @@ void choose_split(int m_tiles, int kt_total, int tiles, int bn, int* s_out, int*
     const double grid = std::min<double>(kPlanCtas, units);
     const double waves = std::ceil(units / grid);
     const double extra = se > 1 ? 0.5 * units * bn / 16.0 / kPlanCtas : 0.0;
-    const double cost = waves * kts + extra;
+    const double cost = waves * (kts + unit_cost) + extra;
     if (cost < best - 1e-9) {
       best = cost;
       bs = se;
@@ -301,6 +312,7 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
   p->me2 = (!p->fp8 && !p->w8 && p->bm >= 128 && p->mt2 % 2 == 0 &&
              !(o && o->single_weight_tile)) ? 2 : 1;
   const int est = est_tiles(p->T, p->k, p->E, p->bm, p->tiles_cap);
+  const double unit_cost = (p->fp8 || p->w8) ? 0.0 : kPlanUnitCost;
   if (!p->fp8 && !(o && o->separate_act)) {
     // bf16 activations: an unsplit Gate-Up applies SiLU-and-mul in its
     // epilogue; measured faster than any split (whose partials then need the
@@ -308,9 +320,11 @@ moe_status make_plan(const moe_shape* s, const moe_forward_opts* o, Plan* p, boo
     p->s1 = 1;
     p->kts1 = p->kt1;
   } else {
-    choose_split(p->mt1 / p->me1, p->kt1, est, p->bm, &p->s1, &p->kts1);
+    choose_split(p->mt1 / p->me1, p->kt1, est, p->bm, &p->s1, &p->kts1, kMaxSplits, true,
+                 unit_cost);
   }
-  choose_split(p->mt2 / p->me2, p->kt2, est, p->bm, &p->s2, &p->kts2);
+  choose_split(p->mt2 / p->me2, p->kt2, est, p->bm, &p->s2, &p->kts2, kMaxSplits, true,
+               unit_cost);
   if (o && o->split_gateup > 0) {
     p->kts1 = (p->kt1 + o->split_gateup - 1) / o->split_gateup;
     p->s1 = (p->kt1 + p->kts1 - 1) / p->kts1;
