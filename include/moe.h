@@ -162,8 +162,9 @@ typedef struct {
    * the GEMM leaves free, then, after a second barrier, its block's rows of
    * the index), preceded by an 8-byte memset of its barrier counters.
    * 0 (default) or -1: as separate PDL-chained kernels (router GEMM, top-k,
-   * index, x-quant), measured faster on the Zipf-routed Qwen3-shaped FP8
-   * layer at every token count tried.  Bit-identical results. */
+   * then the index and x-quant: one launch where one CTA builds the index,
+   * see separate_quant), measured faster on the Zipf-routed Qwen3-shaped
+   * FP8 layer at every token count tried.  Bit-identical results. */
   int32_t fuse_routing;
   /* Order in which each persistent GEMM walks its work units (weight tile x
    * split x token tile).  0: planner.  1: weight-tile-major (the units of
