@@ -185,6 +185,24 @@ def test_routed_plan():
         moe.moe_plan_routed(moe.make_shape(64, 2048, 768, 100, 8))
 
 
+def test_split_counts_of_the_measured_decode_shapes():
+    """The planner's split-K counts where they were measured against the
+    alternatives: the Mixtral-shaped Down 4 ways at T=16..128 and 7 at T=4,
+    the Qwen3-shaped Down unsplit at T=1..64 (bf16 units carry a fixed
+    per-unit cost), the DeepSeek-shaped FP8 Gate-Up split 4 / 3 / 2 ways at
+    T=1 / 4 / 16 (FP8 units do not)."""
+    def splits(T, H, I, E, k, fp8):
+        L = moe.moe_plan(moe.make_shape(T, H, I, E, k, 0, fp8))
+        return L.split_gateup, L.split_down
+    for T in (16, 32, 64, 128):
+        assert splits(T, 4096, 14336, 8, 2, False) == (1, 4), T
+    assert splits(4, 4096, 14336, 8, 2, False) == (1, 7)
+    for T in (1, 4, 8, 64):
+        assert splits(T, 2048, 768, 128, 8, False) == (1, 1), T
+    for T, s1 in ((1, 4), (4, 3), (16, 2), (64, 1)):
+        assert splits(T, 7168, 2048, 256, 8, True) == (s1, 1), T
+
+
 def test_static_scratch_covers_the_documented_token_counts():
     """The header's statement of what MOE_STATIC_SCRATCH_BYTES covers with the
     current plans: every T up to 768 / 912 / 20 for the Mixtral-, Qwen3- and
